@@ -1,0 +1,143 @@
+"""The double-precision CPU oracle -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg (and its ``--impl reference`` arm) may import this package. The product
+path (``chunked_prefill_gqa_gb300``) never imports it, and it never imports the
+product path: the two share no code, header, table or constant. Inputs come
+from ``workloads.py`` and are handed to both.
+
+What it computes, and the passages it follows, is stated in
+``attn_oracle.c``: exact causal grouped-query attention of a chunk of C query
+rows at positions P..P+C-1 against keys 0..P+C-1, in double precision, two
+passes per (row, head) with the maximum taken first.
+
+The check rule of the attention-v1 oracle ("Inference Attention 2: Flash
+Prefill Against a Cached Prefix", Lesson; "Inference Attention 1: The Full
+Score Matrix", Lesson) is ``|got - ref| <= 1e-4 + 1e-3 * |ref|`` on every
+value; :func:`check` applies it, and a non-finite value always fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+ATOL = 1e-4
+RTOL = 1e-3
+
+
+def build(force: bool = False) -> str:
+    """Compile ``attn_oracle.c`` with gcc (-O2, OpenMP, no fast-math)."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c99",
+               "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _bind(lib):
+    lib.oracle_prefill.restype = ctypes.c_int
+    lib.oracle_prefill.argtypes = [
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_long, ctypes.c_long, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_double, ctypes.c_void_p, ctypes.c_long, ctypes.c_int]
+    lib.oracle_max_threads.restype = ctypes.c_int
+    lib.oracle_max_threads.argtypes = []
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = _bind(ctypes.CDLL(build()))
+    return _lib
+
+
+def load_variant(path: str):
+    """An ``attention`` callable bound to another build of the same C source.
+
+    Used by the tests that compile deliberately broken copies of the oracle to
+    show that the pins catch each mistake.
+    """
+    lib = _bind(ctypes.CDLL(path))
+    return lambda *a, **kw: _attention(lib, *a, **kw)
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+def attention(q, k, v, P: int, scale: float = 0.125, rows=None, threads: int = 0) -> np.ndarray:
+    """Exact causal GQA attention of chunk rows ``rows`` (default: all).
+
+    q is [C][HQ][D], k and v are [P + C][HKV][D], fp32. Returns float64
+    [len(rows)][HQ][D].
+    """
+    return _attention(_load(), q, k, v, P, scale, rows, threads)
+
+
+def _attention(lib, q, k, v, P, scale=0.125, rows=None, threads=0):
+    q = np.ascontiguousarray(q, dtype=np.float32)
+    k = np.ascontiguousarray(k, dtype=np.float32)
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    if q.ndim != 3 or k.ndim != 3 or v.shape != k.shape:
+        raise ValueError("q must be [C][HQ][D]; k and v [T][HKV][D] with equal shapes")
+    C, HQ, D = q.shape
+    T, HKV, Dk = k.shape
+    if Dk != D or T != P + C or HQ % HKV != 0:
+        raise ValueError(f"shape mismatch: q {q.shape}, k {k.shape}, P={P}")
+    if rows is None:
+        rows_arr = None
+        nrows = C
+    else:
+        rows_arr = np.ascontiguousarray(rows, dtype=np.int32)
+        nrows = rows_arr.size
+    out = np.empty((nrows, HQ, D), dtype=np.float64)
+    rc = lib.oracle_prefill(
+        q.ctypes.data, k.ctypes.data, v.ctypes.data, out.ctypes.data,
+        C, P, HQ, HKV, D, float(scale),
+        None if rows_arr is None else rows_arr.ctypes.data, nrows, int(threads))
+    if rc != 0:
+        raise RuntimeError(f"oracle_prefill failed with code {rc}")
+    return out
+
+
+def prefill(inp, rows=None, threads: int = 0) -> np.ndarray:
+    """The oracle on a ``workloads.Inputs`` (scale 1/8)."""
+    return attention(inp.q, inp.k, inp.v, inp.P, 0.125, rows=rows, threads=threads)
+
+
+def violations(got, ref, atol: float = ATOL, rtol: float = RTOL) -> np.ndarray:
+    """Boolean mask of elements failing |got - ref| <= atol + rtol * |ref| (NaN fails)."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    ok = np.abs(got - ref) <= atol + rtol * np.abs(ref)
+    ok &= np.isfinite(got)
+    return ~ok
+
+
+def check(got, ref, atol: float = ATOL, rtol: float = RTOL) -> dict:
+    """Apply the attention-v1 rule; report the worst element as err / tolerance."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    bad = violations(got, ref, atol, rtol)
+    with np.errstate(invalid="ignore"):
+        ratio = np.abs(got - ref) / (atol + rtol * np.abs(ref))
+    ratio = np.where(np.isfinite(got), ratio, np.inf)
+    worst = float(np.max(ratio)) if ratio.size else 0.0
+    return {"n": int(got.size), "n_bad": int(bad.sum()), "worst_ratio": worst,
+            "max_abs_err": float(np.nanmax(np.abs(got - ref))) if got.size else 0.0}

@@ -1,0 +1,101 @@
+"""The oracle against facts fixed by the pages and by the mathematics (CPU only)."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from conftest import read_golden
+from oracle_pins import ALL_PINS
+from online_model import online_rows
+
+
+@pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
+def test_oracle_pin(pin):
+    pin(oracle.attention)
+
+
+def test_worked_example_online_intermediates(golden_dir):
+    """The tile update the kernels run, replayed on the page's worked example
+    ("FlashAttention and inference kernels", Exercises 1) with tiles of two keys,
+    reproduces every intermediate the page prints."""
+    g = read_golden(f"{golden_dir}/online_softmax_worked_example.txt")
+    s = [float(x) for x in g["scores_tile1"] + g["scores_tile2"]]
+    vals = [[float(x)] for x in g["values_tile1"] + g["values_tile2"]]
+    trace = []
+    res = online_rows(s, vals, tile=2, trace=trace)
+
+    def near(x, printed):
+        decimals = len(printed.split(".")[1]) if "." in printed else 0
+        return abs(x - float(printed)) <= 1.5 * 10.0 ** (-decimals)
+
+    (m1, l1, o1), (m2, l2, o2) = trace
+    assert near(m1, g["tile1_m"][0]) and near(l1, g["tile1_l"][0]) and near(o1[0], g["tile1_O"][0])
+    assert near(m2, g["tile2_m"][0]) and near(l2, g["tile2_l"][0]) and near(o2[0], g["tile2_O"][0])
+    assert near(math.exp(m1 - m2), g["tile2_correction"][0])
+    assert near(res[0], g["result"][0])
+    w = [math.exp(x) for x in s]
+    for got, printed in zip(w, g["direct_weights"]):
+        assert abs(got - float(printed)) <= 1.5 * 10.0 ** (-(len(printed.split(".")[1])))
+    assert near(sum(w), g["direct_weight_sum"][0])
+
+
+@pytest.mark.parametrize("tile", [1, 2, 3, 64, 128])
+@pytest.mark.parametrize("stale", [None, 0.0, 8.0 * math.log(2.0)])
+def test_online_model_matches_oracle(tile, stale):
+    """Any tile width, with or without a stale reference maximum, gives the exact
+    attention of the oracle (the update is exact, page 2: "mathematically
+    identical to standard attention, not an approximation")."""
+    inp = W.tiny()
+    ref = oracle.prefill(inp, rows=[0, 8, 16])
+    for r, i in enumerate([0, 8, 16]):
+        for h in (0, 1, 5, 31):
+            g = h // 4
+            n = inp.P + i + 1
+            s = [float(np.dot(inp.q[i, h].astype(np.float64), inp.k[j, g].astype(np.float64))) * 0.125
+                 for j in range(n)]
+            vals = [list(inp.v[j, g].astype(np.float64)) for j in range(n)]
+            got = online_rows(s, vals, tile, stale_threshold=stale)
+            np.testing.assert_allclose(got, ref[r, h], rtol=1e-11, atol=1e-12)
+
+
+def test_online_model_fully_masked_tile():
+    """A tile whose scores are all -inf before any visible key leaves m at -inf and
+    produces no NaN (the teaching kernel's guard, page 2)."""
+    s = [-math.inf, -math.inf, 1.0, 2.0]
+    got = online_rows(s, [[1.0], [2.0], [3.0], [4.0]], tile=2)
+    expect = (3.0 * math.e + 4.0 * math.e ** 2) / (math.e + math.e ** 2)
+    assert abs(got[0] - expect) < 1e-12
+
+
+def test_rows_subset_matches_full():
+    inp = W.edge(33, 31)
+    full = oracle.prefill(inp)
+    rows = [32, 0, 17, 5]
+    sub = oracle.prefill(inp, rows=rows)
+    np.testing.assert_array_equal(sub, full[rows])
+
+
+def test_thread_count_does_not_change_result():
+    inp = W.edge(17, 31)
+    a = oracle.prefill(inp, threads=1)
+    b = oracle.prefill(inp, threads=4)
+    np.testing.assert_array_equal(a, b)
+
+
+def test_bad_arguments_raise():
+    inp = W.edge(4, 3)
+    with pytest.raises(ValueError):
+        oracle.attention(inp.q, inp.k, inp.v, 2)          # T != P + C
+    with pytest.raises(RuntimeError):
+        oracle.attention(inp.q, inp.k, inp.v, 3, rows=[4])  # row outside the chunk
+
+
+def test_check_rule():
+    ref = np.array([0.0, 1.0, -2.0, 10.0])
+    tol = 1e-4 + 1e-3 * np.abs(ref)
+    assert oracle.check(ref + 0.99 * tol, ref)["n_bad"] == 0
+    assert oracle.check(ref + 1.01 * tol, ref)["n_bad"] == 4
+    assert oracle.check(np.array([np.nan, 1.0, -2.0, 10.0]), ref)["n_bad"] == 1
+    assert oracle.check(np.array([np.inf, 1.0, -2.0, 10.0]), ref)["n_bad"] == 1

@@ -1,0 +1,202 @@
+"""Seeded synthetic inputs for chunked-prefill grouped-query attention.
+
+This module only makes numbers: it holds none of the attention arithmetic.
+Both the double-precision oracle (``oracle/``) and the CUDA path receive the
+arrays made here, so neither side ever generates its own inputs.
+
+Tensor shapes follow the attention-v1 contract of "Inference Attention 2:
+Flash Prefill Against a Cached Prefix" (Lesson): q is [C][32][64], kCache and
+vCache are [P + C][8][64], all fp32, row-major.
+
+Generator. Each tensor draws from its own SplitMix64 stream (Steele, Lea and
+Flood, "Fast splittable pseudorandom number generators", OOPSLA 2014): the
+n-th output is mix64(seed + (n + 1) * 0x9E3779B97F4A7C15) with the published
+mixing constants. A uniform draw keeps the top 24 bits, so every value in
+[-1, 1) is exact in fp32. Normal draws use the Box-Muller transform in double
+precision. Seeds follow the teaching program of "FlashAttention and inference
+kernels" (A working FlashAttention forward kernel): q, k and v get seeds
+s, s + 1 and s + 2; planted positions come from seed s + 3.
+
+Hazards (page 1, Lesson): a planted position t carries 4.0 in every element of
+KV head 0 of kCache and vCache, and, when t lies inside the chunk, in query
+head 0 of chunk row t - P, so a planted query meets a planted key with score
+64 * 16 / 8 = 128.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+HQ = 32          # query heads
+HKV = 8          # KV heads
+D = 64           # head dimension
+GROUP = HQ // HKV
+
+_GOLDEN = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+
+
+def splitmix64(seed: int, n: int) -> np.ndarray:
+    """The first ``n`` outputs of the SplitMix64 stream started at ``seed``."""
+    with np.errstate(over="ignore"):
+        idx = np.arange(1, n + 1, dtype=np.uint64)
+        z = np.uint64(seed & 0xFFFFFFFFFFFFFFFF) + idx * _GOLDEN
+        z = (z ^ (z >> np.uint64(30))) * _M1
+        z = (z ^ (z >> np.uint64(27))) * _M2
+        z = z ^ (z >> np.uint64(31))
+    return z
+
+
+def uniform(seed: int, n: int) -> np.ndarray:
+    """``n`` fp32 values uniform on [-1, 1), each exactly representable."""
+    top24 = (splitmix64(seed, n) >> np.uint64(40)).astype(np.float64)
+    return (top24 * (2.0 / (1 << 24)) - 1.0).astype(np.float32)
+
+
+def normal_clipped(seed: int, n: int, sigma: float = 0.5, clip: float = 2.0) -> np.ndarray:
+    """``n`` fp32 values, normal(0, sigma) by Box-Muller, clipped to [-clip, clip]."""
+    m = (n + 1) // 2
+    raw = splitmix64(seed, 2 * m)
+    u1 = ((raw[0::2] >> np.uint64(11)).astype(np.float64) + 1.0) * (1.0 / (1 << 53))  # (0, 1]
+    u2 = (raw[1::2] >> np.uint64(11)).astype(np.float64) * (1.0 / (1 << 53))          # [0, 1)
+    r = np.sqrt(-2.0 * np.log(u1))
+    z = np.empty(2 * m, dtype=np.float64)
+    z[0::2] = r * np.cos(2.0 * np.pi * u2)
+    z[1::2] = r * np.sin(2.0 * np.pi * u2)
+    return np.clip(z[:n] * sigma, -clip, clip).astype(np.float32)
+
+
+def distinct_positions(seed: int, count: int, upper: int) -> np.ndarray:
+    """``count`` distinct positions in [0, upper), drawn in order from one stream."""
+    if count > upper:
+        raise ValueError("more planted positions than positions")
+    chosen: list[int] = []
+    seen: set[int] = set()
+    block = 0
+    while len(chosen) < count:
+        draws = splitmix64(seed + 0x1000 * block, 4 * count + 16)
+        for x in (draws % np.uint64(upper)).tolist():
+            if x not in seen:
+                seen.add(x)
+                chosen.append(int(x))
+                if len(chosen) == count:
+                    break
+        block += 1
+    return np.array(sorted(chosen), dtype=np.int64)
+
+
+@dataclass
+class Inputs:
+    """One attention call's inputs: q [C][32][64], k/v [P+C][8][64], fp32."""
+    q: np.ndarray
+    k: np.ndarray
+    v: np.ndarray
+    C: int
+    P: int
+    planted: np.ndarray = field(default_factory=lambda: np.zeros(0, dtype=np.int64))
+    name: str = ""
+
+    @property
+    def T(self) -> int:
+        return self.P + self.C
+
+    @property
+    def pairs(self) -> int:
+        """Visible (row, key) pairs: sum over chunk rows i of P + i + 1."""
+        return self.C * self.P + self.C * (self.C + 1) // 2
+
+
+def make_inputs(C: int, P: int, seed: int = 1, dist: str = "uniform",
+                planted=None, name: str = "") -> Inputs:
+    """Fresh inputs for a chunk of ``C`` rows at offset ``P``.
+
+    ``dist`` is "uniform" (uniform[-1, 1)) or "normal" (normal(0, 0.5) clipped
+    to [-2, 2]). ``planted`` is an iterable of positions in [0, P + C).
+    """
+    if C < 0 or P < 0:
+        raise ValueError("C and P must be non-negative")
+    T = P + C
+    draw = uniform if dist == "uniform" else normal_clipped
+    if dist not in ("uniform", "normal"):
+        raise ValueError(f"unknown distribution {dist!r}")
+    q = draw(seed, C * HQ * D).reshape(C, HQ, D)
+    k = draw(seed + 1, T * HKV * D).reshape(T, HKV, D)
+    v = draw(seed + 2, T * HKV * D).reshape(T, HKV, D)
+    pos = np.array(sorted(set(int(t) for t in (planted if planted is not None else []))), dtype=np.int64)
+    plant(q, k, v, P, pos)
+    return Inputs(q=q, k=k, v=v, C=C, P=P, planted=pos, name=name)
+
+
+def plant(q: np.ndarray, k: np.ndarray, v: np.ndarray, P: int, positions) -> None:
+    """Write 4.0 into KV head 0 (K and V) at each position, and into query head 0
+    of the chunk row at that position when it lies inside the chunk."""
+    T = k.shape[0]
+    for t in positions:
+        t = int(t)
+        if not 0 <= t < T:
+            raise ValueError(f"planted position {t} outside [0, {T})")
+        k[t, 0, :] = 4.0
+        v[t, 0, :] = 4.0
+        if t >= P:
+            q[t - P, 0, :] = 4.0
+
+
+def ramp(inp: Inputs) -> Inputs:
+    """Make every chunk row's largest score sit on its own diagonal key.
+
+    Query head 0 is all ones and key j of KV head 0 is 2 (j + 1) / T in every
+    element, so scores rise with j and row i's maximum is key P + i, which lies
+    in that row's last K/V tile whatever the tile width.
+    """
+    T = inp.T
+    inp.q[:, 0, :] = 1.0
+    inp.k[:, 0, :] = (2.0 * (np.arange(T, dtype=np.float64) + 1.0) / T).astype(np.float32)[:, None]
+    return inp
+
+
+# ---------------------------------------------------------------------------
+# The named workloads. Sizes come from the page-1 hazards and the serving
+# shapes; the recipe is stated once here and used by tests and bench alike.
+# ---------------------------------------------------------------------------
+
+TINY_PLANTED = (0, 13, 31, 39, 47)
+
+
+def tiny(seed: int = 1) -> Inputs:
+    """C=17, P=31, uniform, planted at prefix and chunk positions incl. the last key."""
+    return make_inputs(17, 31, seed, "uniform", TINY_PLANTED, name="tiny C=17 P=31")
+
+
+def edge(C: int, P: int, seed: int = 1, variant: str = "plain") -> Inputs:
+    """Tile-edge sweep case; ``variant`` is "plain", "lastkey" or "ramp"."""
+    if variant == "plain":
+        return make_inputs(C, P, seed, "uniform", name=f"edge C={C} P={P}")
+    if variant == "lastkey":
+        return make_inputs(C, P, seed, "uniform", [P + C - 1], name=f"edge-lastkey C={C} P={P}")
+    if variant == "ramp":
+        return ramp(make_inputs(C, P, seed, "uniform", name=f"edge-ramp C={C} P={P}"))
+    raise ValueError(variant)
+
+
+def full_causal(T: int, seed: int = 1) -> Inputs:
+    """A whole prompt of T tokens with no cached prefix (P = 0)."""
+    return make_inputs(T, 0, seed, "uniform", name=f"full-causal T={T}")
+
+
+def serve(seed: int = 1, C: int = 2048, P: int = 2048, n_planted: int = 64) -> Inputs:
+    """Serving chunk C=2048 against P=2048 cached keys, 64 planted positions."""
+    pos = distinct_positions(seed + 3, n_planted, P + C)
+    return make_inputs(C, P, seed, "uniform", pos, name=f"serve C={C} P={P}")
+
+
+def long_prefix(seed: int = 1, C: int = 2048, P: int = 30720) -> Inputs:
+    """C=2048 against a 30720-token cached prefix, normal(0, 0.5) clipped to [-2, 2]."""
+    return make_inputs(C, P, seed, "normal", name=f"long C={C} P={P}")
+
+
+EDGE_C = (1, 17, 33, 64)
+EDGE_P = (0, 31, 1000)
+FULL_T = (512, 1024, 2048)
+FULL_T_SMALL = (1, 17, 33, 257)
