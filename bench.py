@@ -1,0 +1,457 @@
+#!/usr/bin/env python
+"""Benchmark: attention TFLOP/s of chunked-prefill GQA attention at C=2048, P=2048.
+
+A step is one call of the hot path (one attn_prefill launch) over the serving
+chunk: q [2048][32][64] against kCache/vCache [4096][8][64], fp32, with 64
+planted score-128 positions. The metric counts visible (row, key) pairs only:
+flops = 4 * d * pairs * 32 heads = 51,547,996,160 per step; no credit for
+tile padding or masked work.
+
+Timing: W untimed warm-up steps, then exactly K timed steps. Before every step
+a 256 MiB buffer is written to flush the 129 MB L2; each step's launch is
+bracketed by CUDA events on the launching stream. The timed region is
+bracketed by a barrier and torch.cuda.synchronize(); with N > 1 (torchrun)
+each rank runs an independent replica and the maximum over ranks is taken.
+
+Also reported on the same JSON line: the end-to-end number through the same
+C-ABI entry point with host (pinned) buffers, copies inside the timed region;
+the roofline of the kernel; the double-precision oracle timed on the host
+cores on a bounded sample of rows; the SM clocks sampled during the timed
+region. ``--impl reference`` times the oracle alone (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "attention TFLOP/s at C=2048,P=2048 (32q/8kv heads, d=64) and % of roofline"
+UNIT = "TFLOP/s"
+L2_FLUSH_BYTES = 256 << 20
+NUM_SMS = 152
+
+# Nominal dense tensor rates (PFLOP/s per GPU) used only as ratios to carry the
+# measured bf16 peak over to tf32: bf16 2.25, tf32 1.1.
+NOMINAL_BF16 = 2.25
+NOMINAL_TF32 = 1.1
+
+
+def flops_for(C: int, P: int) -> float:
+    pairs = C * P + C * (C + 1) // 2
+    return 4.0 * W.D * pairs * W.HQ
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--path", default="attn_prefill",
+                    choices=["attn_prefill", "attn_prefill_ffma", "attn_reference_prefill"])
+    ap.add_argument("--workload", choices=["serve", "long"], default="serve")
+    ap.add_argument("--seed", type=int, default=1)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--compare", action="store_true",
+                    help="also time the FFMA path and the starter reference on the same inputs")
+    return ap.parse_args()
+
+
+def make_workload(name: str, seed: int):
+    if name == "serve":
+        inp = W.serve(seed)
+        desc = "serving chunk C=2048 P=2048, 32q/8kv, d=64, fp32 uniform[-1,1), 64 planted 4.0 positions"
+    else:
+        inp = W.long_prefix(seed)
+        desc = "long cached prefix C=2048 P=30720, 32q/8kv, d=64, fp32 normal(0,0.5) clipped to [-2,2]"
+    return inp, desc
+
+
+def sample_rows_for_cpu(C: int, every: int):
+    """Every ``every``-th chunk row, always including the last (the longest)."""
+    rows = list(range(every - 1, C, every))
+    if rows[-1] != C - 1:
+        rows.append(C - 1)
+    return rows
+
+
+def cpu_oracle_sample(inp, rows, threads):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.prefill(inp, rows=rows, threads=threads)
+    dt = time.perf_counter() - t0
+    pairs = sum(inp.P + i + 1 for i in rows)
+    return 4.0 * W.D * pairs * W.HQ, dt
+
+
+# ----------------------------------------------------------------------------
+# Clock sampling (nvidia-smi, during the timed region)
+# ----------------------------------------------------------------------------
+
+_CLOCK_FIELDS = ["timestamp", "index", "clocks.sm", "clocks.max.sm", "power.draw",
+                 "clocks_event_reasons.active", "clocks_event_reasons.hw_slowdown",
+                 "clocks_event_reasons.hw_thermal_slowdown",
+                 "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+
+class ClockSampler:
+    def __init__(self, device_index: int):
+        self.path = os.path.join(tempfile.mkdtemp(prefix="clk"), "clocks.csv")
+        self.proc = None
+        self.device_index = device_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device_index), "--query-gpu=" + ",".join(_CLOCK_FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "50", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        deadline = time.time() + 10
+        while time.time() < deadline:  # wait for the first sample
+            if os.path.exists(self.path) and os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.05)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t_begin: float, t_end: float):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) != len(_CLOCK_FIELDS):
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+            except ValueError:
+                continue
+            rows.append((ts, parts))
+        window = [p for ts, p in rows if t_begin - 0.05 <= ts <= t_end + 0.05] or [p for _, p in rows]
+        if not window:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(p[2]) for p in window if p[2].replace(".", "").isdigit()]
+        smax = [float(p[3]) for p in window if p[3].replace(".", "").isdigit()]
+        reasons = set()
+        for p in window:
+            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                  "sw_power_cap"), p[6:10]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(window)}
+
+
+# ----------------------------------------------------------------------------
+# Peaks and roofline
+# ----------------------------------------------------------------------------
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d.get("hbm_gbs"), "bf16_tflops": d.get("bf16_tflops"),
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"),
+                "sm_max_mhz": d.get("sm_max_mhz", 2070.0), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "sm_max_mhz": 2070.0, "source": "fallback"}
+
+
+def kernel_source_hash(path_name: str) -> str:
+    """Hash of the kernel source a profile was taken on (traffic goes stale with it)."""
+    fname = {"attn_prefill": "tc.cu", "attn_prefill_ffma": "ffma.cu",
+             "attn_reference_prefill": "reference.cu"}[path_name]
+    src = os.path.join(ROOT, "chunked_prefill_gqa_gb300", "csrc", fname)
+    if not os.path.exists(src):
+        src = os.path.join(ROOT, "chunked_prefill_gqa_gb300", "csrc", "ffma.cu")
+    return hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+
+
+def profiled_traffic(path_name: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source; otherwise None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(f"{path_name}:{workload}")
+    if not e or e.get("source_sha256_16") != kernel_source_hash(path_name):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def roofline(path_name: str, kernel: str, flops: float, ms: float, peaks, workload: str):
+    achieved = flops / (ms * 1e-3) / 1e12
+    if kernel == "tcgen05-split-tf32":
+        peak = peaks["bf16_tflops"] * NOMINAL_TF32 / NOMINAL_BF16
+        r = {"bound": "tensor", "peak_dtype": "tf32",
+             "peak_note": f"{peaks['source']} bf16 burst x {NOMINAL_TF32}/{NOMINAL_BF16} (nominal tf32/bf16)",
+             "tensor_passes": 3,
+             "frac_of_split_roof": None}
+    else:
+        # FP32 FFMA pipe: 152 SMs x 128 lanes x 2 flop per clock at the maximum SM clock.
+        peak = NUM_SMS * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+        r = {"bound": "alu", "peak_dtype": "fp32-ffma",
+             "peak_note": f"152 SMs x 128 FFMA/clk x 2 flop x {peaks['sm_max_mhz']:.0f} MHz"}
+    r.update({"achieved": round(achieved, 3), "peak": round(peak, 3), "unit": UNIT,
+              "frac": round(achieved / peak, 4),
+              "traffic": profiled_traffic(path_name, workload)})
+    if "frac_of_split_roof" in r:
+        r["frac_of_split_roof"] = round(3 * achieved / peak, 4)
+    return r
+
+
+# ----------------------------------------------------------------------------
+# The reference arm: the oracle on the host cores
+# ----------------------------------------------------------------------------
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    inp, desc = make_workload(args.workload, args.seed)
+    threads = os.cpu_count() or 1
+    rows = sample_rows_for_cpu(inp.C, 16)  # 128 rows per step, spread over the chunk
+    for _ in range(args.warmup):
+        cpu_oracle_sample(inp, rows, threads)
+    total_flops, total_s = 0.0, 0.0
+    for _ in range(args.steps):
+        f, dt = cpu_oracle_sample(inp, rows, threads)
+        total_flops += f
+        total_s += dt
+    value = total_flops / total_s / 1e12
+    sample = f"{len(rows)} of {inp.C} chunk rows (every 16th + last), all 32 heads, per step"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": desc, "C": inp.C, "P": inp.P, "parallelism": "host cores"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads() if threads <= 0 else threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ----------------------------------------------------------------------------
+# Our arm
+# ----------------------------------------------------------------------------
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+
+    import chunked_prefill_gqa_gb300 as cp
+    from chunked_prefill_gqa_gb300 import build as B
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group(backend="nccl")
+    else:
+        torch.cuda.set_device(0)
+    if rank == 0:
+        B.build()
+    if world > 1:
+        dist.barrier()
+    cp.load()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    inp, desc = make_workload(args.workload, args.seed)
+    C, P = inp.C, inp.P
+    flops = flops_for(C, P)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    q = torch.from_numpy(inp.q).to(dev)
+    k = torch.from_numpy(inp.k).to(dev)
+    v = torch.from_numpy(inp.v).to(dev)
+    out = torch.empty_like(q)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    fn = getattr(cp, args.path)
+    kernel = "tcgen05-split-tf32" if args.path == "attn_prefill" else (
+        "ffma" if args.path == "attn_prefill_ffma" else "reference")
+
+    def call():
+        fn(q, k, v, out, P, stream)
+
+    sampler = ClockSampler(dev.index if world == 1 else local)
+    sampler.start()
+    for _ in range(args.warmup):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    if cp.attn_get_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    t_begin = time.time()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        call()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    wall = time.perf_counter() - wall0
+    t_end = time.time()
+    sampler.stop()
+    err = cp.attn_get_device_error()
+    if err != 0:
+        raise RuntimeError(f"device error in the timed region: {cp.strerror(err)}")
+    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms_mean = sum(launch_ms) / len(launch_ms)
+    kernel_ms_total = sum(launch_ms)
+    if world > 1:
+        t = torch.tensor([kernel_ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        kernel_ms_total = float(t.item())
+    ms_per_step = kernel_ms_total / args.steps
+    value = world * flops / (ms_per_step * 1e-3) / 1e12
+
+    # End to end through the same entry point: pinned host inputs copied in,
+    # the result copied out, every step inside the timed region.
+    e2e = None
+    if not args.no_e2e:
+        hq = torch.from_numpy(inp.q).pin_memory()
+        hk = torch.from_numpy(inp.k).pin_memory()
+        hv = torch.from_numpy(inp.v).pin_memory()
+        hout = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+        dq, dk, dv, dout = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(out)
+
+        def e2e_step():
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            fn(dq, dk, dv, dout, P, stream)
+            hout.copy_(dout, non_blocking=True)
+
+        for _ in range(max(3, args.warmup // 4)):
+            flush.zero_()
+            e2e_step()
+        n_e2e = max(10, args.steps // 5)
+        es = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e)]
+        ee = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e)]
+        barrier()
+        torch.cuda.synchronize()
+        for i in range(n_e2e):
+            flush.zero_()
+            es[i].record(stream)
+            e2e_step()
+            ee[i].record(stream)
+        torch.cuda.synchronize()
+        e_ms = sum(a.elapsed_time(b) for a, b in zip(es, ee))
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e_ms /= n_e2e
+        ok = np.array_equal(hout.numpy().view(np.uint32), out.cpu().numpy().view(np.uint32))
+        e2e = {"value": world * flops / (e_ms * 1e-3) / 1e12, "unit": UNIT,
+               "ms_per_step": e_ms, "steps": n_e2e,
+               "h2d_bytes_per_step": int(hq.numel() + hk.numel() + hv.numel()) * 4,
+               "d2h_bytes_per_step": int(hout.numel()) * 4,
+               "matches_device_timed_output": bool(ok)}
+
+    compare = None
+    if args.compare and rank == 0:
+        compare = {}
+        for other in ("attn_prefill_ffma", "attn_reference_prefill"):
+            if other == args.path:
+                continue
+            g = getattr(cp, other)
+            reps = 3 if other == "attn_reference_prefill" else 20
+            for _ in range(2):
+                g(q, k, v, out, P, stream)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            tot = 0.0
+            for _ in range(reps):
+                flush.zero_()
+                e0.record(stream)
+                g(q, k, v, out, P, stream)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                tot += e0.elapsed_time(e1)
+            compare[other] = {"ms": tot / reps, "tflops": flops / (tot / reps * 1e-3) / 1e12,
+                              "speedup_of_measured_path": (tot / reps) / ms_mean}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        threads = os.cpu_count() or 1
+        rows = sample_rows_for_cpu(C, 4)
+        f, dt = cpu_oracle_sample(inp, rows, threads)
+        cpu = {"value": f / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{len(rows)} of {C} chunk rows (every 4th + last), all 32 heads, "
+                         f"{dt:.2f} s wall on {threads} threads"}
+
+    if rank == 0:
+        peaks = load_peaks()
+        line = {
+            "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": desc, "C": C, "P": P, "hq": W.HQ, "hkv": W.HKV, "d": W.D,
+                       "path": args.path, "kernel": kernel,
+                       "flops_per_step": flops,
+                       "l2": "flushed before every timed step (256 MiB write)",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roofline(args.path, kernel, flops, ms_mean, peaks, args.workload),
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": args.steps,
+            "clocks": sampler.summary(t_begin, t_end),
+            "wall_s_timed_region": round(wall, 4),
+        }
+        if compare:
+            line["compare"] = compare
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

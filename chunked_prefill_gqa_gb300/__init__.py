@@ -1,0 +1,162 @@
+"""Python binding of libattnprefill.so (argument marshalling only).
+
+Every function here has the name of a C entry point declared in
+``include/attn_prefill.h`` and does nothing but check tensor shapes, dtypes
+and devices, pass raw device pointers and the current CUDA stream, and raise
+:class:`AttnError` on a nonzero return code. All arithmetic runs in the
+library's CUDA kernels; there is no CPU or PyTorch fallback. If the library
+is missing, importing the functions works but every call raises.
+
+Tensors (attention-v1 contract): q [C][32][64], kCache and vCache
+[P + C][8][64], out [C][32][64], fp32, contiguous, on the current CUDA device.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HQ, HKV, D = 32, 8, 64
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libattnprefill.so")
+
+ATTN_OK = 0
+ATTN_EINVAL = -1
+ATTN_EALIGN = -2
+ATTN_ERANGE = -3
+ATTN_ELAUNCH = -4
+ATTN_ETIMEOUT = -5
+ATTN_EBOUNDS = -6
+ATTN_EDEVICE = -7
+ATTN_ETMA = -8
+ATTN_ECUDA = -9
+MAX_TOKENS = 1 << 24
+
+# Every symbol the header declares (the CPU tests check the library exports them).
+EXPORTS = ("attn_prefill", "attn_full_causal", "attn_prefill_ffma", "attn_reference_prefill",
+           "attn_get_device_error", "attn_strerror", "attn_version")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {strerror(code)} (code {code})")
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def load():
+    """Load the shared library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with `python -m chunked_prefill_gqa_gb300.build` "
+                    "(there is no fallback implementation)")
+            lib = ctypes.CDLL(LIB_PATH)
+            vp, ci = ctypes.c_void_p, ctypes.c_int
+            for name in ("attn_prefill", "attn_prefill_ffma", "attn_reference_prefill"):
+                fn = getattr(lib, name)
+                fn.restype = ci
+                fn.argtypes = [vp, vp, vp, vp, ci, ci, vp]
+            lib.attn_full_causal.restype = ci
+            lib.attn_full_causal.argtypes = [vp, vp, vp, vp, ci, vp]
+            lib.attn_get_device_error.restype = ci
+            lib.attn_get_device_error.argtypes = []
+            lib.attn_strerror.restype = ctypes.c_char_p
+            lib.attn_strerror.argtypes = [ci]
+            lib.attn_version.restype = ctypes.c_char_p
+            lib.attn_version.argtypes = []
+            _lib = lib
+    return _lib
+
+
+def strerror(code: int) -> str:
+    try:
+        return load().attn_strerror(int(code)).decode()
+    except Exception:  # library missing: still produce a message
+        return f"error {code}"
+
+
+def version() -> str:
+    return load().attn_version().decode()
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _check_tensors(q, k, v, out, C, P):
+    import torch
+    for name, t, shape in (("q", q, (C, HQ, D)), ("kCache", k, (P + C, HKV, D)),
+                           ("vCache", v, (P + C, HKV, D)), ("out", out, (C, HQ, D))):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor")
+        if t.dtype != torch.float32:
+            raise TypeError(f"{name} must be float32, got {t.dtype}")
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be on a CUDA device")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if tuple(t.shape) != shape:
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {shape}")
+
+
+def _call(name, q, k, v, out, P, stream):
+    C = q.shape[0]
+    _check_tensors(q, k, v, out, C, P)
+    rc = getattr(load(), name)(_ptr(q), _ptr(k), _ptr(v), _ptr(out), C, P, _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, name)
+    return out
+
+
+def attn_prefill(q, kCache, vCache, out, P: int, stream=None):
+    """out <- causal GQA attention of chunk q at offset P (tensor-core path)."""
+    return _call("attn_prefill", q, kCache, vCache, out, P, stream)
+
+
+def attn_full_causal(q, k, v, out, stream=None):
+    """out <- causal GQA attention of a whole prompt (P = 0)."""
+    T = q.shape[0]
+    _check_tensors(q, k, v, out, T, 0)
+    rc = load().attn_full_causal(_ptr(q), _ptr(k), _ptr(v), _ptr(out), T, _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_full_causal")
+    return out
+
+
+def attn_prefill_ffma(q, kCache, vCache, out, P: int, stream=None):
+    """The same operation on the FP32 CUDA cores."""
+    return _call("attn_prefill_ffma", q, kCache, vCache, out, P, stream)
+
+
+def attn_reference_prefill(q, kCache, vCache, out, P: int, stream=None):
+    """The starter-design in-run reference (slow by design)."""
+    return _call("attn_reference_prefill", q, kCache, vCache, out, P, stream)
+
+
+def attn_get_device_error() -> int:
+    """Synchronise the device; return and clear the device error word."""
+    return int(load().attn_get_device_error())
+
+
+def raw(name: str):
+    """The raw ctypes function ``name`` (pointers and ints in, code out)."""
+    return getattr(load(), name)

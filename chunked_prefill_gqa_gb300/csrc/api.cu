@@ -1,0 +1,134 @@
+// api.cu -- the extern "C" entry points of libattnprefill.so: argument
+// validation, the device check, the device error word and dispatch to the
+// kernel launchers. No entry point allocates device memory.
+#include <cstdint>
+#include <cstdio>
+
+#include "common.cuh"
+
+namespace attn {
+namespace {
+
+// The device error word: kernels record the first internal fault here
+// (a bounded wait that expired, a failed bounds check) instead of trapping.
+__device__ unsigned g_error_word;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool checked = false;
+  bool supported = false;
+  unsigned* err = nullptr;  // device address of g_error_word on this device
+};
+DeviceState g_devices[kMaxDevices];
+
+// Looks up (once per device) whether the current device is sm_103 and where
+// its error word lives. Returns an ATTN_* code.
+int current_device(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ECUDA;
+  DeviceState& st = g_devices[dev];
+  if (!st.checked) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return ATTN_ECUDA;
+    st.supported = (major == 10 && minor == 3);
+    if (st.supported) {
+      void* addr = nullptr;
+      if (cudaGetSymbolAddress(&addr, g_error_word) != cudaSuccess) return ATTN_ECUDA;
+      st.err = static_cast<unsigned*>(addr);
+    }
+    st.checked = true;
+  }
+  if (!st.supported) return ATTN_EDEVICE;
+  *out = &st;
+  return ATTN_OK;
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+// Shared validation of every compute entry point. On success fills `p`.
+int prepare(const float* q, const float* k, const float* v, float* out, int C, int P,
+            Problem* p) {
+  if (C < 0 || P < 0) return ATTN_EINVAL;
+  if (C > ATTN_MAX_TOKENS || (long long)P + C > ATTN_MAX_TOKENS) return ATTN_ERANGE;
+  if (C == 0) return ATTN_OK;  // empty chunk: nothing to do, pointers unused
+  if (!q || !k || !v || !out) return ATTN_EINVAL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return ATTN_EALIGN;
+  DeviceState* st = nullptr;
+  const int rc = current_device(&st);
+  if (rc != ATTN_OK) return rc;
+  *p = Problem{q, k, v, out, C, P, st->err};
+  return ATTN_OK;
+}
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ELAUNCH; }
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" int attn_prefill(const float* q, const float* kCache, const float* vCache, float* out,
+                            int C, int P, cudaStream_t stream) {
+  Problem p{};
+  const int rc = prepare(q, kCache, vCache, out, C, P, &p);
+  if (rc != ATTN_OK || C == 0) return rc;
+  return from_cuda(launch_ffma(p, stream));
+}
+
+extern "C" int attn_full_causal(const float* q, const float* k, const float* v, float* out, int T,
+                                cudaStream_t stream) {
+  return attn_prefill(q, k, v, out, T, 0, stream);
+}
+
+extern "C" int attn_prefill_ffma(const float* q, const float* kCache, const float* vCache,
+                                 float* out, int C, int P, cudaStream_t stream) {
+  Problem p{};
+  const int rc = prepare(q, kCache, vCache, out, C, P, &p);
+  if (rc != ATTN_OK || C == 0) return rc;
+  return from_cuda(launch_ffma(p, stream));
+}
+
+extern "C" int attn_reference_prefill(const float* q, const float* kCache, const float* vCache,
+                                      float* out, int C, int P, cudaStream_t stream) {
+  Problem p{};
+  const int rc = prepare(q, kCache, vCache, out, C, P, &p);
+  if (rc != ATTN_OK || C == 0) return rc;
+  return from_cuda(launch_reference(p, stream));
+}
+
+extern "C" int attn_get_device_error(void) {
+  DeviceState* st = nullptr;
+  const int rc = current_device(&st);
+  if (rc != ATTN_OK) return rc;
+  if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ECUDA;
+  unsigned word = 0;
+  const unsigned zero = 0;
+  if (cudaMemcpyFromSymbol(&word, g_error_word, sizeof(word)) != cudaSuccess) return ATTN_ECUDA;
+  if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)) != cudaSuccess) return ATTN_ECUDA;
+  if (word == kDevErrTimeout) return ATTN_ETIMEOUT;
+  if (word == kDevErrBounds) return ATTN_EBOUNDS;
+  return word == 0 ? ATTN_OK : ATTN_ECUDA;
+}
+
+extern "C" const char* attn_strerror(int code) {
+  switch (code) {
+    case ATTN_OK: return "success";
+    case ATTN_EINVAL: return "invalid argument (NULL pointer, C < 0 or P < 0)";
+    case ATTN_EALIGN: return "a tensor pointer is not 16-byte aligned";
+    case ATTN_ERANGE: return "C or P + C exceeds ATTN_MAX_TOKENS";
+    case ATTN_ELAUNCH: return "kernel launch failed";
+    case ATTN_ETIMEOUT: return "a device-side bounded wait expired";
+    case ATTN_EBOUNDS: return "a device-side bounds check failed";
+    case ATTN_EDEVICE: return "the current device is not sm_103 (GB300)";
+    case ATTN_ETMA: return "a TMA tensor map could not be encoded";
+    case ATTN_ECUDA: return "a CUDA runtime call failed";
+    default: return "unknown error code";
+  }
+}
+
+extern "C" const char* attn_version(void) {
+  return "libattnprefill: tcgen05 split-TF32 / FFMA / reference kernels, sm_103a";
+}

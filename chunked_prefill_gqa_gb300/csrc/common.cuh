@@ -1,0 +1,51 @@
+// common.cuh -- definitions shared by the CUDA translation units of
+// libattnprefill.so: problem constants, the launch-parameter block, the
+// device error word protocol and the host-side launcher declarations.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/attn_prefill.h"
+
+namespace attn {
+
+constexpr int kHQ = ATTN_HQ;            // query heads
+constexpr int kHKV = ATTN_HKV;          // KV heads
+constexpr int kGroup = kHQ / kHKV;      // query heads per KV head (4)
+constexpr int kD = ATTN_D;              // head dimension
+constexpr float kScale = 0.125f;        // 1 / sqrt(64), exact in fp32
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Device error codes written into the error word (first writer wins).
+constexpr unsigned kDevErrTimeout = 1u;
+constexpr unsigned kDevErrBounds = 2u;
+
+// Everything a kernel needs about one call.
+struct Problem {
+  const float* q;   // [C][32][64]
+  const float* k;   // [P+C][8][64]
+  const float* v;   // [P+C][8][64]
+  float* out;       // [C][32][64]
+  int C;            // chunk rows
+  int P;            // cached prefix length
+  unsigned* err;    // device error word
+};
+
+__device__ __forceinline__ void record_error(unsigned* err, unsigned code) {
+  atomicCAS(err, 0u, code);
+}
+
+// Visible keys of chunk rows [t0, t0 + rows) clipped to the chunk: the unit's
+// key range is [0, P + min(t0 + rows, C)).
+__host__ __device__ __forceinline__ int unit_keys(int P, int C, int t0, int rows) {
+  const int end = t0 + rows < C ? t0 + rows : C;
+  return P + end;
+}
+
+// Host launchers, one per kernel family (defined in their own .cu files).
+cudaError_t launch_reference(const Problem& p, cudaStream_t stream);
+cudaError_t launch_ffma(const Problem& p, cudaStream_t stream);
+int launch_tc(const Problem& p, cudaStream_t stream);  // returns an ATTN_* code
+
+}  // namespace attn

@@ -1,0 +1,129 @@
+/*
+ * attn_prefill.h -- C ABI of libattnprefill.so: causal grouped-query flash
+ * attention of a prefill chunk against a cached prefix, for sm_103a (GB300).
+ *
+ * The operation ("Inference Attention 2: Flash Prefill Against a Cached
+ * Prefix", Lesson). A chunk of C new tokens at positions P .. P+C-1 attends to
+ * the cached keys and values at positions 0 .. P+C-1, causally: chunk row i
+ * sees keys j <= P + i. With 32 query heads, 8 KV heads and head dimension 64,
+ * query head h reads KV head h / 4, the scale is exactly 1/8, and
+ *
+ *   out[i][h][:] = sum_{j <= P+i} softmax_j( q[i][h] . k[j][h/4] / 8 ) * v[j][h/4][:]
+ *
+ * Layouts (attention-v1 contract, same page): fp32, row-major, contiguous:
+ *   q       [C][32][64]       the chunk's queries
+ *   kCache  [P + C][8][64]    keys of the whole visible sequence
+ *   vCache  [P + C][8][64]    values of the whole visible sequence
+ *   out     [C][32][64]       written, never read (it may hold garbage or NaN)
+ *
+ * Ownership. Every pointer is a DEVICE pointer owned by the caller, on the
+ * current CUDA device. The library allocates no device memory per call and
+ * takes no workspace: there is no score matrix anywhere (the contract has no
+ * workspace argument). q, kCache and vCache are only read.
+ *
+ * Execution. Every compute entry point validates its arguments on the host,
+ * enqueues its kernel(s) on `stream` and returns; completion is observed by
+ * synchronising the stream. A NULL stream is the legacy default stream.
+ * Calls on different streams may overlap; each call reads only its inputs and
+ * writes only its out.
+ *
+ * Errors. 0 means enqueued. A negative return is one of ATTN_E* below and
+ * means nothing was enqueued (argument errors) or the launch failed. A kernel
+ * that detects an internal fault (a bounded wait that expired, a bounds check
+ * that failed) records it in a device-side error word instead of trapping;
+ * attn_get_device_error() reads and clears that word. There is no CPU
+ * fallback and no alternative back end: on a device that is not sm_103 the
+ * entry points return ATTN_EDEVICE.
+ *
+ * Sizes. 0 <= C <= ATTN_MAX_TOKENS, 0 <= P, P + C <= ATTN_MAX_TOKENS. C == 0
+ * is a valid empty call: nothing is read, written or launched and the
+ * pointers may be NULL. Pointers must be 16-byte aligned.
+ */
+#ifndef ATTN_PREFILL_H
+#define ATTN_PREFILL_H
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ATTN_HQ 32
+#define ATTN_HKV 8
+#define ATTN_D 64
+#define ATTN_MAX_TOKENS (1 << 24)
+
+/* Return codes. */
+#define ATTN_OK 0
+#define ATTN_EINVAL -1      /* NULL pointer with C > 0, C < 0, P < 0 */
+#define ATTN_EALIGN -2      /* a pointer is not 16-byte aligned */
+#define ATTN_ERANGE -3      /* C or P + C above ATTN_MAX_TOKENS */
+#define ATTN_ELAUNCH -4     /* the kernel launch failed (cudaGetLastError) */
+#define ATTN_ETIMEOUT -5    /* device word: a bounded wait expired */
+#define ATTN_EBOUNDS -6     /* device word: a device-side bounds check failed */
+#define ATTN_EDEVICE -7     /* the current device is not sm_103 */
+#define ATTN_ETMA -8        /* a TMA tensor map could not be encoded */
+#define ATTN_ECUDA -9       /* another CUDA runtime call failed */
+
+/*
+ * attn_prefill -- the main path: one persistent, warp-specialised tcgen05
+ * kernel. A CTA owns a work unit of 32 chunk positions x the 4 query heads of
+ * one KV head (GQA packing, "FlashAttention and inference kernels", GQA read
+ * amplification exercise), so each K/V tile is staged in shared memory once
+ * per group (page 1, Lesson: stage each K/V tile once, reuse it across a
+ * resident tile of query rows). Tiles past the causal edge are never loaded
+ * and the diagonal tile is masked ("FlashAttention and inference kernels",
+ * How FlashAttention evolved: the causal mask). The online softmax carries
+ * m, l and the accumulator across tiles and divides once at the end (page 1,
+ * Lesson, the tile update). In this build the contractions run on the FP32
+ * CUDA cores (the attn_prefill_ffma kernel).
+ */
+int attn_prefill(const float *q, const float *kCache, const float *vCache, float *out,
+                 int C, int P, cudaStream_t stream);
+
+/*
+ * attn_full_causal -- a whole prompt with nothing cached: identical to
+ * attn_prefill(q, k, v, out, T, 0, stream) ("Inference Attention 1: The Full
+ * Score Matrix", Lesson: q [T][32][64], k and v [T][8][64], row i sees j <= i).
+ */
+int attn_full_causal(const float *q, const float *k, const float *v, float *out,
+                     int T, cudaStream_t stream);
+
+/*
+ * attn_prefill_ffma -- the same operation on the FP32 CUDA cores (FFMA), with
+ * the same GQA-packed tiling but plain shared-memory staging. Exact fp32
+ * products; kept as the precision reference for the tensor-core path and as
+ * the fallback design. Same arguments, layouts and errors as attn_prefill.
+ */
+int attn_prefill_ffma(const float *q, const float *kCache, const float *vCache, float *out,
+                      int C, int P, cudaStream_t stream);
+
+/*
+ * attn_reference_prefill -- the page's starter design rebuilt as the in-run
+ * timing reference (page 1, Starter code): one warp per (chunk row, query
+ * head), every row walking its whole K/V prefix through the memory system,
+ * rescaling by exp(m_old - m_new) at every key. Correct and slow by design.
+ * Same arguments, layouts and errors as attn_prefill.
+ */
+int attn_reference_prefill(const float *q, const float *kCache, const float *vCache, float *out,
+                           int C, int P, cudaStream_t stream);
+
+/*
+ * attn_get_device_error -- synchronises the current device, then returns and
+ * clears the device-side error word: 0, ATTN_ETIMEOUT or ATTN_EBOUNDS (the
+ * first fault recorded since the last call), or ATTN_ECUDA if the
+ * synchronisation itself failed.
+ */
+int attn_get_device_error(void);
+
+/* attn_strerror -- a static, human-readable string for any return code. */
+const char *attn_strerror(int code);
+
+/* attn_version -- a static string naming the build (kernels and arch). */
+const char *attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_PREFILL_H */
