@@ -35,7 +35,7 @@ MAX_TOKENS = 1 << 24
 
 # Every symbol the header declares (the CPU tests check the library exports them).
 EXPORTS = ("attn_prefill", "attn_full_causal", "attn_prefill_ffma", "attn_reference_prefill",
-           "attn_get_device_error", "attn_strerror", "attn_version")
+           "attn_selftest_timeout", "attn_get_device_error", "attn_strerror", "attn_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -62,7 +62,8 @@ def load():
                     "(there is no fallback implementation)")
             lib = ctypes.CDLL(LIB_PATH)
             vp, ci = ctypes.c_void_p, ctypes.c_int
-            for name in ("attn_prefill", "attn_prefill_ffma", "attn_reference_prefill"):
+            for name in ("attn_prefill", "attn_prefill_ffma", "attn_reference_prefill",
+                         "attn_selftest_timeout"):
                 fn = getattr(lib, name)
                 fn.restype = ci
                 fn.argtypes = [vp, vp, vp, vp, ci, ci, vp]
@@ -150,6 +151,12 @@ def attn_prefill_ffma(q, kCache, vCache, out, P: int, stream=None):
 def attn_reference_prefill(q, kCache, vCache, out, P: int, stream=None):
     """The starter-design in-run reference (slow by design)."""
     return _call("attn_reference_prefill", q, kCache, vCache, out, P, stream)
+
+
+def attn_selftest_timeout(q, kCache, vCache, out, P: int, stream=None):
+    """Run the tensor-core kernel with a load withheld so a bounded wait expires
+    (a failure-path test); read the outcome with attn_get_device_error()."""
+    return _call("attn_selftest_timeout", q, kCache, vCache, out, P, stream)
 
 
 def attn_get_device_error() -> int:

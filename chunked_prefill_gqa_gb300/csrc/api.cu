@@ -75,7 +75,7 @@ extern "C" int attn_prefill(const float* q, const float* kCache, const float* vC
   Problem p{};
   const int rc = prepare(q, kCache, vCache, out, C, P, &p);
   if (rc != ATTN_OK || C == 0) return rc;
-  return from_cuda(launch_ffma(p, stream));
+  return launch_tc(p, stream);
 }
 
 extern "C" int attn_full_causal(const float* q, const float* k, const float* v, float* out, int T,
@@ -97,6 +97,15 @@ extern "C" int attn_reference_prefill(const float* q, const float* kCache, const
   const int rc = prepare(q, kCache, vCache, out, C, P, &p);
   if (rc != ATTN_OK || C == 0) return rc;
   return from_cuda(launch_reference(p, stream));
+}
+
+extern "C" int attn_selftest_timeout(const float* q, const float* kCache, const float* vCache,
+                                     float* out, int C, int P, cudaStream_t stream) {
+  Problem p{};
+  const int rc = prepare(q, kCache, vCache, out, C, P, &p);
+  if (rc != ATTN_OK) return rc;
+  if (C == 0) return ATTN_EINVAL;
+  return launch_tc_fault_test(p, stream);
 }
 
 extern "C" int attn_get_device_error(void) {

@@ -46,6 +46,7 @@ __host__ __device__ __forceinline__ int unit_keys(int P, int C, int t0, int rows
 // Host launchers, one per kernel family (defined in their own .cu files).
 cudaError_t launch_reference(const Problem& p, cudaStream_t stream);
 cudaError_t launch_ffma(const Problem& p, cudaStream_t stream);
-int launch_tc(const Problem& p, cudaStream_t stream);  // returns an ATTN_* code
+int launch_tc(const Problem& p, cudaStream_t stream);             // returns an ATTN_* code
+int launch_tc_fault_test(const Problem& p, cudaStream_t stream);  // skips a load, 20 ms waits
 
 }  // namespace attn

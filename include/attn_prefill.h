@@ -75,8 +75,10 @@ extern "C" {
  * and the diagonal tile is masked ("FlashAttention and inference kernels",
  * How FlashAttention evolved: the causal mask). The online softmax carries
  * m, l and the accumulator across tiles and divides once at the end (page 1,
- * Lesson, the tile update). In this build the contractions run on the FP32
- * CUDA cores (the attn_prefill_ffma kernel).
+ * Lesson, the tile update). QK^T and PV run on the tensor cores as
+ * error-compensated split-TF32: each fp32 operand x = hi + lo with hi exactly
+ * representable in tf32, and each product accumulates hi*hi + hi*lo + lo*hi in
+ * fp32, so the result matches exact fp32 products to about 2^-20 relative.
  */
 int attn_prefill(const float *q, const float *kCache, const float *vCache, float *out,
                  int C, int P, cudaStream_t stream);
@@ -107,6 +109,18 @@ int attn_prefill_ffma(const float *q, const float *kCache, const float *vCache, 
  */
 int attn_reference_prefill(const float *q, const float *kCache, const float *vCache, float *out,
                            int C, int P, cudaStream_t stream);
+
+/*
+ * attn_selftest_timeout -- a test of the failure path, not a computation. It
+ * launches the attn_prefill kernel with one K tile deliberately never loaded
+ * and every bounded wait limited to 20 ms, so a wait expires: the kernel
+ * records ATTN_ETIMEOUT in the device error word, winds down all its warps,
+ * frees its tensor memory and returns; the context stays usable. `out` is left
+ * unspecified. Requires C >= 1 (ATTN_EINVAL otherwise). Returns 0 once enqueued;
+ * the caller then reads the outcome with attn_get_device_error().
+ */
+int attn_selftest_timeout(const float *q, const float *kCache, const float *vCache, float *out,
+                          int C, int P, cudaStream_t stream);
 
 /*
  * attn_get_device_error -- synchronises the current device, then returns and
