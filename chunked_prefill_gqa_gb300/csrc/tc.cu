@@ -18,18 +18,24 @@
 // Contractions: fp32 split-TF32. Every operand x is split into hi = x with the
 // 13 low mantissa bits cleared (exactly tf32) and lo = x - hi (exact in fp32);
 // a product is accumulated as hi*hi + hi*lo + lo*hi on the tensor cores in
-// fp32, dropping only lo*lo (relative size 2^-20). QK^T: A = Q (hi and lo in
-// TMEM), B = K (shared memory, K-major, 128-byte swizzle). PV: A = P (hi and lo
-// in TMEM, P hi overwriting the S columns it came from), B = V^T (shared
-// memory, written transposed by the converter warps).
+// fp32, dropping only lo*lo (relative size 2^-20). The two terms that share
+// an A operand run as one MMA of N = 128 by stacking the B operands:
+//   S' = Q_hi [K_hi; K_lo]^T  (N = 128)   then  S'[:, :64] += Q_lo K_hi^T
+//   S  = S'[:, :64] + S'[:, 64:]            (summed by the softmax warps)
+//   O' += P_hi [V_hi^T; V_lo^T]^T (N = 128) then O'[:, :64] += P_lo V_hi^T
+//   O  = O'[:, :64] + O'[:, 64:]            (summed in the epilogue)
+// Q and P are TMEM operands (P hi and P lo overwrite the S columns they came
+// from); K and V^T are 128-byte-swizzled K-major shared-memory operands.
 //
 // Warp roles (10 warps):
-//   0-3  softmax: own TMEM lanes 0-127 (one row each); split Q into TMEM at the
-//        start of a unit; per tile read S, mask, online softmax, write P hi/lo,
-//        rescale O when the reference maximum moves; epilogue O / l -> out.
-//   4    producer: TMA loads of Q, K and V tiles into the shared-memory rings.
+//   0-3  softmax: own TMEM lanes 0-127 (one row each); load and split Q into
+//        TMEM at the start of a unit; per tile read S, mask, online softmax,
+//        write P hi/lo, rescale O when the reference maximum moves; epilogue.
+//   4    K producer: TMA loads of K tiles into the K ring.
 //   5    MMA: allocates TMEM; one lane issues every tcgen05.mma and commit.
-//   6-9  converters: K -> K lo; V -> V^T hi and V^T lo.
+//   6    V producer: TMA loads of V tiles into the raw V ring.
+//   7    K converter: K lo next to each K tile.
+//   8-9  V converters: raw V -> V^T hi / V^T lo.
 // Every wait is bounded; on expiry the kernel records ATTN_ETIMEOUT in the
 // device error word, all roles wind down, and TMEM is freed.
 #include <cuda.h>
@@ -43,54 +49,54 @@ namespace {
 
 using namespace tc;
 
-constexpr int kBq = 32;         // chunk positions per unit
+constexpr int kBq = 32;           // chunk positions per unit
 constexpr int kM = kBq * kGroup;  // 128 rows = TMEM lanes
-constexpr int kBc = 64;         // keys per tile
-constexpr int kKStages = 3;     // K ring (raw K as tf32 hi after the in-place split, plus K lo)
-constexpr int kVRawStages = 2;  // raw V landing ring
-constexpr int kVStages = 2;     // V^T hi/lo ring
+constexpr int kBc = 64;           // keys per tile
+constexpr int kKStages = 3;       // K ring: [K | K lo] per d-half region
+constexpr int kVRawStages = 4;    // raw V landing ring
+constexpr int kVStages = 2;       // V^T ring: [V^T hi | V^T lo] per key-half region
 
 constexpr int kSoftmaxWarps = 4;
-constexpr int kProducerWarp = 4;
+constexpr int kKProducerWarp = 4;
 constexpr int kMmaWarp = 5;
-constexpr int kFirstConvWarp = 6;
-constexpr int kConvWarps = 4;
-constexpr int kThreads = 32 * (kFirstConvWarp + kConvWarps);
+constexpr int kVProducerWarp = 6;
+constexpr int kKConvWarp = 7;
+constexpr int kFirstVConvWarp = 8;
+constexpr int kVConvWarps = 2;
+constexpr int kThreads = 32 * (kFirstVConvWarp + kVConvWarps);
 
 // TMEM columns (fp32, one per column).
 constexpr uint32_t kColQhi = 0;
 constexpr uint32_t kColQlo = 64;
-constexpr uint32_t kColS = 128;    // two S buffers of 64 columns; P hi overwrites S
-constexpr uint32_t kColPlo = 256;  // two P lo buffers of 64 columns
-constexpr uint32_t kColO = 384;
+constexpr uint32_t kColS = 128;  // two 128-column S buffers; P hi | P lo overwrite them
+constexpr uint32_t kColO = 384;  // O' = [P_hi V_hi + P_lo V_hi | P_hi V_lo]
 constexpr uint32_t kTmemCols = 512;
 
-// Shared memory (byte offsets from a 1024-aligned base). Every operand tile
-// is a set of 128-byte-swizzled regions: rows of 128 bytes (32 floats).
-constexpr uint32_t kQBytes = kM * kD * 4;                 // 32 KB: 2 d-half regions of 128 rows
-constexpr uint32_t kKTileBytes = kBc * kD * 4;            // 16 KB: 2 d-half regions of 64 rows
-constexpr uint32_t kSmemQ = 0;
-constexpr uint32_t kSmemK = kSmemQ + kQBytes;                             // [stage][K | K lo]
-constexpr uint32_t kSmemVRaw = kSmemK + kKStages * 2 * kKTileBytes;       // [stage][V]
-constexpr uint32_t kSmemVT = kSmemVRaw + kVRawStages * kKTileBytes;       // [stage][V^T hi | V^T lo]
-constexpr uint32_t kSmemBar = kSmemVT + kVStages * 2 * kKTileBytes;
-constexpr uint32_t kNumBars = 3 * kKStages + 2 * kVRawStages + 2 * kVStages + 2 + 2 + 5;
+// Shared memory (byte offsets from a 1024-aligned base). An operand region
+// is rows of 128 bytes (32 floats) in the 128-byte swizzle, 8-row groups
+// 1024 bytes apart; a stacked region holds 64 hi rows then 64 lo rows.
+constexpr uint32_t kRegion = 128 * 128;                  // 16 KB: 128 rows
+constexpr uint32_t kHalf = 64 * 128;                     // 8 KB: 64 rows
+constexpr uint32_t kKStageBytes = 2 * kRegion;           // 2 d-half regions
+constexpr uint32_t kVRawBytes = 2 * kHalf;               // 2 d-half regions of 64 keys
+constexpr uint32_t kVStageBytes = 2 * kRegion;           // 2 key-half regions
+constexpr uint32_t kSmemK = 0;
+constexpr uint32_t kSmemVRaw = kSmemK + kKStages * kKStageBytes;
+constexpr uint32_t kSmemVT = kSmemVRaw + kVRawStages * kVRawBytes;
+constexpr uint32_t kSmemBar = kSmemVT + kVStages * kVStageBytes;
+constexpr uint32_t kNumBars = 3 * kKStages + 2 * kVRawStages + 2 * kVStages + 2 + 2 + 2 + 2;
 constexpr uint32_t kSmemTotal = kSmemBar + kNumBars * 8 + 16;
 constexpr uint32_t kSmemAlloc = kSmemTotal + 1024;  // slack to align the base
 
 static_assert(kSmemAlloc <= 232448, "exceeds the 227 KB per-block shared memory limit");
 static_assert(kM == 128 && kD == 64 && kBc == 64, "the MMA shapes below assume 128 x 64 x 64");
 
-constexpr uint32_t kIdesc = idesc_tf32(128, 64);
+constexpr uint32_t kIdescN128 = idesc_tf32(128, 128);
+constexpr uint32_t kIdescN64 = idesc_tf32(128, 64);
 // Keep a stale reference maximum while the new maximum exceeds it by at most
 // this much in log2 units (p stays <= 2^8): l and O share the reference, so
 // O / l is exact either way, and O needs no rescale.
 constexpr float kStaleLog2 = 8.0f;
-// The tensor core reads an fp32 operand as tf32 by ignoring its 13 low
-// mantissa bits (measured on GB300 for both shared-memory and TMEM operands:
-// 1 + 3 * 2^-12 reads as 1), so raw K already is tf32_hi(K) to the MMA and
-// only K lo has to be written. Set to false to truncate K in place as well.
-constexpr bool kHwTruncatesTf32 = true;
 
 struct Params {
   Problem p;
@@ -102,18 +108,16 @@ struct Params {
 
 struct Bars {
   uint64_t* kfull;   // [kKStages] TMA K landed
-  uint64_t* kconv;   // [kKStages] K lo written (converter warps)
+  uint64_t* kconv;   // [kKStages] K lo written
   uint64_t* kempty;  // [kKStages] QK done with the stage (MMA commit)
   uint64_t* vfull;   // [kVRawStages] TMA V landed
-  uint64_t* vrfree;  // [kVRawStages] converters done reading raw V
+  uint64_t* vrfree;  // [kVRawStages] V converters done reading raw V
   uint64_t* vconv;   // [kVStages] V^T hi/lo written
   uint64_t* vempty;  // [kVStages] PV done with the stage (MMA commit)
   uint64_t* sfull;   // [2] S buffer written (MMA commit)
   uint64_t* pfull;   // [2] P hi/lo written and O rescaled (softmax warps)
-  uint64_t* odone;   // PV done (MMA commit)
-  uint64_t* qfull;   // TMA Q landed
-  uint64_t* qfree;   // softmax warps done reading the Q staging buffer
-  uint64_t* qready;  // Q hi/lo in TMEM
+  uint64_t* odone;   // [2] PV(n) done, barrier n & 1 (MMA commit)
+  uint64_t* qready;  // Q hi/lo in TMEM (softmax warps)
   uint64_t* drain;   // MMA drain on abort
 };
 
@@ -129,9 +133,7 @@ __device__ __forceinline__ Bars carve_bars(uint8_t* base) {
   r.vempty = b; b += kVStages;
   r.sfull = b; b += 2;
   r.pfull = b; b += 2;
-  r.odone = b++;
-  r.qfull = b++;
-  r.qfree = b++;
+  r.odone = b; b += 2;
   r.qready = b++;
   r.drain = b++;
   return r;
@@ -187,9 +189,14 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&r)[64]) {
+  tmem_ld32(taddr, *reinterpret_cast<float(*)[32]>(&r[0]));
+  tmem_ld32(taddr + 32, *reinterpret_cast<float(*)[32]>(&r[32]));
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
-tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-          const __grid_constant__ CUtensorMap tmv, const Params prm) {
+tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+          const Params prm) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const Bars bars = carve_bars(smem);
@@ -202,24 +209,23 @@ tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUten
   if (threadIdx.x == 0) {
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(&bars.kfull[s], 1);
-      mbar_init(&bars.kconv[s], kConvWarps);
+      mbar_init(&bars.kconv[s], 1);
       mbar_init(&bars.kempty[s], 1);
     }
     for (int s = 0; s < kVRawStages; ++s) {
       mbar_init(&bars.vfull[s], 1);
-      mbar_init(&bars.vrfree[s], kConvWarps);
+      mbar_init(&bars.vrfree[s], kVConvWarps);
     }
     for (int s = 0; s < kVStages; ++s) {
-      mbar_init(&bars.vconv[s], kConvWarps);
+      mbar_init(&bars.vconv[s], kVConvWarps);
       mbar_init(&bars.vempty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars.sfull[b], 1);
       mbar_init(&bars.pfull[b], kSoftmaxWarps);
     }
-    mbar_init(bars.odone, 1);
-    mbar_init(bars.qfull, 1);
-    mbar_init(bars.qfree, kSoftmaxWarps);
+    mbar_init(&bars.odone[0], 1);
+    mbar_init(&bars.odone[1], 1);
     mbar_init(bars.qready, kSoftmaxWarps);
     mbar_init(bars.drain, 1);
     *abort_flag = 0;
@@ -229,11 +235,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUten
     tmem_alloc(tmem_holder, kTmemCols);
     tmem_relinquish();
   }
-  if (warp == kProducerWarp && lane == 0) {
-    tma_prefetch_desc(&tmq);
-    tma_prefetch_desc(&tmk);
-    tma_prefetch_desc(&tmv);
-  }
+  if (warp == kKProducerWarp && lane == 0) tma_prefetch_desc(&tmk);
+  if (warp == kVProducerWarp && lane == 0) tma_prefetch_desc(&tmv);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -242,38 +245,33 @@ tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUten
   const int cta = blockIdx.x, grid = gridDim.x;
   const Problem& p = prm.p;
 
-  if (warp == kProducerWarp) {
-    // ------------------------------------------------------------- producer
+  if (warp == kKProducerWarp || warp == kVProducerWarp) {
+    // ------------------------------------------------------------ producers
+    const bool is_k = warp == kKProducerWarp;
     if (lane == 0) {
-      int n = 0, lu = 0;
+      const int stages = is_k ? kKStages : kVRawStages;
+      int n = 0;
       for (int k = 0;; ++k) {
         const int u = unit_index(k, cta, grid);
         if (u >= prm.n_units) break;
         const Unit w = decode_unit(u, prm);
-        if (lu > 0 && !wait_bar(bars.qfree, (lu - 1) & 1, prm, abort_flag)) goto producer_done;
-        mbar_arrive_expect_tx(bars.qfull, kQBytes);
-        tma_load_3d(smem + kSmemQ, &tmq, bars.qfull, 0, w.g * kGroup, w.t0);
-        tma_load_3d(smem + kSmemQ + kQBytes / 2, &tmq, bars.qfull, 32, w.g * kGroup, w.t0);
         for (int j = 0; j < w.ntiles; ++j, ++n) {
-          const int j0 = j * kBc;
-          const int ks = n % kKStages;
-          if (n >= kKStages && !wait_bar(&bars.kempty[ks], ((n / kKStages) - 1) & 1, prm, abort_flag))
-            goto producer_done;
-          uint8_t* kdst = smem + kSmemK + ks * 2 * kKTileBytes;
-          if (!(prm.fault_skip_first_k && n == 0)) {
-            mbar_arrive_expect_tx(&bars.kfull[ks], kKTileBytes);
-            tma_load_2d(kdst, &tmk, &bars.kfull[ks], w.g * kD, j0);
-            tma_load_2d(kdst + kKTileBytes / 2, &tmk, &bars.kfull[ks], w.g * kD + 32, j0);
+          const int st = n % stages;
+          uint64_t* freed = is_k ? &bars.kempty[st] : &bars.vrfree[st];
+          if (n >= stages && !wait_bar(freed, ((n / stages) - 1) & 1, prm, abort_flag)) goto producer_done;
+          if (is_k) {
+            if (prm.fault_skip_first_k && n == 0) continue;
+            uint8_t* dst = smem + kSmemK + st * kKStageBytes;
+            mbar_arrive_expect_tx(&bars.kfull[st], 2 * kHalf);
+            tma_load_2d(dst, &tmk, &bars.kfull[st], w.g * kD, j * kBc);
+            tma_load_2d(dst + kRegion, &tmk, &bars.kfull[st], w.g * kD + 32, j * kBc);
+          } else {
+            uint8_t* dst = smem + kSmemVRaw + st * kVRawBytes;
+            mbar_arrive_expect_tx(&bars.vfull[st], kVRawBytes);
+            tma_load_2d(dst, &tmv, &bars.vfull[st], w.g * kD, j * kBc);
+            tma_load_2d(dst + kHalf, &tmv, &bars.vfull[st], w.g * kD + 32, j * kBc);
           }
-          const int vs = n % kVRawStages;
-          if (n >= kVRawStages && !wait_bar(&bars.vrfree[vs], ((n / kVRawStages) - 1) & 1, prm, abort_flag))
-            goto producer_done;
-          uint8_t* vdst = smem + kSmemVRaw + vs * kKTileBytes;
-          mbar_arrive_expect_tx(&bars.vfull[vs], kKTileBytes);
-          tma_load_2d(vdst, &tmv, &bars.vfull[vs], w.g * kD, j0);
-          tma_load_2d(vdst + kKTileBytes / 2, &tmv, &bars.vfull[vs], w.g * kD + 32, j0);
         }
-        ++lu;
       }
     producer_done:
       if (*abort_flag) {
@@ -283,6 +281,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUten
         while (globaltimer_ns() - t0 < 200000ull) __nanosleep(1000);
       }
     }
+    __syncwarp();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA
     if (lane == 0) {
@@ -291,18 +290,16 @@ tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUten
         const int ks = m % kKStages;
         if (!wait_bar(&bars.kconv[ks], (m / kKStages) & 1, prm, abort_flag)) return false;
         tc_fence_after();
-        const uint32_t kb = smem_u32(smem + kSmemK + ks * 2 * kKTileBytes);
-        const uint32_t klo = kb + kKTileBytes;
-        const uint32_t d = tmem + kColS + (m & 1) * 64;
+        const uint32_t kb = smem_u32(smem + kSmemK + ks * kKStageBytes);
+        const uint32_t d = tmem + kColS + (m & 1) * 128;
 #pragma unroll
-        for (int s = 0; s < 8; ++s)
-          mma_tf32_ts(d, tmem + kColQhi + s * 8, sdesc_sw128(kb + (s >> 2) * 8192 + (s & 3) * 32), kIdesc, s > 0);
+        for (int s = 0; s < 8; ++s)  // [Q_hi K_hi^T | Q_hi K_lo^T]
+          mma_tf32_ts(d, tmem + kColQhi + s * 8, sdesc_sw128(kb + (s >> 2) * kRegion + (s & 3) * 32),
+                      kIdescN128, s > 0);
 #pragma unroll
-        for (int s = 0; s < 8; ++s)
-          mma_tf32_ts(d, tmem + kColQhi + s * 8, sdesc_sw128(klo + (s >> 2) * 8192 + (s & 3) * 32), kIdesc, 1);
-#pragma unroll
-        for (int s = 0; s < 8; ++s)
-          mma_tf32_ts(d, tmem + kColQlo + s * 8, sdesc_sw128(kb + (s >> 2) * 8192 + (s & 3) * 32), kIdesc, 1);
+        for (int s = 0; s < 8; ++s)  // += Q_lo K_hi^T into the first half
+          mma_tf32_ts(d, tmem + kColQlo + s * 8, sdesc_sw128(kb + (s >> 2) * kRegion + (s & 3) * 32),
+                      kIdescN64, 1);
         mma_commit(&bars.sfull[m & 1]);
         mma_commit(&bars.kempty[ks]);
         return true;
@@ -311,21 +308,18 @@ tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUten
         const int vs = m % kVStages;
         if (!wait_bar(&bars.vconv[vs], (m / kVStages) & 1, prm, abort_flag)) return false;
         tc_fence_after();
-        const uint32_t vhi = smem_u32(smem + kSmemVT + vs * 2 * kKTileBytes);
-        const uint32_t vlo = vhi + kKTileBytes;
-        const uint32_t phi = tmem + kColS + (m & 1) * 64;
-        const uint32_t plo = tmem + kColPlo + (m & 1) * 64;
+        const uint32_t vt = smem_u32(smem + kSmemVT + vs * kVStageBytes);
+        const uint32_t phi = tmem + kColS + (m & 1) * 128;
+        const uint32_t plo = phi + 64;
 #pragma unroll
-        for (int s = 0; s < 8; ++s)
-          mma_tf32_ts(tmem + kColO, phi + s * 8, sdesc_sw128(vhi + (s >> 2) * 8192 + (s & 3) * 32), kIdesc,
-                      (first && s == 0) ? 0u : 1u);
+        for (int s = 0; s < 8; ++s)  // [P_hi V_hi | P_hi V_lo]
+          mma_tf32_ts(tmem + kColO, phi + s * 8, sdesc_sw128(vt + (s >> 2) * kRegion + (s & 3) * 32),
+                      kIdescN128, (first && s == 0) ? 0u : 1u);
 #pragma unroll
-        for (int s = 0; s < 8; ++s)
-          mma_tf32_ts(tmem + kColO, phi + s * 8, sdesc_sw128(vlo + (s >> 2) * 8192 + (s & 3) * 32), kIdesc, 1);
-#pragma unroll
-        for (int s = 0; s < 8; ++s)
-          mma_tf32_ts(tmem + kColO, plo + s * 8, sdesc_sw128(vhi + (s >> 2) * 8192 + (s & 3) * 32), kIdesc, 1);
-        mma_commit(bars.odone);
+        for (int s = 0; s < 8; ++s)  // += P_lo V_hi into the first half
+          mma_tf32_ts(tmem + kColO, plo + s * 8, sdesc_sw128(vt + (s >> 2) * kRegion + (s & 3) * 32),
+                      kIdescN64, 1);
+        mma_commit(&bars.odone[m & 1]);
         mma_commit(&bars.vempty[vs]);
         return true;
       };
@@ -337,6 +331,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUten
         tc_fence_after();
         for (int j = 0; j < w.ntiles; ++j, ++n) {
           if (j == 0 && !issue_qk(n)) goto mma_done;
+          // QK(n+1) goes ahead of PV(n) so that the softmax of tile n+1
+          // overlaps PV(n) on the tensor pipe.
           if (j + 1 < w.ntiles && !issue_qk(n + 1)) goto mma_done;
           if (!wait_bar(&bars.pfull[n & 1], (n >> 1) & 1, prm, abort_flag)) goto mma_done;
           tc_fence_after();
@@ -354,65 +350,90 @@ tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUten
       }
     }
     __syncwarp();
-  } else if (warp >= kFirstConvWarp) {
-    // ----------------------------------------------------------- converters
-    const int cw = warp - kFirstConvWarp;
-    const int ct = threadIdx.x - kFirstConvWarp * 32;
+  } else if (warp == kKConvWarp) {
+    // ---------------------------------------------------------- K converter
+    // K lo = K - tf32_hi(K) into the lower half of each d-half region. The
+    // tensor core reads raw K as tf32_hi(K) by itself: it ignores the 13 low
+    // mantissa bits of an fp32 operand (measured on GB300: 1 + 3 * 2^-12
+    // reads as 1 from shared memory and from TMEM).
     int n = 0;
     for (int k = 0;; ++k) {
       const int u = unit_index(k, cta, grid);
       if (u >= prm.n_units) break;
       const Unit w = decode_unit(u, prm);
       for (int j = 0; j < w.ntiles; ++j, ++n) {
-        // K: lo = K - tf32_hi(K), same swizzled layout; hi in place unless the
-        // tensor core truncates by itself.
         const int ks = n % kKStages;
-        if (!wait_bar_warp(&bars.kfull[ks], (n / kKStages) & 1, prm, abort_flag)) goto conv_done;
-        {
-          uint8_t* kb = smem + kSmemK + ks * 2 * kKTileBytes;
+        if (!wait_bar_warp(&bars.kfull[ks], (n / kKStages) & 1, prm, abort_flag)) goto kconv_done;
+        uint8_t* kb = smem + kSmemK + ks * kKStageBytes;
+        // Two batches of 16 independent 16-byte loads, then their stores.
 #pragma unroll
-          for (int i = 0; i < kKTileBytes / 16 / (kConvWarps * 32); ++i) {
-            const uint32_t off = (uint32_t)(ct + i * kConvWarps * 32) * 16u;
-            float4 x = *reinterpret_cast<const float4*>(kb + off);
-            float4 hi = make_float4(tf32_hi(x.x), tf32_hi(x.y), tf32_hi(x.z), tf32_hi(x.w));
-            *reinterpret_cast<float4*>(kb + kKTileBytes + off) =
-                make_float4(x.x - hi.x, x.y - hi.y, x.z - hi.z, x.w - hi.w);
-            if (!kHwTruncatesTf32) *reinterpret_cast<float4*>(kb + off) = hi;
+        for (int b = 0; b < 2; ++b) {
+          float4 x[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const uint32_t idx = (uint32_t)(lane + 32 * (b * 16 + i));  // 16-byte chunk, 0..1023
+            x[i] = *reinterpret_cast<const float4*>(kb + (idx >> 9) * kRegion + (idx & 511u) * 16u);
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const uint32_t idx = (uint32_t)(lane + 32 * (b * 16 + i));
+            *reinterpret_cast<float4*>(kb + (idx >> 9) * kRegion + (idx & 511u) * 16u + kHalf) =
+                make_float4(x[i].x - tf32_hi(x[i].x), x[i].y - tf32_hi(x[i].y), x[i].z - tf32_hi(x[i].z),
+                            x[i].w - tf32_hi(x[i].w));
           }
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.kconv[ks]);
-
-        // V: raw [key][d] (two d-half regions) -> V^T hi / lo [d][key] (two
-        // key-half regions). Lane = key within a 32-key half; this warp takes
-        // head-dimension chunks 4 cw .. 4 cw + 3.
+      }
+    }
+  kconv_done:;
+  } else if (warp >= kFirstVConvWarp) {
+    // ---------------------------------------------------------- V converters
+    // Raw V [key][d] (two d-half regions of 64 keys) -> V^T [d][key] in two
+    // key-half regions, hi rows 0-63 and lo rows 64-127. This warp takes the
+    // d-half cw; a lane owns 4 keys x 4 head dimensions per round and turns
+    // four 16-byte row loads into four 16-byte transposed stores (hi and lo).
+    // With lane = 8 dsub + kq, a store instruction covers 4 V^T rows x 8 key
+    // quads (conflict-free) and a load instruction 8 keys x 4 d-quads.
+    const int cw = warp - kFirstVConvWarp;
+    const int dsub = lane >> 3, kq = lane & 7;
+    int n = 0;
+    for (int k = 0;; ++k) {
+      const int u = unit_index(k, cta, grid);
+      if (u >= prm.n_units) break;
+      const Unit w = decode_unit(u, prm);
+      for (int j = 0; j < w.ntiles; ++j, ++n) {
         const int vr = n % kVRawStages;
         const int vs = n % kVStages;
-        if (!wait_bar_warp(&bars.vfull[vr], (n / kVRawStages) & 1, prm, abort_flag)) goto conv_done;
+        if (!wait_bar_warp(&bars.vfull[vr], (n / kVRawStages) & 1, prm, abort_flag)) goto vconv_done;
         if (n >= kVStages && !wait_bar_warp(&bars.vempty[vs], ((n / kVStages) - 1) & 1, prm, abort_flag))
-          goto conv_done;
-        {
-          const uint8_t* vraw = smem + kSmemVRaw + vr * kKTileBytes;
-          uint8_t* vthi = smem + kSmemVT + vs * 2 * kKTileBytes;
-          uint8_t* vtlo = vthi + kKTileBytes;
+          goto vconv_done;
+        const uint8_t* vraw = smem + kSmemVRaw + vr * kVRawBytes + cw * kHalf;  // this warp's d-half
+        uint8_t* vt = smem + kSmemVT + vs * kVStageBytes;
+        float4 x[4][4];  // [round][key within the quad]
 #pragma unroll
-          for (int kh = 0; kh < 2; ++kh) {
-            const int key = kh * 32 + lane;
+        for (int rd = 0; rd < 4; ++rd) {
+          const uint32_t d4 = (uint32_t)((rd & 1) * 4 + dsub);            // d-quad within the half
+          const uint32_t key0 = (uint32_t)((rd >> 1) * 32 + kq * 4);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const int d4 = cw * 4 + c;  // 4 head dimensions 4 d4 .. 4 d4 + 3
-              const float4 x = *reinterpret_cast<const float4*>(
-                  vraw + (d4 >> 3) * 8192 + sw128((uint32_t)key * 128u + (uint32_t)(d4 & 7) * 16u));
-              const float xs[4] = {x.x, x.y, x.z, x.w};
+          for (int r = 0; r < 4; ++r)
+            x[rd][r] = *reinterpret_cast<const float4*>(vraw + sw128((key0 + r) * 128u + d4 * 16u));
+        }
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const uint32_t off = kh * 8192 + sw128((uint32_t)(d4 * 4 + i) * 128u + (uint32_t)lane * 4u);
-                const float hi = tf32_hi(xs[i]);
-                *reinterpret_cast<float*>(vthi + off) = hi;
-                *reinterpret_cast<float*>(vtlo + off) = xs[i] - hi;
-              }
-            }
+        for (int rd = 0; rd < 4; ++rd) {
+          const uint32_t kh = (uint32_t)(rd >> 1);
+          const uint32_t d0 = (uint32_t)(cw * 32) + 4u * (uint32_t)((rd & 1) * 4 + dsub);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float e0 = i == 0 ? x[rd][0].x : i == 1 ? x[rd][0].y : i == 2 ? x[rd][0].z : x[rd][0].w;
+            const float e1 = i == 0 ? x[rd][1].x : i == 1 ? x[rd][1].y : i == 2 ? x[rd][1].z : x[rd][1].w;
+            const float e2 = i == 0 ? x[rd][2].x : i == 1 ? x[rd][2].y : i == 2 ? x[rd][2].z : x[rd][2].w;
+            const float e3 = i == 0 ? x[rd][3].x : i == 1 ? x[rd][3].y : i == 2 ? x[rd][3].z : x[rd][3].w;
+            const float4 hi = make_float4(tf32_hi(e0), tf32_hi(e1), tf32_hi(e2), tf32_hi(e3));
+            const uint32_t off = kh * kRegion + sw128((d0 + (uint32_t)i) * 128u + (uint32_t)kq * 16u);
+            *reinterpret_cast<float4*>(vt + off) = hi;
+            *reinterpret_cast<float4*>(vt + off + kHalf) = make_float4(e0 - hi.x, e1 - hi.y, e2 - hi.z, e3 - hi.w);
           }
         }
         fence_proxy_async_smem();
@@ -423,44 +444,44 @@ tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUten
         }
       }
     }
-  conv_done:;
+  vconv_done:;
   } else {
     // -------------------------------------------------- softmax (warps 0-3)
     const int row = warp * 32 + lane;  // TMEM lane
     const uint32_t lane_tmem = tmem + ((uint32_t)(warp * 32) << 16);
-    const float c = kLog2e * kScale;   // exp(s / 8) = 2^(s c)
+    const float c = kLog2e * kScale;     // exp(s / 8) = 2^(s c)
     const float stale = kStaleLog2 / c;  // in raw-score units
-    int n = 0, lu = 0;
-    uint32_t od = 0;  // PV completions consumed
+    int n = 0;
 
-    // Split the unit's Q tile (staged by TMA, 128-byte swizzled) into TMEM.
-    auto load_q = [&](int which) -> bool {
-      if (!wait_bar_warp(bars.qfull, which & 1, prm, abort_flag)) return false;
-      float hi[32], lo[32];
+    // This row's query (zeros past the chunk), split into TMEM.
+    auto load_q = [&](const Unit& w) {
+      const int pos = w.t0 + (row >> 2);
+      const float* src = p.q + ((size_t)pos * kHQ + w.g * kGroup + (row & 3)) * kD;
+      float x[64];
 #pragma unroll
-      for (int dh = 0; dh < 2; ++dh) {
-        const uint8_t* src = smem + kSmemQ + dh * (kQBytes / 2);
+      for (int i = 0; i < 64; i += 4) {
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (pos < p.C) v = __ldg(reinterpret_cast<const float4*>(src + i));
+        x[i] = v.x;
+        x[i + 1] = v.y;
+        x[i + 2] = v.z;
+        x[i + 3] = v.w;
+      }
 #pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
-          const float4 x = *reinterpret_cast<const float4*>(src + sw128((uint32_t)row * 128u + (uint32_t)c4 * 16u));
-          const float xs[4] = {x.x, x.y, x.z, x.w};
+      for (int half = 0; half < 2; ++half) {
+        float hi[32], lo[32];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            hi[c4 * 4 + i] = tf32_hi(xs[i]);
-            lo[c4 * 4 + i] = xs[i] - hi[c4 * 4 + i];
-          }
+        for (int i = 0; i < 32; ++i) {
+          hi[i] = tf32_hi(x[half * 32 + i]);
+          lo[i] = x[half * 32 + i] - hi[i];
         }
-        tmem_st32(lane_tmem + kColQhi + dh * 32, hi);
-        tmem_st32(lane_tmem + kColQlo + dh * 32, lo);
+        tmem_st32(lane_tmem + kColQhi + half * 32, hi);
+        tmem_st32(lane_tmem + kColQlo + half * 32, lo);
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bars.qfree);
-        mbar_arrive(bars.qready);
-      }
-      return true;
+      if (lane == 0) mbar_arrive(bars.qready);
     };
 
     bool q_loaded = false;
@@ -468,22 +489,24 @@ tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUten
       const int u = unit_index(k, cta, grid);
       if (u >= prm.n_units) break;
       const Unit w = decode_unit(u, prm);
-      if (!q_loaded && !load_q(lu)) goto softmax_done;
+      if (!q_loaded) load_q(w);
       q_loaded = false;
       float m_ref = -INFINITY, l = 0.f;
       const int pos = w.t0 + (row >> 2);
       const int limit = p.P + pos;  // last visible key of this row
       for (int j = 0; j < w.ntiles; ++j, ++n) {
         const int j0 = j * kBc;
+        const uint32_t sbuf = lane_tmem + kColS + (n & 1) * 128;
         if (!wait_bar_warp(&bars.sfull[n & 1], (n >> 1) & 1, prm, abort_flag)) goto softmax_done;
         tc_fence_after();
         float s[64];
         {
-          float* s0 = s;
-          float* s1 = s + 32;
-          tmem_ld32(lane_tmem + kColS + (n & 1) * 64, *reinterpret_cast<float(*)[32]>(s0));
-          tmem_ld32(lane_tmem + kColS + (n & 1) * 64 + 32, *reinterpret_cast<float(*)[32]>(s1));
+          float t[64];
+          tmem_ld64(sbuf, s);
+          tmem_ld64(sbuf + 64, t);
           tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 64; ++i) s[i] += t[i];
         }
         if (j0 + kBc - 1 > p.P + w.t0) {
 #pragma unroll
@@ -511,25 +534,27 @@ tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUten
             hi[i] = tf32_hi(pj);
             lo[i] = pj - hi[i];
           }
-          tmem_st32(lane_tmem + kColS + (n & 1) * 64 + half * 32, hi);
-          tmem_st32(lane_tmem + kColPlo + (n & 1) * 64 + half * 32, lo);
+          tmem_st32(sbuf + half * 32, hi);
+          tmem_st32(sbuf + 64 + half * 32, lo);
         }
         l = fmaf(l, alpha, lsum);
         tmem_wait_st();
-        if (j > 0) {
-          // PV of the previous tile must be complete before O is touched.
-          if (!wait_bar_warp(bars.odone, od & 1, prm, abort_flag)) goto softmax_done;
-          ++od;
+        // O is rescaled only when the reference maximum moved; PV(n-1) must be
+        // complete first. Skipping this wait otherwise is safe for the parity
+        // bookkeeping: PV(n+1) cannot run before this warp releases P(n+1), so
+        // odone[(n-1) & 1] is at most one phase past the one waited for here.
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          if (!wait_bar_warp(&bars.odone[(n - 1) & 1], ((n - 1) >> 1) & 1, prm, abort_flag)) goto softmax_done;
           tc_fence_after();
-          if (__any_sync(0xffffffffu, alpha != 1.f)) {
-            float o[32];
+          {
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              tmem_ld32(lane_tmem + kColO + half * 32, o);
+            for (int part = 0; part < 4; ++part) {
+              float o[32];
+              tmem_ld32(lane_tmem + kColO + part * 32, o);
               tmem_wait_ld();
 #pragma unroll
               for (int i = 0; i < 32; ++i) o[i] *= alpha;
-              tmem_st32(lane_tmem + kColO + half * 32, o);
+              tmem_st32(lane_tmem + kColO + part * 32, o);
             }
             tmem_wait_st();
           }
@@ -542,31 +567,31 @@ tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUten
       {
         const int u_next = unit_index(k + 1, cta, grid);
         if (u_next < prm.n_units) {
-          if (!load_q(lu + 1)) goto softmax_done;
+          load_q(decode_unit(u_next, prm));
           q_loaded = true;
         }
       }
-      // Epilogue: wait for the last PV, one division per element.
-      if (!wait_bar_warp(bars.odone, od & 1, prm, abort_flag)) goto softmax_done;
-      ++od;
+      // Epilogue: wait for the last PV, sum the two halves, one division per element.
+      if (!wait_bar_warp(&bars.odone[(n - 1) & 1], ((n - 1) >> 1) & 1, prm, abort_flag)) goto softmax_done;
       tc_fence_after();
       {
         float* dst = p.out + ((size_t)pos * kHQ + w.g * kGroup + (row & 3)) * kD;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-          float o[32];
-          tmem_ld32(lane_tmem + kColO + half * 32, o);
+          float a[32], b[32];
+          tmem_ld32(lane_tmem + kColO + half * 32, a);
+          tmem_ld32(lane_tmem + kColO + 64 + half * 32, b);
           tmem_wait_ld();
           if (pos < p.C) {
 #pragma unroll
             for (int i = 0; i < 32; i += 4)
               *reinterpret_cast<float4*>(dst + half * 32 + i) =
-                  make_float4(o[i] / l, o[i + 1] / l, o[i + 2] / l, o[i + 3] / l);
+                  make_float4((a[i] + b[i]) / l, (a[i + 1] + b[i + 1]) / l, (a[i + 2] + b[i + 2]) / l,
+                              (a[i + 3] + b[i + 3]) / l);
           }
         }
       }
       tc_fence_before();
-      ++lu;
     }
   softmax_done:;
   }
@@ -596,30 +621,16 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
   return fn;
 }
 
-int encode_maps(const Problem& p, CUtensorMap* mq, CUtensorMap* mk, CUtensorMap* mv) {
+// k, v [T][8][64] as a 2-D tensor (head * 64 + d, position); a box is 32
+// floats (one 128-byte swizzle row) x 64 keys.
+int encode_kv_map(const float* base, int T, CUtensorMap* map) {
   auto enc = get_encoder();
   if (!enc) return ATTN_ETMA;
-  const cuuint32_t ones[3] = {1, 1, 1};
-  // q [C][32][64] as (d, head, position); a box is 32 d x 4 heads x 32 positions.
-  {
-    const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)kHQ, (cuuint64_t)p.C};
-    const cuuint64_t strides[2] = {(cuuint64_t)kD * 4, (cuuint64_t)kHQ * kD * 4};
-    const cuuint32_t box[3] = {32, (cuuint32_t)kGroup, (cuuint32_t)kBq};
-    if (enc(mq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(p.q), dims, strides, box, ones,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return ATTN_ETMA;
-  }
-  // k, v [T][8][64] as (head * 64 + d, position); a box is 32 floats x 64 keys.
-  const cuuint64_t T = (cuuint64_t)p.P + (cuuint64_t)p.C;
-  const cuuint64_t dims[2] = {(cuuint64_t)kHKV * kD, T};
+  const cuuint32_t ones[2] = {1, 1};
+  const cuuint64_t dims[2] = {(cuuint64_t)kHKV * kD, (cuuint64_t)T};
   const cuuint64_t strides[1] = {(cuuint64_t)kHKV * kD * 4};
   const cuuint32_t box[2] = {32, (cuuint32_t)kBc};
-  if (enc(mk, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(p.k), dims, strides, box, ones,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return ATTN_ETMA;
-  if (enc(mv, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(p.v), dims, strides, box, ones,
+  if (enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, ones,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return ATTN_ETMA;
@@ -644,8 +655,9 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
       return ATTN_ECUDA;
     st.ready = true;
   }
-  alignas(64) CUtensorMap mq, mk, mv;
-  const int rc = encode_maps(p, &mq, &mk, &mv);
+  alignas(64) CUtensorMap mk, mv;
+  int rc = encode_kv_map(p.k, p.P + p.C, &mk);
+  if (rc == ATTN_OK) rc = encode_kv_map(p.v, p.P + p.C, &mv);
   if (rc != ATTN_OK) return rc;
   Params prm;
   prm.p = p;
@@ -654,7 +666,7 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
   prm.timeout_ns = timeout_ns;
   prm.fault_skip_first_k = fault;
   const int grid = prm.n_units < st.num_sms ? prm.n_units : st.num_sms;
-  tc_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(mq, mk, mv, prm);
+  tc_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(mk, mv, prm);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ELAUNCH;
 }
 
