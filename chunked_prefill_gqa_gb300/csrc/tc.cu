@@ -27,15 +27,18 @@
 // Q and P are TMEM operands (P hi and P lo overwrite the S columns they came
 // from); K and V^T are 128-byte-swizzled K-major shared-memory operands.
 //
-// Warp roles (10 warps):
-//   0-3  softmax: own TMEM lanes 0-127 (one row each); load and split Q into
-//        TMEM at the start of a unit; per tile read S, mask, online softmax,
-//        write P hi/lo, rescale O when the reference maximum moves; epilogue.
-//   4    K producer: TMA loads of K tiles into the K ring.
-//   5    MMA: allocates TMEM; one lane issues every tcgen05.mma and commit.
-//   6    V producer: TMA loads of V tiles into the raw V ring.
-//   7    K converter: K lo next to each K tile.
-//   8-9  V converters: raw V -> V^T hi / V^T lo.
+// Warp roles (15 warps):
+//   0-7   softmax: warp w owns TMEM lanes 32 (w % 4) .. + 31 (one row per
+//         thread) and the keys 32 (w / 4) .. + 31 of every tile; the two
+//         warps of a row set exchange their partial row maxima through shared
+//         memory. They load and split Q into TMEM at the start of a unit, run
+//         the online softmax, write P hi/lo, rescale O when the reference
+//         maximum moves, and write the output.
+//   8     K producer: TMA loads of K tiles into the K ring.
+//   9     MMA: allocates TMEM; one lane issues every tcgen05.mma and commit.
+//   10    V producer: TMA loads of V tiles into the raw V ring.
+//   11-12 K converters: K lo next to each K tile (one d-half each).
+//   13-14 V converters: raw V -> V^T hi / V^T lo (one d-half each).
 // Every wait is bounded; on expiry the kernel records ATTN_ETIMEOUT in the
 // device error word, all roles wind down, and TMEM is freed.
 #include <cuda.h>
@@ -53,15 +56,16 @@ constexpr int kBq = 32;           // chunk positions per unit
 constexpr int kM = kBq * kGroup;  // 128 rows = TMEM lanes
 constexpr int kBc = 64;           // keys per tile
 constexpr int kKStages = 3;       // K ring: [K | K lo] per d-half region
-constexpr int kVRawStages = 4;    // raw V landing ring
+constexpr int kVRawStages = 3;    // raw V landing ring
 constexpr int kVStages = 2;       // V^T ring: [V^T hi | V^T lo] per key-half region
 
-constexpr int kSoftmaxWarps = 4;
-constexpr int kKProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kVProducerWarp = 6;
-constexpr int kKConvWarp = 7;
-constexpr int kFirstVConvWarp = 8;
+constexpr int kSoftmaxWarps = 8;
+constexpr int kKProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kVProducerWarp = 10;
+constexpr int kFirstKConvWarp = 11;
+constexpr int kKConvWarps = 2;
+constexpr int kFirstVConvWarp = 13;
 constexpr int kVConvWarps = 2;
 constexpr int kThreads = 32 * (kFirstVConvWarp + kVConvWarps);
 
@@ -84,8 +88,10 @@ constexpr uint32_t kSmemK = 0;
 constexpr uint32_t kSmemVRaw = kSmemK + kKStages * kKStageBytes;
 constexpr uint32_t kSmemVT = kSmemVRaw + kVRawStages * kVRawBytes;
 constexpr uint32_t kSmemBar = kSmemVT + kVStages * kVStageBytes;
-constexpr uint32_t kNumBars = 3 * kKStages + 2 * kVRawStages + 2 * kVStages + 2 + 2 + 2 + 2;
-constexpr uint32_t kSmemTotal = kSmemBar + kNumBars * 8 + 16;
+constexpr uint32_t kNumBars = 3 * kKStages + 2 * kVRawStages + 2 * kVStages + 2 + 2 + 2 + 2 + 4;
+constexpr uint32_t kSmemRed = kSmemBar + kNumBars * 8 + 16;  // [2 tile parities][2 key halves][128 rows]
+constexpr uint32_t kSmemLsum = kSmemRed + 2 * 2 * 128 * 4;   // [2 key halves][128 rows]
+constexpr uint32_t kSmemTotal = kSmemLsum + 2 * 128 * 4;
 constexpr uint32_t kSmemAlloc = kSmemTotal + 1024;  // slack to align the base
 
 static_assert(kSmemAlloc <= 232448, "exceeds the 227 KB per-block shared memory limit");
@@ -119,6 +125,7 @@ struct Bars {
   uint64_t* odone;   // [2] PV(n) done, barrier n & 1 (MMA commit)
   uint64_t* qready;  // Q hi/lo in TMEM (softmax warps)
   uint64_t* drain;   // MMA drain on abort
+  uint64_t* pair;    // [4] the two softmax warps of a row quarter exchange partial results
 };
 
 __device__ __forceinline__ Bars carve_bars(uint8_t* base) {
@@ -136,6 +143,7 @@ __device__ __forceinline__ Bars carve_bars(uint8_t* base) {
   r.odone = b; b += 2;
   r.qready = b++;
   r.drain = b++;
+  r.pair = b; b += 4;
   return r;
 }
 
@@ -209,7 +217,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
   if (threadIdx.x == 0) {
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(&bars.kfull[s], 1);
-      mbar_init(&bars.kconv[s], 1);
+      mbar_init(&bars.kconv[s], kKConvWarps);
       mbar_init(&bars.kempty[s], 1);
     }
     for (int s = 0; s < kVRawStages; ++s) {
@@ -228,6 +236,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
     mbar_init(&bars.odone[1], 1);
     mbar_init(bars.qready, kSoftmaxWarps);
     mbar_init(bars.drain, 1);
+    for (int q = 0; q < 4; ++q) mbar_init(&bars.pair[q], 2);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -350,12 +359,13 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
       }
     }
     __syncwarp();
-  } else if (warp == kKConvWarp) {
-    // ---------------------------------------------------------- K converter
-    // K lo = K - tf32_hi(K) into the lower half of each d-half region. The
-    // tensor core reads raw K as tf32_hi(K) by itself: it ignores the 13 low
-    // mantissa bits of an fp32 operand (measured on GB300: 1 + 3 * 2^-12
-    // reads as 1 from shared memory and from TMEM).
+  } else if (warp >= kFirstKConvWarp && warp < kFirstKConvWarp + kKConvWarps) {
+    // ---------------------------------------------------------- K converters
+    // K lo = K - tf32_hi(K) into the lower half of each d-half region; warp
+    // kc takes region kc. The tensor core reads raw K as tf32_hi(K) by itself:
+    // it ignores the 13 low mantissa bits of an fp32 operand (measured on
+    // GB300: 1 + 3 * 2^-12 reads as 1 from shared memory and from TMEM).
+    const int kc = warp - kFirstKConvWarp;
     int n = 0;
     for (int k = 0;; ++k) {
       const int u = unit_index(k, cta, grid);
@@ -364,24 +374,15 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
       for (int j = 0; j < w.ntiles; ++j, ++n) {
         const int ks = n % kKStages;
         if (!wait_bar_warp(&bars.kfull[ks], (n / kKStages) & 1, prm, abort_flag)) goto kconv_done;
-        uint8_t* kb = smem + kSmemK + ks * kKStageBytes;
-        // Two batches of 16 independent 16-byte loads, then their stores.
+        uint8_t* kb = smem + kSmemK + ks * kKStageBytes + kc * kRegion;
+        float4 x[16];
 #pragma unroll
-        for (int b = 0; b < 2; ++b) {
-          float4 x[16];
+        for (int i = 0; i < 16; ++i) x[i] = *reinterpret_cast<const float4*>(kb + (uint32_t)(lane + 32 * i) * 16u);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const uint32_t idx = (uint32_t)(lane + 32 * (b * 16 + i));  // 16-byte chunk, 0..1023
-            x[i] = *reinterpret_cast<const float4*>(kb + (idx >> 9) * kRegion + (idx & 511u) * 16u);
-          }
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const uint32_t idx = (uint32_t)(lane + 32 * (b * 16 + i));
-            *reinterpret_cast<float4*>(kb + (idx >> 9) * kRegion + (idx & 511u) * 16u + kHalf) =
-                make_float4(x[i].x - tf32_hi(x[i].x), x[i].y - tf32_hi(x[i].y), x[i].z - tf32_hi(x[i].z),
-                            x[i].w - tf32_hi(x[i].w));
-          }
-        }
+        for (int i = 0; i < 16; ++i)
+          *reinterpret_cast<float4*>(kb + (uint32_t)(lane + 32 * i) * 16u + kHalf) =
+              make_float4(x[i].x - tf32_hi(x[i].x), x[i].y - tf32_hi(x[i].y), x[i].z - tf32_hi(x[i].z),
+                          x[i].w - tf32_hi(x[i].w));
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.kconv[ks]);
@@ -446,38 +447,48 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
     }
   vconv_done:;
   } else {
-    // -------------------------------------------------- softmax (warps 0-3)
-    const int row = warp * 32 + lane;  // TMEM lane
-    const uint32_t lane_tmem = tmem + ((uint32_t)(warp * 32) << 16);
+    // -------------------------------------------------- softmax (warps 0-7)
+    const int rq = warp & 3;           // row quarter: TMEM lanes 32 rq .. 32 rq + 31
+    const int kh = warp >> 2;          // key half of every tile: keys 32 kh .. 32 kh + 31
+    const int row = rq * 32 + lane;    // TMEM lane = row of the unit
+    const uint32_t lane_tmem = tmem + ((uint32_t)(rq * 32) << 16);
+    float* red = reinterpret_cast<float*>(smem + kSmemRed);    // partial maxima
+    float* lred = reinterpret_cast<float*>(smem + kSmemLsum);  // partial sums
     const float c = kLog2e * kScale;     // exp(s / 8) = 2^(s c)
     const float stale = kStaleLog2 / c;  // in raw-score units
     int n = 0;
 
-    // This row's query (zeros past the chunk), split into TMEM.
+    // The two warps of a row set exchange partial results through shared
+    // memory and meet on the mbarrier pair[rq] (one arrival per warp, bounded
+    // wait). Neither warp can get two exchanges ahead of its partner, so the
+    // phase parity identifies the exchange.
+    uint32_t pc = 0;  // exchanges done
+    auto pair_sync = [&]() -> bool {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.pair[rq]);
+      const bool ok = wait_bar_warp(&bars.pair[rq], pc & 1, prm, abort_flag);
+      ++pc;
+      return ok;
+    };
+
+    // This warp's half of the row's query (zeros past the chunk), split into TMEM.
     auto load_q = [&](const Unit& w) {
       const int pos = w.t0 + (row >> 2);
-      const float* src = p.q + ((size_t)pos * kHQ + w.g * kGroup + (row & 3)) * kD;
-      float x[64];
+      const float* src = p.q + ((size_t)pos * kHQ + w.g * kGroup + (row & 3)) * kD + kh * 32;
+      float hi[32], lo[32];
 #pragma unroll
-      for (int i = 0; i < 64; i += 4) {
+      for (int i = 0; i < 32; i += 4) {
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         if (pos < p.C) v = __ldg(reinterpret_cast<const float4*>(src + i));
-        x[i] = v.x;
-        x[i + 1] = v.y;
-        x[i + 2] = v.z;
-        x[i + 3] = v.w;
-      }
+        const float xs[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float hi[32], lo[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          hi[i] = tf32_hi(x[half * 32 + i]);
-          lo[i] = x[half * 32 + i] - hi[i];
+        for (int t = 0; t < 4; ++t) {
+          hi[i + t] = tf32_hi(xs[t]);
+          lo[i + t] = xs[t] - hi[i + t];
         }
-        tmem_st32(lane_tmem + kColQhi + half * 32, hi);
-        tmem_st32(lane_tmem + kColQlo + half * 32, lo);
       }
+      tmem_st32(lane_tmem + kColQhi + kh * 32, hi);
+      tmem_st32(lane_tmem + kColQlo + kh * 32, lo);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -491,31 +502,37 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
       const Unit w = decode_unit(u, prm);
       if (!q_loaded) load_q(w);
       q_loaded = false;
-      float m_ref = -INFINITY, l = 0.f;
+      float m_ref = -INFINITY, l = 0.f;  // l: this warp's share of the row sum
       const int pos = w.t0 + (row >> 2);
       const int limit = p.P + pos;  // last visible key of this row
       for (int j = 0; j < w.ntiles; ++j, ++n) {
-        const int j0 = j * kBc;
-        const uint32_t sbuf = lane_tmem + kColS + (n & 1) * 128;
+        const int j0 = j * kBc + kh * 32;  // first key of this warp's half
+        const uint32_t sbuf = lane_tmem + kColS + (n & 1) * 128 + kh * 32;
         if (!wait_bar_warp(&bars.sfull[n & 1], (n >> 1) & 1, prm, abort_flag)) goto softmax_done;
         tc_fence_after();
-        float s[64];
+        float s[32];
         {
-          float t[64];
-          tmem_ld64(sbuf, s);
-          tmem_ld64(sbuf + 64, t);
+          float t[32];
+          tmem_ld32(sbuf, s);
+          tmem_ld32(sbuf + 64, t);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 64; ++i) s[i] += t[i];
+          for (int i = 0; i < 32; ++i) s[i] += t[i];
         }
-        if (j0 + kBc - 1 > p.P + w.t0) {
+        if (j * kBc + kBc - 1 > p.P + w.t0) {
 #pragma unroll
-          for (int i = 0; i < 64; ++i)
+          for (int i = 0; i < 32; ++i)
             if (j0 + i > limit) s[i] = -INFINITY;
         }
         float mt = s[0];
 #pragma unroll
-        for (int i = 1; i < 64; ++i) mt = fmaxf(mt, s[i]);
+        for (int i = 1; i < 32; ++i) mt = fmaxf(mt, s[i]);
+        {
+          float* slot = red + (n & 1) * 256;
+          slot[kh * 128 + row] = mt;
+          if (!pair_sync()) goto softmax_done;
+          mt = fmaxf(mt, slot[(kh ^ 1) * 128 + row]);
+        }
         float alpha = 1.f;
         if (m_ref == -INFINITY || mt > m_ref + stale) {
           const float m_new = fmaxf(m_ref, mt);
@@ -524,40 +541,38 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
         }
         const float mc = m_ref == -INFINITY ? 0.f : m_ref * c;
         float lsum = 0.f;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
+        {
           float hi[32], lo[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const float pj = ex2(fmaf(s[half * 32 + i], c, -mc));
+            const float pj = ex2(fmaf(s[i], c, -mc));
             lsum += pj;
             hi[i] = tf32_hi(pj);
             lo[i] = pj - hi[i];
           }
-          tmem_st32(sbuf + half * 32, hi);
-          tmem_st32(sbuf + 64 + half * 32, lo);
+          tmem_st32(sbuf, hi);
+          tmem_st32(sbuf + 64, lo);
         }
         l = fmaf(l, alpha, lsum);
         tmem_wait_st();
         // O is rescaled only when the reference maximum moved; PV(n-1) must be
         // complete first. Skipping this wait otherwise is safe for the parity
-        // bookkeeping: PV(n+1) cannot run before this warp releases P(n+1), so
+        // bookkeeping: PV(n+1) cannot run before these warps release P(n+1), so
         // odone[(n-1) & 1] is at most one phase past the one waited for here.
+        // Both warps of a row set take the same decision (same m_ref, same mt).
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
           if (!wait_bar_warp(&bars.odone[(n - 1) & 1], ((n - 1) >> 1) & 1, prm, abort_flag)) goto softmax_done;
           tc_fence_after();
-          {
 #pragma unroll
-            for (int part = 0; part < 4; ++part) {
-              float o[32];
-              tmem_ld32(lane_tmem + kColO + part * 32, o);
-              tmem_wait_ld();
+          for (int part = 0; part < 2; ++part) {  // O' columns 64 kh .. 64 kh + 63
+            float o[32];
+            tmem_ld32(lane_tmem + kColO + kh * 64 + part * 32, o);
+            tmem_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] *= alpha;
-              tmem_st32(lane_tmem + kColO + part * 32, o);
-            }
-            tmem_wait_st();
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tmem_st32(lane_tmem + kColO + kh * 64 + part * 32, o);
           }
+          tmem_wait_st();
         }
         tc_fence_before();
         __syncwarp();
@@ -571,26 +586,31 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
           q_loaded = true;
         }
       }
-      // Epilogue: wait for the last PV, sum the two halves, one division per element.
+      // Epilogue: the row sum is the two warps' shares; wait for the last PV,
+      // add the two stacked halves of O', one division per element. This warp
+      // writes head dimensions 32 kh .. 32 kh + 31.
+      lred[kh * 128 + row] = l;
+      if (!pair_sync()) goto softmax_done;
+      l += lred[(kh ^ 1) * 128 + row];
       if (!wait_bar_warp(&bars.odone[(n - 1) & 1], ((n - 1) >> 1) & 1, prm, abort_flag)) goto softmax_done;
       tc_fence_after();
       {
-        float* dst = p.out + ((size_t)pos * kHQ + w.g * kGroup + (row & 3)) * kD;
+        float a[32], b[32];
+        tmem_ld32(lane_tmem + kColO + kh * 32, a);
+        tmem_ld32(lane_tmem + kColO + 64 + kh * 32, b);
+        tmem_wait_ld();
+        if (pos < p.C) {
+          float* dst = p.out + ((size_t)pos * kHQ + w.g * kGroup + (row & 3)) * kD + kh * 32;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float a[32], b[32];
-          tmem_ld32(lane_tmem + kColO + half * 32, a);
-          tmem_ld32(lane_tmem + kColO + 64 + half * 32, b);
-          tmem_wait_ld();
-          if (pos < p.C) {
-#pragma unroll
-            for (int i = 0; i < 32; i += 4)
-              *reinterpret_cast<float4*>(dst + half * 32 + i) =
-                  make_float4((a[i] + b[i]) / l, (a[i + 1] + b[i + 1]) / l, (a[i + 2] + b[i + 2]) / l,
-                              (a[i + 3] + b[i + 3]) / l);
-          }
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(dst + i) =
+                make_float4((a[i] + b[i]) / l, (a[i + 1] + b[i + 1]) / l, (a[i + 2] + b[i + 2]) / l,
+                            (a[i + 3] + b[i + 3]) / l);
         }
       }
+      // The next write of this warp's share (the next unit's epilogue) comes
+      // after at least one more exchange, which the partner only joins after
+      // reading this one.
       tc_fence_before();
     }
   softmax_done:;
