@@ -393,12 +393,16 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
     // ---------------------------------------------------------- V converters
     // Raw V [key][d] (two d-half regions of 64 keys) -> V^T [d][key] in two
     // key-half regions, hi rows 0-63 and lo rows 64-127. This warp takes the
-    // d-half cw; a lane owns 4 keys x 4 head dimensions per round and turns
-    // four 16-byte row loads into four 16-byte transposed stores (hi and lo).
-    // With lane = 8 dsub + kq, a store instruction covers 4 V^T rows x 8 key
-    // quads (conflict-free) and a load instruction 8 keys x 4 d-quads.
+    // d-half cw; a lane owns a block of 4 keys x 4 head dimensions per round
+    // and turns four 16-byte row loads into four 16-byte transposed stores
+    // (hi and lo). 16-byte accesses are served per quarter-warp, so lane x of
+    // a quarter takes key quad x and d-quad (x + t) mod 8: under the 128-byte
+    // swizzle both its loads and its stores then fall in 8 distinct 16-byte
+    // bank groups. Quarter q in round rd covers key half kh = (q + 4 rd) / 8
+    // and diagonal t = (q + 4 rd) mod 8: all 2 x 8 x 8 blocks, once each.
     const int cw = warp - kFirstVConvWarp;
-    const int dsub = lane >> 3, kq = lane & 7;
+    const uint32_t x = (uint32_t)(lane & 7);
+    const int quarter = lane >> 3;
     int n = 0;
     for (int k = 0;; ++k) {
       const int u = unit_index(k, cta, grid);
@@ -412,27 +416,29 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
           goto vconv_done;
         const uint8_t* vraw = smem + kSmemVRaw + vr * kVRawBytes + cw * kHalf;  // this warp's d-half
         uint8_t* vt = smem + kSmemVT + vs * kVStageBytes;
-        float4 x[4][4];  // [round][key within the quad]
+        float4 xv[4][4];  // [round][key within the quad]
 #pragma unroll
         for (int rd = 0; rd < 4; ++rd) {
-          const uint32_t d4 = (uint32_t)((rd & 1) * 4 + dsub);            // d-quad within the half
-          const uint32_t key0 = (uint32_t)((rd >> 1) * 32 + kq * 4);
+          const uint32_t combo = (uint32_t)(quarter + 4 * rd);
+          const uint32_t key0 = (combo >> 3) * 32u + 4u * x;
+          const uint32_t d4 = (x + combo) & 7u;
 #pragma unroll
           for (int r = 0; r < 4; ++r)
-            x[rd][r] = *reinterpret_cast<const float4*>(vraw + sw128((key0 + r) * 128u + d4 * 16u));
+            xv[rd][r] = *reinterpret_cast<const float4*>(vraw + sw128((key0 + r) * 128u + d4 * 16u));
         }
 #pragma unroll
         for (int rd = 0; rd < 4; ++rd) {
-          const uint32_t kh = (uint32_t)(rd >> 1);
-          const uint32_t d0 = (uint32_t)(cw * 32) + 4u * (uint32_t)((rd & 1) * 4 + dsub);
+          const uint32_t combo = (uint32_t)(quarter + 4 * rd);
+          const uint32_t kh = combo >> 3;
+          const uint32_t d0 = (uint32_t)(cw * 32) + 4u * ((x + combo) & 7u);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const float e0 = i == 0 ? x[rd][0].x : i == 1 ? x[rd][0].y : i == 2 ? x[rd][0].z : x[rd][0].w;
-            const float e1 = i == 0 ? x[rd][1].x : i == 1 ? x[rd][1].y : i == 2 ? x[rd][1].z : x[rd][1].w;
-            const float e2 = i == 0 ? x[rd][2].x : i == 1 ? x[rd][2].y : i == 2 ? x[rd][2].z : x[rd][2].w;
-            const float e3 = i == 0 ? x[rd][3].x : i == 1 ? x[rd][3].y : i == 2 ? x[rd][3].z : x[rd][3].w;
+            const float e0 = i == 0 ? xv[rd][0].x : i == 1 ? xv[rd][0].y : i == 2 ? xv[rd][0].z : xv[rd][0].w;
+            const float e1 = i == 0 ? xv[rd][1].x : i == 1 ? xv[rd][1].y : i == 2 ? xv[rd][1].z : xv[rd][1].w;
+            const float e2 = i == 0 ? xv[rd][2].x : i == 1 ? xv[rd][2].y : i == 2 ? xv[rd][2].z : xv[rd][2].w;
+            const float e3 = i == 0 ? xv[rd][3].x : i == 1 ? xv[rd][3].y : i == 2 ? xv[rd][3].z : xv[rd][3].w;
             const float4 hi = make_float4(tf32_hi(e0), tf32_hi(e1), tf32_hi(e2), tf32_hi(e3));
-            const uint32_t off = kh * kRegion + sw128((d0 + (uint32_t)i) * 128u + (uint32_t)kq * 16u);
+            const uint32_t off = kh * kRegion + sw128((d0 + (uint32_t)i) * 128u + x * 16u);
             *reinterpret_cast<float4*>(vt + off) = hi;
             *reinterpret_cast<float4*>(vt + off + kHalf) = make_float4(e0 - hi.x, e1 - hi.y, e2 - hi.z, e3 - hi.w);
           }
