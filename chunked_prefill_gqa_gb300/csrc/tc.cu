@@ -27,7 +27,7 @@
 // Q and P are TMEM operands (P hi and P lo overwrite the S columns they came
 // from); K and V^T are 128-byte-swizzled K-major shared-memory operands.
 //
-// Warp roles (15 warps):
+// Warp roles (16 warps):
 //   0-7   softmax: warp w owns TMEM lanes 32 (w % 4) .. + 31 (one row per
 //         thread) and the keys 32 (w / 4) .. + 31 of every tile; the two
 //         warps of a row set exchange their partial row maxima through shared
@@ -35,10 +35,15 @@
 //         the online softmax, write P hi/lo, rescale O when the reference
 //         maximum moves, and write the output.
 //   8     K producer: TMA loads of K tiles into the K ring.
-//   9     MMA: allocates TMEM; one lane issues every tcgen05.mma and commit.
+//   9     QK issuer: allocates TMEM; one lane issues QK(n) as soon as K(n) is
+//         converted and S buffer n & 1 is free (PV(n-2) complete).
 //   10    V producer: TMA loads of V tiles into the raw V ring.
 //   11-12 K converters: K lo next to each K tile (one d-half each).
 //   13-14 V converters: raw V -> V^T hi / V^T lo (one d-half each).
+//   15    PV issuer: one lane issues PV(n) as soon as P(n) and V^T(n) are ready.
+// The two issuers are separate threads so that neither stream of MMAs waits
+// behind the other's inputs: the tensor core's issue queue is shallow, and a
+// single issuer that blocks on one condition leaves the pipe idle.
 // Every wait is bounded; on expiry the kernel records ATTN_ETIMEOUT in the
 // device error word, all roles wind down, and TMEM is freed.
 #include <cuda.h>
@@ -67,7 +72,8 @@ constexpr int kFirstKConvWarp = 11;
 constexpr int kKConvWarps = 2;
 constexpr int kFirstVConvWarp = 13;
 constexpr int kVConvWarps = 2;
-constexpr int kThreads = 32 * (kFirstVConvWarp + kVConvWarps);
+constexpr int kPvWarp = kFirstVConvWarp + kVConvWarps;
+constexpr int kThreads = 32 * (kPvWarp + 1);
 
 // TMEM columns (fp32, one per column).
 constexpr uint32_t kColQhi = 0;
@@ -88,7 +94,7 @@ constexpr uint32_t kSmemK = 0;
 constexpr uint32_t kSmemVRaw = kSmemK + kKStages * kKStageBytes;
 constexpr uint32_t kSmemVT = kSmemVRaw + kVRawStages * kVRawBytes;
 constexpr uint32_t kSmemBar = kSmemVT + kVStages * kVStageBytes;
-constexpr uint32_t kNumBars = 3 * kKStages + 2 * kVRawStages + 2 * kVStages + 2 + 2 + 2 + 2 + 4;
+constexpr uint32_t kNumBars = 3 * kKStages + 2 * kVRawStages + 2 * kVStages + 2 + 2 + 2 + 1 + 2 + 4;
 constexpr uint32_t kSmemRed = kSmemBar + kNumBars * 8 + 16;  // [2 tile parities][2 key halves][128 rows]
 constexpr uint32_t kSmemLsum = kSmemRed + 2 * 2 * 128 * 4;   // [2 key halves][128 rows]
 constexpr uint32_t kSmemTotal = kSmemLsum + 2 * 128 * 4;
@@ -124,7 +130,7 @@ struct Bars {
   uint64_t* pfull;   // [2] P hi/lo written and O rescaled (softmax warps)
   uint64_t* odone;   // [2] PV(n) done, barrier n & 1 (MMA commit)
   uint64_t* qready;  // Q hi/lo in TMEM (softmax warps)
-  uint64_t* drain;   // MMA drain on abort
+  uint64_t* drain;   // [2] drain of each MMA issuer on abort (QK, PV)
   uint64_t* pair;    // [4] the two softmax warps of a row quarter exchange partial results
 };
 
@@ -142,7 +148,7 @@ __device__ __forceinline__ Bars carve_bars(uint8_t* base) {
   r.pfull = b; b += 2;
   r.odone = b; b += 2;
   r.qready = b++;
-  r.drain = b++;
+  r.drain = b; b += 2;
   r.pair = b; b += 4;
   return r;
 }
@@ -235,7 +241,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
     mbar_init(&bars.odone[0], 1);
     mbar_init(&bars.odone[1], 1);
     mbar_init(bars.qready, kSoftmaxWarps);
-    mbar_init(bars.drain, 1);
+    mbar_init(&bars.drain[0], 1);
+    mbar_init(&bars.drain[1], 1);
     for (int q = 0; q < 4; ++q) mbar_init(&bars.pair[q], 2);
     *abort_flag = 0;
     fence_mbar_init();
@@ -291,70 +298,71 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
       }
     }
     __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------------ MMA
+  } else if (warp == kMmaWarp || warp == kPvWarp) {
+    // ---------------------------------------------------------- MMA issuers
+    const bool is_qk = warp == kMmaWarp;
     if (lane == 0) {
       int n = 0, lu = 0;
-      auto issue_qk = [&](int m) -> bool {
-        const int ks = m % kKStages;
-        if (!wait_bar(&bars.kconv[ks], (m / kKStages) & 1, prm, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t kb = smem_u32(smem + kSmemK + ks * kKStageBytes);
-        const uint32_t d = tmem + kColS + (m & 1) * 128;
-#pragma unroll
-        for (int s = 0; s < 8; ++s)  // [Q_hi K_hi^T | Q_hi K_lo^T]
-          mma_tf32_ts(d, tmem + kColQhi + s * 8, sdesc_sw128(kb + (s >> 2) * kRegion + (s & 3) * 32),
-                      kIdescN128, s > 0);
-#pragma unroll
-        for (int s = 0; s < 8; ++s)  // += Q_lo K_hi^T into the first half
-          mma_tf32_ts(d, tmem + kColQlo + s * 8, sdesc_sw128(kb + (s >> 2) * kRegion + (s & 3) * 32),
-                      kIdescN64, 1);
-        mma_commit(&bars.sfull[m & 1]);
-        mma_commit(&bars.kempty[ks]);
-        return true;
-      };
-      auto issue_pv = [&](int m, bool first) -> bool {
-        const int vs = m % kVStages;
-        if (!wait_bar(&bars.vconv[vs], (m / kVStages) & 1, prm, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t vt = smem_u32(smem + kSmemVT + vs * kVStageBytes);
-        const uint32_t phi = tmem + kColS + (m & 1) * 128;
-        const uint32_t plo = phi + 64;
-#pragma unroll
-        for (int s = 0; s < 8; ++s)  // [P_hi V_hi | P_hi V_lo]
-          mma_tf32_ts(tmem + kColO, phi + s * 8, sdesc_sw128(vt + (s >> 2) * kRegion + (s & 3) * 32),
-                      kIdescN128, (first && s == 0) ? 0u : 1u);
-#pragma unroll
-        for (int s = 0; s < 8; ++s)  // += P_lo V_hi into the first half
-          mma_tf32_ts(tmem + kColO, plo + s * 8, sdesc_sw128(vt + (s >> 2) * kRegion + (s & 3) * 32),
-                      kIdescN64, 1);
-        mma_commit(&bars.odone[m & 1]);
-        mma_commit(&bars.vempty[vs]);
-        return true;
-      };
       for (int k = 0;; ++k) {
         const int u = unit_index(k, cta, grid);
         if (u >= prm.n_units) break;
         const Unit w = decode_unit(u, prm);
-        if (!wait_bar(bars.qready, lu & 1, prm, abort_flag)) goto mma_done;
-        tc_fence_after();
-        for (int j = 0; j < w.ntiles; ++j, ++n) {
-          if (j == 0 && !issue_qk(n)) goto mma_done;
-          // QK(n+1) goes ahead of PV(n) so that the softmax of tile n+1
-          // overlaps PV(n) on the tensor pipe.
-          if (j + 1 < w.ntiles && !issue_qk(n + 1)) goto mma_done;
-          if (!wait_bar(&bars.pfull[n & 1], (n >> 1) & 1, prm, abort_flag)) goto mma_done;
+        if (is_qk) {
+          if (!wait_bar(bars.qready, lu & 1, prm, abort_flag)) goto mma_done;
           tc_fence_after();
-          if (!issue_pv(n, j == 0)) goto mma_done;
+        }
+        for (int j = 0; j < w.ntiles; ++j, ++n) {
+          if (is_qk) {
+            // QK(n): K(n) converted; S buffer n & 1 free once PV(n-2) has read
+            // P(n-2) from it (odone[n & 1] is at most one phase past PV(n-2):
+            // PV(n) needs S(n), which is issued only below).
+            const int ks = n % kKStages;
+            if (!wait_bar(&bars.kconv[ks], (n / kKStages) & 1, prm, abort_flag)) goto mma_done;
+            if (n >= 2 && !wait_bar(&bars.odone[n & 1], ((n >> 1) - 1) & 1, prm, abort_flag)) goto mma_done;
+            tc_fence_after();
+            const uint32_t kb = smem_u32(smem + kSmemK + ks * kKStageBytes);
+            const uint32_t d = tmem + kColS + (n & 1) * 128;
+#pragma unroll
+            for (int s = 0; s < 8; ++s)  // [Q_hi K_hi^T | Q_hi K_lo^T]
+              mma_tf32_ts(d, tmem + kColQhi + s * 8, sdesc_sw128(kb + (s >> 2) * kRegion + (s & 3) * 32),
+                          kIdescN128, s > 0);
+#pragma unroll
+            for (int s = 0; s < 8; ++s)  // += Q_lo K_hi^T into the first half
+              mma_tf32_ts(d, tmem + kColQlo + s * 8, sdesc_sw128(kb + (s >> 2) * kRegion + (s & 3) * 32),
+                          kIdescN64, 1);
+            mma_commit(&bars.sfull[n & 1]);
+            mma_commit(&bars.kempty[ks]);
+          } else {
+            // PV(n): P(n) written by the softmax warps, V^T(n) converted.
+            const int vs = n % kVStages;
+            if (!wait_bar(&bars.pfull[n & 1], (n >> 1) & 1, prm, abort_flag)) goto mma_done;
+            if (!wait_bar(&bars.vconv[vs], (n / kVStages) & 1, prm, abort_flag)) goto mma_done;
+            tc_fence_after();
+            const uint32_t vt = smem_u32(smem + kSmemVT + vs * kVStageBytes);
+            const uint32_t phi = tmem + kColS + (n & 1) * 128;
+            const uint32_t plo = phi + 64;
+            const bool first = j == 0;
+#pragma unroll
+            for (int s = 0; s < 8; ++s)  // [P_hi V_hi | P_hi V_lo]
+              mma_tf32_ts(tmem + kColO, phi + s * 8, sdesc_sw128(vt + (s >> 2) * kRegion + (s & 3) * 32),
+                          kIdescN128, (first && s == 0) ? 0u : 1u);
+#pragma unroll
+            for (int s = 0; s < 8; ++s)  // += P_lo V_hi into the first half
+              mma_tf32_ts(tmem + kColO, plo + s * 8, sdesc_sw128(vt + (s >> 2) * kRegion + (s & 3) * 32),
+                          kIdescN64, 1);
+            mma_commit(&bars.odone[n & 1]);
+            mma_commit(&bars.vempty[vs]);
+          }
         }
         ++lu;
       }
     mma_done:
       if (*abort_flag) {
-        // Nothing may be in flight when TMEM is released.
-        mma_commit(bars.drain);
+        // Nothing this thread issued may be in flight when TMEM is released.
+        uint64_t* drain = &bars.drain[is_qk ? 0 : 1];
+        mma_commit(drain);
         const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(bars.drain, 0) && globaltimer_ns() - t0 < prm.timeout_ns) {
+        while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < prm.timeout_ns) {
         }
       }
     }
