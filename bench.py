@@ -65,6 +65,8 @@ def parse_args():
     ap.add_argument("--path", default="attn_prefill",
                     choices=["attn_prefill", "attn_prefill_ffma", "attn_reference_prefill"])
     ap.add_argument("--workload", choices=["serve", "long"], default="serve")
+    ap.add_argument("--paged", action="store_true",
+                    help="time attn_prefill_paged on the same workload scattered into shuffled 16-token pages")
     ap.add_argument("--seed", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -211,7 +213,7 @@ def profiled_traffic(path_name: str, workload: str):
 
 def roofline(path_name: str, kernel: str, flops: float, ms: float, peaks, workload: str):
     achieved = flops / (ms * 1e-3) / 1e12
-    if kernel == "tcgen05-split-tf32":
+    if kernel.startswith("tcgen05-split-tf32"):
         peak = peaks["bf16_tflops"] * NOMINAL_TF32 / NOMINAL_BF16
         r = {"bound": "tensor", "peak_dtype": "tf32",
              "peak_note": f"{peaks['source']} bf16 burst x {NOMINAL_TF32}/{NOMINAL_BF16} (nominal tf32/bf16)",
@@ -312,8 +314,21 @@ def main():
     kernel = "tcgen05-split-tf32" if args.path == "attn_prefill" else (
         "ffma" if args.path == "attn_prefill_ffma" else "reference")
 
-    def call():
-        fn(q, k, v, out, P, stream)
+    if args.paged:
+        if args.path != "attn_prefill":
+            raise SystemExit("--paged times attn_prefill_paged only")
+        pg = W.to_pages(inp, seed=args.seed + 5)
+        kp = torch.from_numpy(pg.k_pages).to(dev)
+        vp = torch.from_numpy(pg.v_pages).to(dev)
+        tb = torch.from_numpy(pg.table).to(dev)
+        kernel = "tcgen05-split-tf32-paged"
+        desc += "; K/V in shuffled 16-token pages"
+
+        def call():
+            cp.attn_prefill_paged(q, kp, vp, tb, out, P, stream)
+    else:
+        def call():
+            fn(q, k, v, out, P, stream)
 
     sampler = ClockSampler(dev.index if world == 1 else local)
     sampler.start()
@@ -356,7 +371,7 @@ def main():
     # End to end through the same entry point: pinned host inputs copied in,
     # the result copied out, every step inside the timed region.
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not args.paged:
         hq = torch.from_numpy(inp.q).pin_memory()
         hk = torch.from_numpy(inp.k).pin_memory()
         hv = torch.from_numpy(inp.v).pin_memory()
@@ -441,7 +456,8 @@ def main():
                        "flops_per_step": flops,
                        "l2": "flushed before every timed step (256 MiB write)",
                        "parallelism": f"replicas x{world}"},
-            "roofline": roofline(args.path, kernel, flops, ms_mean, peaks, args.workload),
+            "roofline": roofline(args.path, kernel, flops, ms_mean, peaks,
+                                 args.workload + ("-paged" if args.paged else "")),
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": args.steps,

@@ -32,10 +32,11 @@ ATTN_EDEVICE = -7
 ATTN_ETMA = -8
 ATTN_ECUDA = -9
 MAX_TOKENS = 1 << 24
+PAGE = 16
 
 # Every symbol the header declares (the CPU tests check the library exports them).
-EXPORTS = ("attn_prefill", "attn_full_causal", "attn_prefill_ffma", "attn_reference_prefill",
-           "attn_selftest_timeout", "attn_get_device_error", "attn_strerror", "attn_version")
+EXPORTS = ("attn_prefill", "attn_full_causal", "attn_prefill_paged", "attn_prefill_ffma",
+           "attn_reference_prefill", "attn_selftest_timeout", "attn_get_device_error", "attn_strerror", "attn_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -67,6 +68,8 @@ def load():
                 fn = getattr(lib, name)
                 fn.restype = ci
                 fn.argtypes = [vp, vp, vp, vp, ci, ci, vp]
+            lib.attn_prefill_paged.restype = ci
+            lib.attn_prefill_paged.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, vp]
             lib.attn_full_causal.restype = ci
             lib.attn_full_causal.argtypes = [vp, vp, vp, vp, ci, vp]
             lib.attn_get_device_error.restype = ci
@@ -140,6 +143,37 @@ def attn_full_causal(q, k, v, out, stream=None):
     rc = load().attn_full_causal(_ptr(q), _ptr(k), _ptr(v), _ptr(out), T, _stream_handle(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_full_causal")
+    return out
+
+
+def attn_prefill_paged(q, kPages, vPages, blockTable, out, P: int, stream=None):
+    """out <- attn_prefill against a paged cache: token t at slot t % 16 of page
+    blockTable[t // 16]; kPages / vPages [numPages][16][8][64] fp32, blockTable
+    int32 with at least ceil((P + C) / 16) entries."""
+    import torch
+    C = q.shape[0]
+    if not (isinstance(kPages, torch.Tensor) and kPages.dim() == 4 and tuple(kPages.shape[1:]) == (PAGE, HKV, D)):
+        raise ValueError("kPages must be [numPages][16][8][64]")
+    if vPages.shape != kPages.shape:
+        raise ValueError("vPages must have kPages' shape")
+    if not (isinstance(blockTable, torch.Tensor) and blockTable.dtype == torch.int32 and blockTable.is_cuda
+            and blockTable.is_contiguous()):
+        raise TypeError("blockTable must be a contiguous int32 CUDA tensor")
+    if blockTable.numel() < (P + C + PAGE - 1) // PAGE:
+        raise ValueError("blockTable has fewer than ceil((P + C) / 16) entries")
+    num_pages = kPages.shape[0]
+    flat_k = kPages.view(num_pages * PAGE, HKV, D)
+    flat_v = vPages.view(num_pages * PAGE, HKV, D)
+    for name, t in (("q", q), ("out", out)):
+        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous() or tuple(t.shape) != (C, HQ, D):
+            raise ValueError(f"{name} must be a contiguous float32 CUDA tensor of shape ({C}, {HQ}, {D})")
+    for name, t in (("kPages", flat_k), ("vPages", flat_v)):
+        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous float32 CUDA tensor")
+    rc = load().attn_prefill_paged(_ptr(q), _ptr(kPages), _ptr(vPages), _ptr(blockTable), _ptr(out),
+                                   C, P, num_pages, _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_prefill_paged")
     return out
 
 

@@ -99,6 +99,18 @@ extern "C" int attn_reference_prefill(const float* q, const float* kCache, const
   return from_cuda(launch_reference(p, stream));
 }
 
+extern "C" int attn_prefill_paged(const float* q, const float* kPages, const float* vPages,
+                                  const int* blockTable, float* out, int C, int P, int numPages,
+                                  cudaStream_t stream) {
+  Problem p{};
+  const int rc = prepare(q, kPages, vPages, out, C, P, &p);
+  if (rc != ATTN_OK || C == 0) return rc;
+  if (!blockTable || numPages < 1) return ATTN_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(blockTable) & 3u) != 0) return ATTN_EALIGN;
+  if (numPages > ATTN_MAX_TOKENS / ATTN_PAGE) return ATTN_ERANGE;
+  return launch_tc_paged(p, blockTable, numPages, stream);
+}
+
 extern "C" int attn_selftest_timeout(const float* q, const float* kCache, const float* vCache,
                                      float* out, int C, int P, cudaStream_t stream) {
   Problem p{};

@@ -48,5 +48,7 @@ cudaError_t launch_reference(const Problem& p, cudaStream_t stream);
 cudaError_t launch_ffma(const Problem& p, cudaStream_t stream);
 int launch_tc(const Problem& p, cudaStream_t stream);             // returns an ATTN_* code
 int launch_tc_fault_test(const Problem& p, cudaStream_t stream);  // skips a load, 20 ms waits
+// Paged K/V: p.k / p.v point at [num_pages * 16][8][64] page pools.
+int launch_tc_paged(const Problem& p, const int* table, int num_pages, cudaStream_t stream);
 
 }  // namespace attn

@@ -116,7 +116,14 @@ struct Params {
   int n_qtiles;
   unsigned long long timeout_ns;
   int fault_skip_first_k;  // test hook: never load the first K tile
+  // Paged K/V ("FlashAttention and inference kernels", PagedAttention): token t
+  // lives in slot t % 16 of physical page table[t / 16]. table == nullptr:
+  // contiguous [P + C][8][64] caches.
+  const int* table;
+  int num_pages;
 };
+
+constexpr int kPage = 16;  // tokens per page of a paged cache
 
 struct Bars {
   uint64_t* kfull;   // [kKStages] TMA K landed
@@ -275,17 +282,36 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
           const int st = n % stages;
           uint64_t* freed = is_k ? &bars.kempty[st] : &bars.vrfree[st];
           if (n >= stages && !wait_bar(freed, ((n / stages) - 1) & 1, prm, abort_flag)) goto producer_done;
-          if (is_k) {
-            if (prm.fault_skip_first_k && n == 0) continue;
-            uint8_t* dst = smem + kSmemK + st * kKStageBytes;
-            mbar_arrive_expect_tx(&bars.kfull[st], 2 * kHalf);
-            tma_load_2d(dst, &tmk, &bars.kfull[st], w.g * kD, j * kBc);
-            tma_load_2d(dst + kRegion, &tmk, &bars.kfull[st], w.g * kD + 32, j * kBc);
+          if (is_k && prm.fault_skip_first_k && n == 0) continue;
+          const CUtensorMap* map = is_k ? &tmk : &tmv;
+          uint64_t* full = is_k ? &bars.kfull[st] : &bars.vfull[st];
+          uint8_t* dst = is_k ? smem + kSmemK + st * kKStageBytes : smem + kSmemVRaw + st * kVRawBytes;
+          const uint32_t half_stride = is_k ? kRegion : kHalf;  // d-half regions
+          mbar_arrive_expect_tx(full, 2 * kHalf);
+          if (prm.table == nullptr) {
+            tma_load_2d(dst, map, full, w.g * kD, j * kBc);
+            tma_load_2d(dst + half_stride, map, full, w.g * kD + 32, j * kBc);
           } else {
-            uint8_t* dst = smem + kSmemVRaw + st * kVRawBytes;
-            mbar_arrive_expect_tx(&bars.vfull[st], kVRawBytes);
-            tma_load_2d(dst, &tmv, &bars.vfull[st], w.g * kD, j * kBc);
-            tma_load_2d(dst + kHalf, &tmv, &bars.vfull[st], w.g * kD + 32, j * kBc);
+            // Four 16-row boxes per d-half; each is two whole 1024-byte swizzle
+            // atoms, so the tile lands exactly as a contiguous load would.
+            // A page past the sequence, or a table entry outside [0,
+            // num_pages) (also recorded as a bounds error), is read from an
+            // out-of-range row, which TMA fills with zeros.
+            const int T = p.P + p.C;
+#pragma unroll
+            for (int pg = 0; pg < kBc / kPage; ++pg) {
+              const int lp = j * (kBc / kPage) + pg;
+              int y = prm.num_pages * kPage;
+              if (lp * kPage < T) {
+                const int phys = __ldg(prm.table + lp);
+                if (phys >= 0 && phys < prm.num_pages)
+                  y = phys * kPage;
+                else
+                  record_error(p.err, kDevErrBounds);
+              }
+              tma_load_2d(dst + pg * kPage * 128, map, full, w.g * kD, y);
+              tma_load_2d(dst + half_stride + pg * kPage * 128, map, full, w.g * kD + 32, y);
+            }
           }
         }
       }
@@ -431,8 +457,12 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
           const uint32_t key0 = (combo >> 3) * 32u + 4u * x;
           const uint32_t d4 = (x + combo) & 7u;
 #pragma unroll
-          for (int r = 0; r < 4; ++r)
+          for (int r = 0; r < 4; ++r) {
             xv[rd][r] = *reinterpret_cast<const float4*>(vraw + sw128((key0 + r) * 128u + d4 * 16u));
+            // Keys at or past P + C carry zero weight, but 0 * NaN is NaN: the
+            // unused slots of a cache page need not hold finite values.
+            if (j * kBc + (int)(key0 + r) >= p.P + p.C) xv[rd][r] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
         }
 #pragma unroll
         for (int rd = 0; rd < 4; ++rd) {
@@ -655,15 +685,16 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
   return fn;
 }
 
-// k, v [T][8][64] as a 2-D tensor (head * 64 + d, position); a box is 32
-// floats (one 128-byte swizzle row) x 64 keys.
-int encode_kv_map(const float* base, int T, CUtensorMap* map) {
+// k, v [rows][8][64] as a 2-D tensor (head * 64 + d, row); a box is 32 floats
+// (one 128-byte swizzle row) x box_rows rows: 64 keys of a contiguous cache, or
+// one 16-token page of a paged cache ([pages * 16][8][64]).
+int encode_kv_map(const float* base, int rows, int box_rows, CUtensorMap* map) {
   auto enc = get_encoder();
   if (!enc) return ATTN_ETMA;
   const cuuint32_t ones[2] = {1, 1};
-  const cuuint64_t dims[2] = {(cuuint64_t)kHKV * kD, (cuuint64_t)T};
+  const cuuint64_t dims[2] = {(cuuint64_t)kHKV * kD, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)kHKV * kD * 4};
-  const cuuint32_t box[2] = {32, (cuuint32_t)kBc};
+  const cuuint32_t box[2] = {32, (cuuint32_t)box_rows};
   if (enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, ones,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -677,7 +708,8 @@ struct TcDeviceState {
 };
 TcDeviceState g_tc_state[64];
 
-int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long timeout_ns, int fault) {
+int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long timeout_ns, int fault,
+                   const int* table = nullptr, int num_pages = 0) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ECUDA;
   TcDeviceState& st = g_tc_state[dev];
@@ -690,8 +722,10 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
     st.ready = true;
   }
   alignas(64) CUtensorMap mk, mv;
-  int rc = encode_kv_map(p.k, p.P + p.C, &mk);
-  if (rc == ATTN_OK) rc = encode_kv_map(p.v, p.P + p.C, &mv);
+  const int rows = table ? num_pages * kPage : p.P + p.C;
+  const int box_rows = table ? kPage : kBc;
+  int rc = encode_kv_map(p.k, rows, box_rows, &mk);
+  if (rc == ATTN_OK) rc = encode_kv_map(p.v, rows, box_rows, &mv);
   if (rc != ATTN_OK) return rc;
   Params prm;
   prm.p = p;
@@ -699,6 +733,8 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
   prm.n_units = prm.n_qtiles * kHKV;
   prm.timeout_ns = timeout_ns;
   prm.fault_skip_first_k = fault;
+  prm.table = table;
+  prm.num_pages = num_pages;
   const int grid = prm.n_units < st.num_sms ? prm.n_units : st.num_sms;
   tc_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(mk, mv, prm);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ELAUNCH;
@@ -712,6 +748,10 @@ int launch_tc(const Problem& p, cudaStream_t stream) {
 
 int launch_tc_fault_test(const Problem& p, cudaStream_t stream) {
   return tc_launch_impl(p, stream, 20000000ull, 1);
+}
+
+int launch_tc_paged(const Problem& p, const int* table, int num_pages, cudaStream_t stream) {
+  return tc_launch_impl(p, stream, 2000000000ull, 0, table, num_pages);
 }
 
 }  // namespace attn

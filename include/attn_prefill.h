@@ -52,6 +52,7 @@ extern "C" {
 #define ATTN_HKV 8
 #define ATTN_D 64
 #define ATTN_MAX_TOKENS (1 << 24)
+#define ATTN_PAGE 16        /* tokens per page of a paged K/V cache */
 
 /* Return codes. */
 #define ATTN_OK 0
@@ -82,6 +83,26 @@ extern "C" {
  */
 int attn_prefill(const float *q, const float *kCache, const float *vCache, float *out,
                  int C, int P, cudaStream_t stream);
+
+/*
+ * attn_prefill_paged -- attn_prefill against a paged K/V cache ("FlashAttention
+ * and inference kernels", PagedAttention: a cache is cut into fixed pages and a
+ * block table maps the i-th logical page to its physical page, so the kernel
+ * gains one indirection per K/V read). Token t's key and value live in slot
+ * t % 16 of physical page blockTable[t / 16]:
+ *   kPages, vPages  [numPages][16][8][64] fp32, device pointers
+ *   blockTable      int32 device array of at least ceil((P + C) / 16) entries,
+ *                   each in [0, numPages); pages may be shared and in any order
+ * q and out as for attn_prefill. Slots of a page past position P + C - 1 are
+ * never given weight and may hold any values, NaN included. An entry outside
+ * [0, numPages) is read as zeros and recorded as ATTN_EBOUNDS in the device
+ * error word (see attn_get_device_error). Errors: ATTN_EINVAL for a NULL table
+ * or numPages < 1, ATTN_EALIGN for a table not 4-byte aligned, ATTN_ERANGE for
+ * numPages > ATTN_MAX_TOKENS / 16, otherwise as attn_prefill.
+ */
+int attn_prefill_paged(const float *q, const float *kPages, const float *vPages,
+                       const int *blockTable, float *out, int C, int P, int numPages,
+                       cudaStream_t stream);
 
 /*
  * attn_full_causal -- a whole prompt with nothing cached: identical to

@@ -121,6 +121,22 @@ def prefill(inp, rows=None, threads: int = 0) -> np.ndarray:
     return attention(inp.q, inp.k, inp.v, inp.P, 0.125, rows=rows, threads=threads)
 
 
+def gather_pages(pages, table, T: int, page: int = 16) -> np.ndarray:
+    """The contiguous [T][HKV][D] cache a paged one stands for: token t is slot
+    t % page of physical page table[t // page] ("FlashAttention and inference
+    kernels", PagedAttention)."""
+    t = np.arange(T)
+    return np.ascontiguousarray(pages[np.asarray(table)[t // page], t % page])
+
+
+def prefill_paged(q, k_pages, v_pages, table, P: int, rows=None, threads: int = 0) -> np.ndarray:
+    """The oracle against a paged cache: gather by the block table, then the
+    same exact attention as :func:`attention` (scale 1/8)."""
+    T = P + q.shape[0]
+    return attention(q, gather_pages(k_pages, table, T), gather_pages(v_pages, table, T), P, 0.125,
+                     rows=rows, threads=threads)
+
+
 def violations(got, ref, atol: float = ATOL, rtol: float = RTOL) -> np.ndarray:
     """Boolean mask of elements failing |got - ref| <= atol + rtol * |ref| (NaN fails)."""
     got = np.asarray(got, dtype=np.float64)

@@ -99,3 +99,26 @@ def test_check_rule():
     assert oracle.check(ref + 1.01 * tol, ref)["n_bad"] == 4
     assert oracle.check(np.array([np.nan, 1.0, -2.0, 10.0]), ref)["n_bad"] == 1
     assert oracle.check(np.array([np.inf, 1.0, -2.0, 10.0]), ref)["n_bad"] == 1
+
+
+def test_paged_oracle_equals_contiguous():
+    """Gathering a paged cache through its block table (token t at slot t % 16 of
+    page table[t // 16], "FlashAttention and inference kernels", PagedAttention)
+    gives back the contiguous cache, so the paged oracle equals the oracle."""
+    for C, P in ((17, 31), (1, 0), (33, 1000)):
+        inp = W.edge(C, P)
+        pg = W.to_pages(inp, seed=C + P)
+        np.testing.assert_array_equal(oracle.gather_pages(pg.k_pages, pg.table, inp.T), inp.k)
+        np.testing.assert_array_equal(oracle.gather_pages(pg.v_pages, pg.table, inp.T), inp.v)
+        np.testing.assert_array_equal(oracle.prefill_paged(inp.q, pg.k_pages, pg.v_pages, pg.table, P),
+                                      oracle.prefill(inp))
+
+
+def test_paged_gather_follows_the_table():
+    """A hand-made two-page cache with the pages swapped: token 0..15 live in
+    physical page 1, tokens 16..19 in physical page 0."""
+    pages = np.zeros((2, 16, 1, 1), np.float32)
+    pages[1, :, 0, 0] = np.arange(16)
+    pages[0, :4, 0, 0] = 16 + np.arange(4)
+    got = oracle.gather_pages(pages, np.array([1, 0]), 20)
+    np.testing.assert_array_equal(got[:, 0, 0], np.arange(20))

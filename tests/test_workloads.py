@@ -78,3 +78,15 @@ def test_lastkey_variant():
     inp = W.edge(33, 1000, variant="lastkey")
     assert inp.planted.tolist() == [1032]
     assert np.all(inp.q[32, 0] == 4.0)
+
+
+def test_to_pages_layout():
+    inp = W.edge(17, 31)
+    pg = W.to_pages(inp, seed=3, spare_pages=4)
+    assert pg.k_pages.shape == ((48 + 15) // 16 + 4, 16, 8, 64)
+    assert len(set(pg.table.tolist())) == len(pg.table)        # distinct physical pages
+    for t in (0, 15, 16, 31, 47):
+        np.testing.assert_array_equal(pg.k_pages[pg.table[t // 16], t % 16], inp.k[t])
+        np.testing.assert_array_equal(pg.v_pages[pg.table[t // 16], t % 16], inp.v[t])
+    unused = np.setdiff1d(np.arange(pg.k_pages.shape[0]), pg.table)
+    assert np.isnan(pg.k_pages[unused]).all() and np.isnan(pg.v_pages[unused]).all()

@@ -200,3 +200,37 @@ EDGE_C = (1, 17, 33, 64)
 EDGE_P = (0, 31, 1000)
 FULL_T = (512, 1024, 2048)
 FULL_T_SMALL = (1, 17, 33, 257)
+
+
+PAGE = 16  # tokens per page of a paged cache
+
+
+@dataclass
+class Paged:
+    """A paged copy of a cache: k_pages / v_pages [num_pages][16][8][64] and an
+    int32 block table; token t is slot t % 16 of physical page table[t // 16]
+    ("FlashAttention and inference kernels", PagedAttention)."""
+    k_pages: np.ndarray
+    v_pages: np.ndarray
+    table: np.ndarray
+
+
+def to_pages(inp: Inputs, seed: int = 7, spare_pages: int = 5) -> Paged:
+    """Scatter ``inp``'s K/V into shuffled physical pages.
+
+    Physical pages are a seeded permutation (``spare_pages`` extra pages that no
+    token uses are included). Unused pool content -- the spare pages and the
+    slots of the last page past P + C - 1 -- is NaN, so a kernel that gives any
+    weight to it, or multiplies it by a zero weight, fails.
+    """
+    T = inp.T
+    n_logical = (T + PAGE - 1) // PAGE
+    n_pages = n_logical + spare_pages
+    perm = np.argsort(uniform(seed, n_pages), kind="stable")
+    table = perm[:n_logical].astype(np.int32)
+    k_pages = np.full((n_pages, PAGE, HKV, D), np.nan, dtype=np.float32)
+    v_pages = np.full((n_pages, PAGE, HKV, D), np.nan, dtype=np.float32)
+    t = np.arange(T)
+    k_pages[table[t // PAGE], t % PAGE] = inp.k
+    v_pages[table[t // PAGE], t % PAGE] = inp.v
+    return Paged(k_pages=k_pages, v_pages=v_pages, table=table)
