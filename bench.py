@@ -64,7 +64,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--path", default="attn_prefill",
                     choices=["attn_prefill", "attn_prefill_ffma", "attn_reference_prefill"])
-    ap.add_argument("--workload", choices=["serve", "long"], default="serve")
+    ap.add_argument("--workload", choices=["serve", "long", "decode"], default="serve",
+                    help="decode: one decode step of 16 sequences x 16384 cached tokens (paged)")
     ap.add_argument("--paged", action="store_true",
                     help="time attn_prefill_paged on the same workload scattered into shuffled 16-token pages")
     ap.add_argument("--seed", type=int, default=1)
@@ -271,10 +272,65 @@ def run_reference(args):
 # Our arm
 # ----------------------------------------------------------------------------
 
+def run_decode(args):
+    """One decode step (attn_decode_paged) for 16 sequences of 16384 cached
+    tokens: bandwidth-bound, reported as K/V bytes per second against the
+    measured HBM copy bandwidth."""
+    import torch
+    import chunked_prefill_gqa_gb300 as cp
+    from chunked_prefill_gqa_gb300 import build as B
+    torch.cuda.set_device(0)
+    B.build()
+    cp.load()
+    lens = [16384] * 16
+    batch = W.decode_batch(lens, seed=args.seed, spare_pages=0)
+    dev = torch.device("cuda", 0)
+    q = torch.from_numpy(batch.q).to(dev)
+    kp = torch.from_numpy(batch.k_pages).to(dev)
+    vp = torch.from_numpy(batch.v_pages).to(dev)
+    tb = torch.from_numpy(batch.table).to(dev)
+    cl = torch.from_numpy(batch.ctx).to(dev)
+    out = torch.empty_like(q)
+    nbytes = cp.attn_decode_workspace_bytes(len(lens), batch.max_context)
+    ws = torch.empty(max(nbytes // 4, 4), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    kv_bytes = sum(lens) * W.HKV * W.D * 4 * 2
+    flops = 4.0 * W.D * sum(lens) * W.HQ
+    for _ in range(args.warmup):
+        cp.attn_decode_paged(q, kp, vp, tb, cl, out, batch.max_context, 0, ws, stream)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        starts[i].record(stream)
+        cp.attn_decode_paged(q, kp, vp, tb, cl, out, batch.max_context, 0, ws, stream)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    if cp.attn_get_device_error() != 0:
+        raise RuntimeError("device error in the decode bench")
+    ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / args.steps
+    gbs = kv_bytes / (ms * 1e-3) / 1e9
+    peaks = load_peaks()
+    line = {"metric": "decode K/V GB/s, 16 sequences x 16384 cached tokens (32q/8kv, d=64, paged)",
+            "value": round(gbs, 1), "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "decode step, 16 x 16384 tokens, shuffled 16-token pages",
+                       "kv_bytes_per_step": kv_bytes, "tflops": round(flops / (ms * 1e-3) / 1e12, 3),
+                       "l2": "K/V (1 GiB) larger than L2"},
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": None},
+            "gpu_launches": 2 * args.steps}
+    print(json.dumps(line))
+    return 0
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == "decode":
+        return run_decode(args)
 
     import torch
     import torch.distributed as dist

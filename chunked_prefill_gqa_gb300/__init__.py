@@ -31,12 +31,13 @@ ATTN_EBOUNDS = -6
 ATTN_EDEVICE = -7
 ATTN_ETMA = -8
 ATTN_ECUDA = -9
+ATTN_ESPACE = -10
 MAX_TOKENS = 1 << 24
 PAGE = 16
 
 # Every symbol the header declares (the CPU tests check the library exports them).
-EXPORTS = ("attn_prefill", "attn_full_causal", "attn_prefill_paged", "attn_prefill_ffma",
-           "attn_reference_prefill", "attn_selftest_timeout", "attn_get_device_error", "attn_strerror", "attn_version")
+EXPORTS = ("attn_prefill", "attn_full_causal", "attn_prefill_paged", "attn_decode_paged",
+           "attn_decode_workspace_bytes", "attn_prefill_ffma", "attn_reference_prefill", "attn_selftest_timeout", "attn_get_device_error", "attn_strerror", "attn_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -70,6 +71,10 @@ def load():
                 fn.argtypes = [vp, vp, vp, vp, ci, ci, vp]
             lib.attn_prefill_paged.restype = ci
             lib.attn_prefill_paged.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, vp]
+            lib.attn_decode_paged.restype = ci
+            lib.attn_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, vp, ctypes.c_size_t, vp]
+            lib.attn_decode_workspace_bytes.restype = ctypes.c_size_t
+            lib.attn_decode_workspace_bytes.argtypes = [ci, ci, ci]
             lib.attn_full_causal.restype = ci
             lib.attn_full_causal.argtypes = [vp, vp, vp, vp, ci, vp]
             lib.attn_get_device_error.restype = ci
@@ -174,6 +179,42 @@ def attn_prefill_paged(q, kPages, vPages, blockTable, out, P: int, stream=None):
                                    C, P, num_pages, _stream_handle(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_prefill_paged")
+    return out
+
+
+def attn_decode_workspace_bytes(B: int, max_context: int, num_splits: int = 0) -> int:
+    """Bytes of workspace attn_decode_paged needs on the current device."""
+    return int(load().attn_decode_workspace_bytes(int(B), int(max_context), int(num_splits)))
+
+
+def attn_decode_paged(q, kPages, vPages, blockTable, contextLens, out, max_context: int,
+                      num_splits: int = 0, workspace=None, stream=None):
+    """One decode step: q, out [B][32][64]; kPages/vPages [numPages][16][8][64];
+    blockTable int32 [B][maxBlocks]; contextLens int32 [B] (device), each <=
+    max_context. ``workspace``: a CUDA tensor of at least
+    attn_decode_workspace_bytes(B, max_context, num_splits) bytes, or None when
+    none is needed."""
+    import torch
+    B = q.shape[0]
+    for name, t in (("q", q), ("out", out)):
+        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous() or tuple(t.shape) != (B, HQ, D):
+            raise ValueError(f"{name} must be a contiguous float32 CUDA tensor of shape ({B}, {HQ}, {D})")
+    for name, t in (("kPages", kPages), ("vPages", vPages)):
+        if (t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4
+                or tuple(t.shape[1:]) != (PAGE, HKV, D)):
+            raise ValueError(f"{name} must be a contiguous float32 CUDA tensor [numPages][16][8][64]")
+    if blockTable.dtype != torch.int32 or not blockTable.is_cuda or blockTable.dim() != 2 or blockTable.shape[0] != B:
+        raise ValueError("blockTable must be an int32 CUDA tensor [B][maxBlocks]")
+    if contextLens.dtype != torch.int32 or not contextLens.is_cuda or contextLens.numel() != B:
+        raise ValueError("contextLens must be an int32 CUDA tensor [B]")
+    blockTable = blockTable.contiguous()
+    ws_ptr = None if workspace is None else workspace.data_ptr()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().attn_decode_paged(_ptr(q), _ptr(kPages), _ptr(vPages), _ptr(blockTable), _ptr(contextLens),
+                                  _ptr(out), B, blockTable.shape[1], kPages.shape[0], int(max_context),
+                                  int(num_splits), ws_ptr, ws_bytes, _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_decode_paged")
     return out
 
 

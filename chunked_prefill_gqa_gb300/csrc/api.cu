@@ -65,6 +65,22 @@ int prepare(const float* q, const float* k, const float* v, float* out, int C, i
 
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ELAUNCH; }
 
+int sm_count(int* n) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ECUDA;
+  if (cudaDeviceGetAttribute(n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return ATTN_ECUDA;
+  return ATTN_OK;
+}
+
+// Shape checks shared by the decode entry points.
+int decode_shape_ok(int B, int maxBlocks, int numPages, int maxContext, int numSplits) {
+  if (B < 0 || maxBlocks < 1 || numPages < 1 || maxContext < 0 || numSplits < 0) return ATTN_EINVAL;
+  if (B > 65535 || (long long)maxBlocks * ATTN_PAGE > ATTN_MAX_TOKENS || numPages > ATTN_MAX_TOKENS / ATTN_PAGE ||
+      maxContext > maxBlocks * ATTN_PAGE)
+    return ATTN_ERANGE;
+  return ATTN_OK;
+}
+
 }  // namespace
 }  // namespace attn
 
@@ -111,6 +127,41 @@ extern "C" int attn_prefill_paged(const float* q, const float* kPages, const flo
   return launch_tc_paged(p, blockTable, numPages, stream);
 }
 
+extern "C" size_t attn_decode_workspace_bytes(int B, int maxContext, int numSplits) {
+  if (B <= 0 || maxContext < 0 || numSplits < 0) return 0;
+  int nsm = 0;
+  if (sm_count(&nsm) != ATTN_OK) return 0;
+  int split_len = 0;
+  const int splits = decode_splits(B, maxContext, numSplits, nsm, &split_len);
+  return decode_workspace_bytes(B, splits);
+}
+
+extern "C" int attn_decode_paged(const float* q, const float* kPages, const float* vPages,
+                                 const int* blockTable, const int* contextLens, float* out, int B,
+                                 int maxBlocks, int numPages, int maxContext, int numSplits, void* workspace,
+                                 size_t workspaceBytes, cudaStream_t stream) {
+  int rc = decode_shape_ok(B, maxBlocks, numPages, maxContext, numSplits);
+  if (rc != ATTN_OK || B == 0) return rc;
+  if (!q || !kPages || !vPages || !blockTable || !contextLens || !out) return ATTN_EINVAL;
+  if (!aligned16(q) || !aligned16(kPages) || !aligned16(vPages) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(blockTable) & 3u) || (reinterpret_cast<uintptr_t>(contextLens) & 3u))
+    return ATTN_EALIGN;
+  DeviceState* st = nullptr;
+  rc = current_device(&st);
+  if (rc != ATTN_OK) return rc;
+  int nsm = 0;
+  if ((rc = sm_count(&nsm)) != ATTN_OK) return rc;
+  int split_len = 0;
+  const int splits = decode_splits(B, maxContext, numSplits, nsm, &split_len);
+  const size_t need = decode_workspace_bytes(B, splits);
+  if (need > 0) {
+    if (!workspace || workspaceBytes < need) return ATTN_ESPACE;
+    if (!aligned16(workspace)) return ATTN_EALIGN;
+  }
+  return from_cuda(launch_decode(q, kPages, vPages, blockTable, contextLens, out, static_cast<float*>(workspace), B,
+                                 maxBlocks, numPages, maxContext, split_len, splits, st->err, stream));
+}
+
 extern "C" int attn_selftest_timeout(const float* q, const float* kCache, const float* vCache,
                                      float* out, int C, int P, cudaStream_t stream) {
   Problem p{};
@@ -146,10 +197,11 @@ extern "C" const char* attn_strerror(int code) {
     case ATTN_EDEVICE: return "the current device is not sm_103 (GB300)";
     case ATTN_ETMA: return "a TMA tensor map could not be encoded";
     case ATTN_ECUDA: return "a CUDA runtime call failed";
+    case ATTN_ESPACE: return "the workspace is missing or smaller than attn_decode_workspace_bytes()";
     default: return "unknown error code";
   }
 }
 
 extern "C" const char* attn_version(void) {
-  return "libattnprefill: tcgen05 split-TF32 / FFMA / reference kernels, sm_103a";
+  return "libattnprefill: tcgen05 split-TF32 prefill (contiguous and paged), split-KV GQA decode, FFMA and reference kernels, sm_103a";
 }

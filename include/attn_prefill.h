@@ -65,6 +65,7 @@ extern "C" {
 #define ATTN_EDEVICE -7     /* the current device is not sm_103 */
 #define ATTN_ETMA -8        /* a TMA tensor map could not be encoded */
 #define ATTN_ECUDA -9       /* another CUDA runtime call failed */
+#define ATTN_ESPACE -10     /* a workspace is missing or too small */
 
 /*
  * attn_prefill -- the main path: one persistent, warp-specialised tcgen05
@@ -103,6 +104,47 @@ int attn_prefill(const float *q, const float *kCache, const float *vCache, float
 int attn_prefill_paged(const float *q, const float *kPages, const float *vPages,
                        const int *blockTable, float *out, int C, int P, int numPages,
                        cudaStream_t stream);
+
+/*
+ * attn_decode_paged -- one decode step for B sequences: the chunk of one token
+ * (page 1, Lesson: the same formula at one row is decode, bandwidth-bound).
+ * Sequence b has one query per head, q[b][h][:], whose own key and value are
+ * already in the cache at position contextLens[b] - 1; it attends to keys
+ * 0 .. contextLens[b] - 1 with scale 1/8, query head h reading KV head h / 4:
+ *   out[b][h][:] = sum_{j < ctx_b} softmax_j(q[b][h] . k_b[j][h/4] / 8) v_b[j][h/4][:]
+ * The cache is paged ("FlashAttention and inference kernels", PagedAttention):
+ *   kPages, vPages  [numPages][16][8][64] fp32
+ *   blockTable      int32 [B][maxBlocks]: sequence b's token t is slot t % 16
+ *                   of page blockTable[b * maxBlocks + t / 16]
+ *   contextLens     int32 [B], each in [0, maxContext] (0 gives zeros)
+ *   q, out          [B][32][64] fp32
+ * A block owns (key segment, KV head, sequence) and all four query heads of
+ * that KV head, so each K/V row is read once per group; segments are merged
+ * with m = max m_s, w_s = e^(m_s - m) l_s, out = sum w_s O_s / sum w_s (same
+ * page, Flash-Decoding / split-K merge), skipping empty segments.
+ * numSplits: segments per sequence, 0 = chosen from B, maxContext and the SM
+ * count. With more than one segment the partials need `workspace`, a device
+ * buffer of at least attn_decode_workspace_bytes(B, maxContext, numSplits)
+ * bytes, 16-byte aligned, owned by the caller, overwritten by the call, not
+ * used after the call's kernels finish. Errors: ATTN_EINVAL (NULL pointer,
+ * negative size, maxBlocks or numPages < 1), ATTN_ERANGE (B > 65535,
+ * maxContext > 16 * maxBlocks, sizes above ATTN_MAX_TOKENS), ATTN_EALIGN,
+ * ATTN_ESPACE (workspace missing or too small). A context length outside
+ * [0, maxContext] or a page index outside [0, numPages) is recorded as
+ * ATTN_EBOUNDS in the device error word and clamped / read as zeros. B == 0 is
+ * a no-op.
+ */
+int attn_decode_paged(const float *q, const float *kPages, const float *vPages, const int *blockTable,
+                      const int *contextLens, float *out, int B, int maxBlocks, int numPages,
+                      int maxContext, int numSplits, void *workspace, size_t workspaceBytes,
+                      cudaStream_t stream);
+
+/*
+ * attn_decode_workspace_bytes -- the workspace attn_decode_paged needs for the
+ * same (B, maxContext, numSplits) on the current device; 0 when one segment
+ * per sequence suffices (or for invalid arguments).
+ */
+size_t attn_decode_workspace_bytes(int B, int maxContext, int numSplits);
 
 /*
  * attn_full_causal -- a whole prompt with nothing cached: identical to

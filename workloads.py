@@ -234,3 +234,56 @@ def to_pages(inp: Inputs, seed: int = 7, spare_pages: int = 5) -> Paged:
     k_pages[table[t // PAGE], t % PAGE] = inp.k
     v_pages[table[t // PAGE], t % PAGE] = inp.v
     return Paged(k_pages=k_pages, v_pages=v_pages, table=table)
+
+
+@dataclass
+class DecodeBatch:
+    """One decode step for B sequences against a paged cache.
+
+    q [B][32][64]; k_pages / v_pages [num_pages][16][8][64] (unused slots and
+    spare pages NaN); table int32 [B][max_blocks] (entries past a sequence's
+    pages are -1 and must never be read); ctx int32 [B]."""
+    q: np.ndarray
+    k_pages: np.ndarray
+    v_pages: np.ndarray
+    table: np.ndarray
+    ctx: np.ndarray
+
+    @property
+    def max_context(self) -> int:
+        return int(self.ctx.max()) if self.ctx.size else 0
+
+
+def decode_batch(ctx_lens, seed: int = 1, spare_pages: int = 3, planted=()) -> DecodeBatch:
+    """Sequences of the given context lengths (the decode teaching program of
+    "FlashAttention and inference kernels" uses 1, 17, 1000 and 4096), pages
+    shuffled over one pool. ``planted`` = positions t: each sequence with
+    ctx > t gets 4.0 in KV head 0 at t, and query head 0 of every sequence is 4.0."""
+    ctx = np.asarray(ctx_lens, dtype=np.int32)
+    B = ctx.size
+    pages_per = (ctx + PAGE - 1) // PAGE
+    max_blocks = max(1, int(pages_per.max()) if B else 1)
+    n_pages = int(pages_per.sum()) + spare_pages
+    perm = np.argsort(uniform(seed + 7, n_pages), kind="stable").astype(np.int32)
+    q = uniform(seed, B * HQ * D).reshape(B, HQ, D)
+    k_pages = np.full((n_pages, PAGE, HKV, D), np.nan, dtype=np.float32)
+    v_pages = np.full((n_pages, PAGE, HKV, D), np.nan, dtype=np.float32)
+    table = np.full((B, max_blocks), -1, dtype=np.int32)
+    nxt = 0
+    for b in range(B):
+        T = int(ctx[b])
+        k = uniform(seed + 1 + 2 * b + 1000, T * HKV * D).reshape(T, HKV, D)
+        v = uniform(seed + 2 + 2 * b + 1000, T * HKV * D).reshape(T, HKV, D)
+        if planted:
+            q[b, 0, :] = 4.0
+            for t in planted:
+                if t < T:
+                    k[t, 0, :] = 4.0
+                    v[t, 0, :] = 4.0
+        for lp in range(int(pages_per[b])):
+            table[b, lp] = perm[nxt]
+            nxt += 1
+        t = np.arange(T)
+        k_pages[table[b, t // PAGE], t % PAGE] = k
+        v_pages[table[b, t // PAGE], t % PAGE] = v
+    return DecodeBatch(q=q, k_pages=k_pages, v_pages=v_pages, table=table, ctx=ctx)
