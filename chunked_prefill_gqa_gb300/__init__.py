@@ -32,12 +32,14 @@ ATTN_EDEVICE = -7
 ATTN_ETMA = -8
 ATTN_ECUDA = -9
 ATTN_ESPACE = -10
+ATTN_ESCRATCH = -11
+DECODE_SCRATCH_BYTES = 4 << 20
 MAX_TOKENS = 1 << 24
 PAGE = 16
 
 # Every symbol the header declares (the CPU tests check the library exports them).
 EXPORTS = ("attn_prefill", "attn_full_causal", "attn_prefill_paged", "attn_decode_paged",
-           "attn_decode_workspace_bytes", "attn_prefill_ffma", "attn_reference_prefill", "attn_selftest_timeout", "attn_get_device_error", "attn_strerror", "attn_version")
+           "attn_decode_workspace_bytes", "attn_decode_paged_noalloc", "attn_prefill_ffma", "attn_reference_prefill", "attn_selftest_timeout", "attn_get_device_error", "attn_strerror", "attn_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -73,6 +75,8 @@ def load():
             lib.attn_prefill_paged.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, vp]
             lib.attn_decode_paged.restype = ci
             lib.attn_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, vp, ctypes.c_size_t, vp]
+            lib.attn_decode_paged_noalloc.restype = ci
+            lib.attn_decode_paged_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, vp]
             lib.attn_decode_workspace_bytes.restype = ctypes.c_size_t
             lib.attn_decode_workspace_bytes.argtypes = [ci, ci, ci]
             lib.attn_full_causal.restype = ci
@@ -215,6 +219,40 @@ def attn_decode_paged(q, kPages, vPages, blockTable, contextLens, out, max_conte
                                   int(num_splits), ws_ptr, ws_bytes, _stream_handle(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_decode_paged")
+    return out
+
+
+def _check_decode_args(q, kPages, vPages, blockTable, contextLens, out):
+    import torch
+    B = q.shape[0]
+    for name, t in (("q", q), ("out", out)):
+        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous() or tuple(t.shape) != (B, HQ, D):
+            raise ValueError(f"{name} must be a contiguous float32 CUDA tensor of shape ({B}, {HQ}, {D})")
+    for name, t in (("kPages", kPages), ("vPages", vPages)):
+        if (t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4
+                or tuple(t.shape[1:]) != (PAGE, HKV, D)):
+            raise ValueError(f"{name} must be a contiguous float32 CUDA tensor [numPages][16][8][64]")
+    if blockTable.dtype != torch.int32 or not blockTable.is_cuda or blockTable.dim() != 2 or blockTable.shape[0] != B:
+        raise ValueError("blockTable must be an int32 CUDA tensor [B][maxBlocks]")
+    if contextLens.dtype != torch.int32 or not contextLens.is_cuda or contextLens.numel() != B:
+        raise ValueError("contextLens must be an int32 CUDA tensor [B]")
+
+
+def attn_decode_paged_noalloc(q, kPages, vPages, blockTable, contextLens, out, max_context: int,
+                              num_splits: int = 0, stream=None):
+    """attn_decode_paged with the partials in the library's fixed 4 MiB device
+    scratch instead of a caller workspace: nothing is allocated. For callers
+    that cannot provide device memory. Calls that may overlap (other streams,
+    other threads) race on the shared scratch; the first call on a device looks
+    up its address and should come before any stream capture."""
+    _check_decode_args(q, kPages, vPages, blockTable, contextLens, out)
+    blockTable = blockTable.contiguous()
+    rc = load().attn_decode_paged_noalloc(_ptr(q), _ptr(kPages), _ptr(vPages), _ptr(blockTable),
+                                          _ptr(contextLens), _ptr(out), q.shape[0], blockTable.shape[1],
+                                          kPages.shape[0], int(max_context), int(num_splits),
+                                          _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_decode_paged_noalloc")
     return out
 
 

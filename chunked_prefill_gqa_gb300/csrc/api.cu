@@ -162,6 +162,31 @@ extern "C" int attn_decode_paged(const float* q, const float* kPages, const floa
                                  maxBlocks, numPages, maxContext, split_len, splits, st->err, stream));
 }
 
+extern "C" int attn_decode_paged_noalloc(const float* q, const float* kPages, const float* vPages,
+                                         const int* blockTable, const int* contextLens, float* out, int B,
+                                         int maxBlocks, int numPages, int maxContext, int numSplits,
+                                         cudaStream_t stream) {
+  static_assert(kDecodeScratchBytes == ATTN_DECODE_SCRATCH_BYTES, "scratch size and header disagree");
+  int rc = decode_shape_ok(B, maxBlocks, numPages, maxContext, numSplits);
+  if (rc != ATTN_OK || B == 0) return rc;
+  if (!q || !kPages || !vPages || !blockTable || !contextLens || !out) return ATTN_EINVAL;
+  if (!aligned16(q) || !aligned16(kPages) || !aligned16(vPages) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(blockTable) & 3u) || (reinterpret_cast<uintptr_t>(contextLens) & 3u))
+    return ATTN_EALIGN;
+  DeviceState* st = nullptr;
+  rc = current_device(&st);
+  if (rc != ATTN_OK) return rc;
+  int nsm = 0;
+  if ((rc = sm_count(&nsm)) != ATTN_OK) return rc;
+  int split_len = 0;
+  const int splits = decode_splits(B, maxContext, numSplits, nsm, &split_len);
+  if (decode_workspace_bytes(B, splits) > kDecodeScratchBytes) return ATTN_ESCRATCH;
+  float* scratch = nullptr;
+  if (decode_scratch(&scratch) != cudaSuccess) return ATTN_ECUDA;
+  return from_cuda(launch_decode(q, kPages, vPages, blockTable, contextLens, out, scratch, B, maxBlocks, numPages,
+                                 maxContext, split_len, splits, st->err, stream));
+}
+
 extern "C" int attn_selftest_timeout(const float* q, const float* kCache, const float* vCache,
                                      float* out, int C, int P, cudaStream_t stream) {
   Problem p{};
@@ -198,6 +223,9 @@ extern "C" const char* attn_strerror(int code) {
     case ATTN_ETMA: return "a TMA tensor map could not be encoded";
     case ATTN_ECUDA: return "a CUDA runtime call failed";
     case ATTN_ESPACE: return "the workspace is missing or smaller than attn_decode_workspace_bytes()";
+    case ATTN_ESCRATCH:
+      return "the decode partials exceed the library's fixed scratch (ATTN_DECODE_SCRATCH_BYTES): "
+             "use fewer splits or attn_decode_paged with a workspace";
     default: return "unknown error code";
   }
 }

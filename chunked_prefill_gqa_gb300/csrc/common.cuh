@@ -55,6 +55,10 @@ size_t decode_workspace_bytes(int B, int splits);
 cudaError_t launch_decode(const float* q, const float* k_pages, const float* v_pages, const int* table,
                           const int* ctx_lens, float* out, float* parts, int B, int max_blocks, int num_pages,
                           int max_context, int split_len, int splits, unsigned* err, cudaStream_t stream);
+// The fixed partials scratch of attn_decode_paged_noalloc (decode.cu) and its
+// device address on the current device (looked up on the first call).
+constexpr size_t kDecodeScratchBytes = size_t(4) << 20;
+cudaError_t decode_scratch(float** ptr);
 // Paged K/V: p.k / p.v point at [num_pages * 16][8][64] page pools.
 int launch_tc_paged(const Problem& p, const int* table, int num_pages, cudaStream_t stream);
 

@@ -20,6 +20,8 @@
 // m = max_s m_s, w_s = e^{m_s - m} l_s, O = sum_s w_s O_s / sum_s w_s, skipping
 // segments with l_s = 0 (m_s = -inf). With one segment the split kernel writes
 // the output directly and no partials are stored.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace attn {
@@ -222,6 +224,33 @@ decode_merge_kernel(DecodeArgs a) {
 }
 
 }  // namespace
+
+// The library's own partials buffer for attn_decode_paged_noalloc: a fixed
+// array in device global memory, created with the module, so that entry point
+// needs neither a workspace from the caller nor an allocation of its own. Every
+// call on a device shares it. Nothing in it has to start at zero: the split
+// kernel writes each (sequence, KV head, segment) record, m_s and l_s always
+// and O_s whenever l_s > 0, before the merge kernel of the same call reads it.
+static __device__ __align__(256) float g_decode_scratch[kDecodeScratchBytes / sizeof(float)];
+
+cudaError_t decode_scratch(float** ptr) {
+  constexpr int kMaxDev = 64;
+  static std::mutex mu;
+  static float* addr[kMaxDev] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {  // once per device, with that device current
+    void* a = nullptr;
+    e = cudaGetSymbolAddress(&a, g_decode_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = static_cast<float*>(a);
+  }
+  *ptr = addr[dev];
+  return cudaSuccess;
+}
 
 int decode_splits(int B, int max_context, int splits_hint, int num_sms, int* split_len) {
   int splits = splits_hint;

@@ -66,6 +66,10 @@ extern "C" {
 #define ATTN_ETMA -8        /* a TMA tensor map could not be encoded */
 #define ATTN_ECUDA -9       /* another CUDA runtime call failed */
 #define ATTN_ESPACE -10     /* a workspace is missing or too small */
+#define ATTN_ESCRATCH -11   /* the decode partials exceed ATTN_DECODE_SCRATCH_BYTES */
+
+/* Size of the fixed device scratch behind attn_decode_paged_noalloc. */
+#define ATTN_DECODE_SCRATCH_BYTES (4u << 20)
 
 /*
  * attn_prefill -- the main path: one persistent, warp-specialised tcgen05
@@ -145,6 +149,41 @@ int attn_decode_paged(const float *q, const float *kPages, const float *vPages, 
  * per sequence suffices (or for invalid arguments).
  */
 size_t attn_decode_workspace_bytes(int B, int maxContext, int numSplits);
+
+/*
+ * attn_decode_paged_noalloc -- attn_decode_paged without a workspace argument,
+ * for callers that cannot hand the library any device memory: a serving loop
+ * whose buffers are all planned once at start-up, a C host that has no access
+ * to the device allocator of the framework that owns the GPU, or a
+ * latency-critical path where a cudaMalloc (which may synchronise the device)
+ * is not allowed. The pages describe no such variant; it exists for those
+ * callers only and computes exactly what attn_decode_paged computes with the
+ * same numSplits.
+ *
+ * The segment partials go to one fixed buffer of ATTN_DECODE_SCRATCH_BYTES
+ * (4 MiB) that is part of the library's device image, so the call allocates
+ * nothing, neither here nor in any library it calls. That buffer holds
+ * B * 8 * splits records of 1056 bytes; the automatic split count keeps B * splits
+ * below 2 * SMs / 8 + B, under 1 MiB on a 152-SM GB300. A call whose partials would not fit (a large
+ * explicit numSplits with many sequences) returns ATTN_ESCRATCH and enqueues
+ * nothing; one segment per sequence uses no scratch at all.
+ *
+ * Sharing. All calls on a device use the same buffer, which keeps whatever the
+ * last call left there (nothing in it needs to start at zero: each call writes
+ * every record it reads). Two calls that can run at the same time, on
+ * different streams or from different host threads without ordering between
+ * them, race on it and may return wrong results: order them on one stream or
+ * use attn_decode_paged with a workspace each.
+ *
+ * Set-up. The first call on a device, with that device current, looks up the
+ * buffer's device address (cudaGetSymbolAddress) and caches it; make that
+ * first call before any stream capture. Arguments, layouts and other errors as
+ * attn_decode_paged; ATTN_ECUDA if the address lookup fails.
+ */
+int attn_decode_paged_noalloc(const float *q, const float *kPages, const float *vPages,
+                              const int *blockTable, const int *contextLens, float *out, int B,
+                              int maxBlocks, int numPages, int maxContext, int numSplits,
+                              cudaStream_t stream);
 
 /*
  * attn_full_causal -- a whole prompt with nothing cached: identical to
