@@ -64,8 +64,9 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--path", default="attn_prefill",
                     choices=["attn_prefill", "attn_prefill_ffma", "attn_reference_prefill"])
-    ap.add_argument("--workload", choices=["serve", "long", "decode"], default="serve",
-                    help="decode: one decode step of 16 sequences x 16384 cached tokens (paged)")
+    ap.add_argument("--workload", choices=["serve", "long", "decode", "matrix"], default="serve",
+                    help="decode: one decode step of 16 sequences x 16384 cached tokens (paged); "
+                         "matrix: the three-kernel score-matrix pipeline at T = 512, 1024, 2048")
     ap.add_argument("--paged", action="store_true",
                     help="time attn_prefill_paged on the same workload scattered into shuffled 16-token pages")
     ap.add_argument("--seed", type=int, default=1)
@@ -325,12 +326,92 @@ def run_decode(args):
     return 0
 
 
+def run_matrix(args):
+    """The three-kernel score-matrix pipeline on full prompts of 512, 1024 and
+    2048 tokens (the sizes the full-score-matrix lab prints), each kernel timed
+    with CUDA events, beside attn_full_causal on the same inputs. The line's
+    value is the pipeline's time at T = 2048."""
+    import torch
+    import chunked_prefill_gqa_gb300 as cp
+    from chunked_prefill_gqa_gb300 import build as B
+    torch.cuda.set_device(0)
+    B.build()
+    cp.load()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    peaks = load_peaks()
+    ffma_peak = NUM_SMS * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+    table = []
+    for T in W.FULL_T:
+        inp = W.full_causal(T, seed=args.seed)
+        q = torch.from_numpy(inp.q).to(dev)
+        k = torch.from_numpy(inp.k).to(dev)
+        v = torch.from_numpy(inp.v).to(dev)
+        out = torch.empty_like(q)
+        ws = torch.empty(cp.attn_naive_workspace_bytes(T, 0) // 4, dtype=torch.float32, device=dev)
+        steps = [lambda: cp.attn_naive_scores(q, k, ws, 0, stream),
+                 lambda: cp.attn_naive_softmax(ws, T, 0, stream),
+                 lambda: cp.attn_naive_weighted_sum(ws, v, out, 0, stream),
+                 lambda: cp.attn_full_causal(q, k, v, out, stream)]
+        for _ in range(args.warmup):
+            for f in steps:
+                f()
+        n = args.steps
+        ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in steps]
+              for _ in range(n)]
+        torch.cuda.synchronize()
+        for i in range(n):
+            for j, f in enumerate(steps):
+                flush.zero_()
+                ev[i][j][0].record(stream)
+                f()
+                ev[i][j][1].record(stream)
+        torch.cuda.synchronize()
+        if cp.attn_get_device_error() != 0:
+            raise RuntimeError("device error in the matrix bench")
+        ms = [sum(ev[i][j][0].elapsed_time(ev[i][j][1]) for i in range(n)) / n for j in range(len(steps))]
+        visible = 32 * T * (T + 1) // 2
+        matrix = 32 * T * T * 4
+        table.append({
+            "T": T, "matrix_mib": matrix / 2**20,
+            "scores_ms": round(ms[0], 4), "softmax_ms": round(ms[1], 4), "weighted_sum_ms": round(ms[2], 4),
+            "pipeline_ms": round(ms[0] + ms[1] + ms[2], 4), "flash_ms": round(ms[3], 4),
+            "scores_tflops": round(2 * 64 * visible / (ms[0] * 1e-3) / 1e12, 2),
+            "softmax_gbs": round((4 * visible + matrix) / (ms[1] * 1e-3) / 1e9, 1),
+            "weighted_sum_tflops": round(2 * 64 * visible / (ms[2] * 1e-3) / 1e12, 2)})
+        del ws
+        torch.cuda.empty_cache()
+    last = table[-1]
+    dom = max(("scores", "softmax", "weighted_sum"), key=lambda name: last[name + "_ms"])
+    if dom == "softmax":
+        rl = {"bound": "hbm", "kernel": "naive_softmax_kernel", "achieved": last["softmax_gbs"],
+              "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(last["softmax_gbs"] / peaks["hbm_gbs"], 4)}
+    else:
+        a = last[dom + "_tflops"]
+        rl = {"bound": "alu", "kernel": f"naive_{dom}_kernel", "achieved": a, "peak": round(ffma_peak, 2),
+              "unit": "TFLOP/s", "frac": round(a / ffma_peak, 4),
+              "peak_note": f"152 SMs x 128 FFMA/clk x 2 flop x {peaks['sm_max_mhz']:.0f} MHz"}
+    rl["traffic"] = None
+    line = {"metric": "score-matrix pipeline attention time, full prompt T=2048 (32q/8kv, d=64)",
+            "value": last["pipeline_ms"], "unit": "ms", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": last["pipeline_ms"], "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "full causal prompts T = 512, 1024, 2048; workspace 32 x T x T fp32",
+                       "l2": "flushed (256 MiB write) before every kernel", "sizes": table},
+            "roofline": rl, "gpu_launches": 4 * args.steps * len(W.FULL_T)}
+    print(json.dumps(line))
+    return 0
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
     if args.workload == "decode":
         return run_decode(args)
+    if args.workload == "matrix":
+        return run_matrix(args)
 
     import torch
     import torch.distributed as dist

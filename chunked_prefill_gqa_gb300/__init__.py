@@ -39,7 +39,9 @@ PAGE = 16
 
 # Every symbol the header declares (the CPU tests check the library exports them).
 EXPORTS = ("attn_prefill", "attn_full_causal", "attn_prefill_paged", "attn_decode_paged",
-           "attn_decode_workspace_bytes", "attn_decode_paged_noalloc", "attn_prefill_ffma", "attn_reference_prefill", "attn_selftest_timeout", "attn_get_device_error", "attn_strerror", "attn_version")
+           "attn_decode_workspace_bytes", "attn_decode_paged_noalloc",
+           "attn_naive_workspace_bytes", "attn_naive_scores", "attn_naive_softmax", "attn_naive_weighted_sum",
+           "attn_naive_prefill", "attn_prefill_ffma", "attn_reference_prefill", "attn_selftest_timeout", "attn_get_device_error", "attn_strerror", "attn_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -79,6 +81,16 @@ def load():
             lib.attn_decode_paged_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, vp]
             lib.attn_decode_workspace_bytes.restype = ctypes.c_size_t
             lib.attn_decode_workspace_bytes.argtypes = [ci, ci, ci]
+            lib.attn_naive_workspace_bytes.restype = ctypes.c_size_t
+            lib.attn_naive_workspace_bytes.argtypes = [ci, ci]
+            lib.attn_naive_scores.restype = ci
+            lib.attn_naive_scores.argtypes = [vp, vp, vp, ci, ci, vp]
+            lib.attn_naive_softmax.restype = ci
+            lib.attn_naive_softmax.argtypes = [vp, ci, ci, vp]
+            lib.attn_naive_weighted_sum.restype = ci
+            lib.attn_naive_weighted_sum.argtypes = [vp, vp, vp, ci, ci, vp]
+            lib.attn_naive_prefill.restype = ci
+            lib.attn_naive_prefill.argtypes = [vp, vp, vp, vp, vp, ctypes.c_size_t, ci, ci, vp]
             lib.attn_full_causal.restype = ci
             lib.attn_full_causal.argtypes = [vp, vp, vp, vp, ci, vp]
             lib.attn_get_device_error.restype = ci
@@ -253,6 +265,61 @@ def attn_decode_paged_noalloc(q, kPages, vPages, blockTable, contextLens, out, m
                                           _stream_handle(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_decode_paged_noalloc")
+    return out
+
+
+def attn_naive_workspace_bytes(C: int, P: int) -> int:
+    """Bytes of the score matrix [32][C][P + C] fp32."""
+    return int(load().attn_naive_workspace_bytes(int(C), int(P)))
+
+
+def _naive_scores_arg(scores, C: int, P: int):
+    import torch
+    if (scores.dtype != torch.float32 or not scores.is_cuda or not scores.is_contiguous()
+            or scores.numel() * 4 < attn_naive_workspace_bytes(C, P)):
+        raise ValueError(f"scores must be a contiguous float32 CUDA tensor of at least 32 x {C} x {P + C} elements")
+    return scores.data_ptr()
+
+
+def attn_naive_prefill(q, kCache, vCache, out, scores, P: int, stream=None):
+    """The three-kernel score-matrix pipeline: scores, in-place row softmax,
+    weighted sum, with ``scores`` the [32][C][P + C] fp32 workspace."""
+    C = q.shape[0]
+    _check_tensors(q, kCache, vCache, out, C, P)
+    ws = _naive_scores_arg(scores, C, P)
+    rc = load().attn_naive_prefill(_ptr(q), _ptr(kCache), _ptr(vCache), _ptr(out), ws,
+                                   scores.numel() * 4, C, int(P), _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_naive_prefill")
+    return out
+
+
+def attn_naive_scores(q, kCache, scores, P: int, stream=None):
+    """Step 1: scores[h][i][j] = q[i][h] . k[j][h/4] / 8, -inf above the diagonal."""
+    C = q.shape[0]
+    ws = _naive_scores_arg(scores, C, P)
+    rc = load().attn_naive_scores(_ptr(q), _ptr(kCache), ws, C, int(P), _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_naive_scores")
+    return scores
+
+
+def attn_naive_softmax(scores, C: int, P: int, stream=None):
+    """Step 2: every row of the score matrix replaced by its softmax, in place."""
+    ws = _naive_scores_arg(scores, C, P)
+    rc = load().attn_naive_softmax(ws, int(C), int(P), _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_naive_softmax")
+    return scores
+
+
+def attn_naive_weighted_sum(scores, vCache, out, P: int, stream=None):
+    """Step 3: out[i][h][:] = sum_j scores[h][i][j] v[j][h/4][:]."""
+    C = out.shape[0]
+    ws = _naive_scores_arg(scores, C, P)
+    rc = load().attn_naive_weighted_sum(ws, _ptr(vCache), _ptr(out), C, int(P), _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_naive_weighted_sum")
     return out
 
 

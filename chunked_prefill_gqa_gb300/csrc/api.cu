@@ -81,6 +81,15 @@ int decode_shape_ok(int B, int maxBlocks, int numPages, int maxContext, int numS
   return ATTN_OK;
 }
 
+// Shared validation of the score-matrix entry points: sizes, and (for C > 0)
+// the device. The pointers are checked by each caller.
+int naive_prepare(int C, int P, DeviceState** st) {
+  if (C < 0 || P < 0) return ATTN_EINVAL;
+  if (C > ATTN_MAX_TOKENS || (long long)P + C > ATTN_MAX_TOKENS || C > naive_max_rows()) return ATTN_ERANGE;
+  if (C == 0) return ATTN_OK;
+  return current_device(st);
+}
+
 }  // namespace
 }  // namespace attn
 
@@ -187,6 +196,54 @@ extern "C" int attn_decode_paged_noalloc(const float* q, const float* kPages, co
                                  maxContext, split_len, splits, st->err, stream));
 }
 
+extern "C" size_t attn_naive_workspace_bytes(int C, int P) {
+  if (C < 0 || P < 0 || (long long)P + C > ATTN_MAX_TOKENS) return 0;
+  return naive_workspace_bytes(C, P);
+}
+
+extern "C" int attn_naive_scores(const float* q, const float* kCache, float* scores, int C, int P,
+                                 cudaStream_t stream) {
+  DeviceState* st = nullptr;
+  const int rc = naive_prepare(C, P, &st);
+  if (rc != ATTN_OK || C == 0) return rc;
+  if (!q || !kCache || !scores) return ATTN_EINVAL;
+  if (!aligned16(q) || !aligned16(kCache) || !aligned16(scores)) return ATTN_EALIGN;
+  return from_cuda(launch_naive_scores(q, kCache, scores, C, P, stream));
+}
+
+extern "C" int attn_naive_softmax(float* scores, int C, int P, cudaStream_t stream) {
+  DeviceState* st = nullptr;
+  const int rc = naive_prepare(C, P, &st);
+  if (rc != ATTN_OK || C == 0) return rc;
+  if (!scores) return ATTN_EINVAL;
+  if (!aligned16(scores)) return ATTN_EALIGN;
+  return from_cuda(launch_naive_softmax(scores, C, P, stream));
+}
+
+extern "C" int attn_naive_weighted_sum(const float* scores, const float* vCache, float* out, int C, int P,
+                                       cudaStream_t stream) {
+  DeviceState* st = nullptr;
+  const int rc = naive_prepare(C, P, &st);
+  if (rc != ATTN_OK || C == 0) return rc;
+  if (!scores || !vCache || !out) return ATTN_EINVAL;
+  if (!aligned16(scores) || !aligned16(vCache) || !aligned16(out)) return ATTN_EALIGN;
+  return from_cuda(launch_naive_weighted_sum(scores, vCache, out, C, P, stream));
+}
+
+extern "C" int attn_naive_prefill(const float* q, const float* kCache, const float* vCache, float* out,
+                                  float* scores, size_t scoresBytes, int C, int P, cudaStream_t stream) {
+  DeviceState* st = nullptr;
+  int rc = naive_prepare(C, P, &st);
+  if (rc != ATTN_OK || C == 0) return rc;
+  if (!q || !kCache || !vCache || !out) return ATTN_EINVAL;
+  if (!scores || scoresBytes < naive_workspace_bytes(C, P)) return ATTN_ESPACE;
+  if (!aligned16(q) || !aligned16(kCache) || !aligned16(vCache) || !aligned16(out) || !aligned16(scores))
+    return ATTN_EALIGN;
+  if ((rc = from_cuda(launch_naive_scores(q, kCache, scores, C, P, stream))) != ATTN_OK) return rc;
+  if ((rc = from_cuda(launch_naive_softmax(scores, C, P, stream))) != ATTN_OK) return rc;
+  return from_cuda(launch_naive_weighted_sum(scores, vCache, out, C, P, stream));
+}
+
 extern "C" int attn_selftest_timeout(const float* q, const float* kCache, const float* vCache,
                                      float* out, int C, int P, cudaStream_t stream) {
   Problem p{};
@@ -231,5 +288,5 @@ extern "C" const char* attn_strerror(int code) {
 }
 
 extern "C" const char* attn_version(void) {
-  return "libattnprefill: tcgen05 split-TF32 prefill (contiguous and paged), split-KV GQA decode, FFMA and reference kernels, sm_103a";
+  return "libattnprefill: tcgen05 split-TF32 prefill (contiguous and paged), split-KV GQA decode, FFMA, score-matrix and reference kernels, sm_103a";
 }

@@ -55,6 +55,14 @@ size_t decode_workspace_bytes(int B, int splits);
 cudaError_t launch_decode(const float* q, const float* k_pages, const float* v_pages, const int* table,
                           const int* ctx_lens, float* out, float* parts, int B, int max_blocks, int num_pages,
                           int max_context, int split_len, int splits, unsigned* err, cudaStream_t stream);
+// Three-kernel score-matrix attention (naive.cu): workspace bytes, the row
+// limit of its grids, and one launcher per kernel.
+size_t naive_workspace_bytes(int C, int P);
+int naive_max_rows();
+cudaError_t launch_naive_scores(const float* q, const float* k, float* S, int C, int P, cudaStream_t stream);
+cudaError_t launch_naive_softmax(float* S, int C, int P, cudaStream_t stream);
+cudaError_t launch_naive_weighted_sum(const float* S, const float* v, float* out, int C, int P,
+                                      cudaStream_t stream);
 // The fixed partials scratch of attn_decode_paged_noalloc (decode.cu) and its
 // device address on the current device (looked up on the first call).
 constexpr size_t kDecodeScratchBytes = size_t(4) << 20;

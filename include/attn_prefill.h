@@ -186,6 +186,35 @@ int attn_decode_paged_noalloc(const float *q, const float *kPages, const float *
                               cudaStream_t stream);
 
 /*
+ * The score-matrix pipeline ("Inference Attention 1: The Full Score Matrix",
+ * Lesson): attention as an eager framework runs it, three kernels with the
+ * whole score matrix in global memory between them. It is the in-run measure
+ * of what that matrix costs; attn_prefill computes the same result without it.
+ *
+ *   scores  [32][C][P + C] fp32, device, owned by the caller: row i of head h
+ *           at scores + (h * C + i) * (P + C), 16-byte aligned,
+ *           attn_naive_workspace_bytes(C, P) bytes (32 x T x T floats for a
+ *           full prompt of T tokens: 512 MiB at T = 2048).
+ *
+ * attn_naive_scores writes q[i][h] . k[j][h/4] / 8 for j <= P + i and -inf
+ * above the diagonal; attn_naive_softmax replaces each row in place by its
+ * softmax (maximum subtracted first; 0 above the diagonal); attn_naive_weighted_sum
+ * writes out[i][h][:] = sum_j scores[h][i][j] v[j][h/4][:]. attn_naive_prefill
+ * runs the three in order on `stream` and returns ATTN_ESPACE if scoresBytes is
+ * too small. q, kCache, vCache and out are as for attn_prefill. Errors as
+ * attn_prefill, plus ATTN_ERANGE for C above 4,194,240 (the grid's row limit).
+ * C == 0 is a no-op. attn_naive_workspace_bytes returns 0 for invalid sizes.
+ */
+size_t attn_naive_workspace_bytes(int C, int P);
+int attn_naive_scores(const float *q, const float *kCache, float *scores, int C, int P,
+                      cudaStream_t stream);
+int attn_naive_softmax(float *scores, int C, int P, cudaStream_t stream);
+int attn_naive_weighted_sum(const float *scores, const float *vCache, float *out, int C, int P,
+                            cudaStream_t stream);
+int attn_naive_prefill(const float *q, const float *kCache, const float *vCache, float *out,
+                       float *scores, size_t scoresBytes, int C, int P, cudaStream_t stream);
+
+/*
  * attn_full_causal -- a whole prompt with nothing cached: identical to
  * attn_prefill(q, k, v, out, T, 0, stream) ("Inference Attention 1: The Full
  * Score Matrix", Lesson: q [T][32][64], k and v [T][8][64], row i sees j <= i).

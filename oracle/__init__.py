@@ -137,6 +137,33 @@ def prefill_paged(q, k_pages, v_pages, table, P: int, rows=None, threads: int = 
                      rows=rows, threads=threads)
 
 
+def score_matrix(q, k, P: int, scale: float = 0.125) -> np.ndarray:
+    """The score workspace of the three-kernel pipeline ("Inference Attention 1:
+    The Full Score Matrix", Lesson): S[h][i][j] = q[i][h] . k[j][h / 4] * scale
+    in float64 for keys j <= P + i, -inf above that diagonal. Shape
+    [HQ][C][P + C]; one float64 matmul per head."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    C, HQ, _ = q.shape
+    T, HKV, _ = k.shape
+    if T != P + C:
+        raise ValueError(f"k has {T} rows, expected P + C = {P + C}")
+    group = HQ // HKV
+    allowed = np.arange(T)[None, :] <= (P + np.arange(C))[:, None]
+    S = np.empty((HQ, C, T))
+    for h in range(HQ):
+        S[h] = np.where(allowed, (q[:, h, :] @ k[:, h // group, :].T) * scale, -np.inf)
+    return S
+
+
+def probability_matrix(S) -> np.ndarray:
+    """Each row of a score workspace replaced by its softmax, maximum subtracted
+    first (same page: the row softmax of the middle kernel; -inf becomes 0)."""
+    S = np.asarray(S, dtype=np.float64)
+    E = np.exp(S - S.max(axis=-1, keepdims=True))
+    return E / E.sum(axis=-1, keepdims=True)
+
+
 def violations(got, ref, atol: float = ATOL, rtol: float = RTOL) -> np.ndarray:
     """Boolean mask of elements failing |got - ref| <= atol + rtol * |ref| (NaN fails)."""
     got = np.asarray(got, dtype=np.float64)

@@ -122,3 +122,37 @@ def test_paged_gather_follows_the_table():
     pages[0, :4, 0, 0] = 16 + np.arange(4)
     got = oracle.gather_pages(pages, np.array([1, 0]), 20)
     np.testing.assert_array_equal(got[:, 0, 0], np.arange(20))
+
+
+def test_score_matrix_by_brute_force():
+    """Every entry of the oracle's score workspace is the plain dot product of
+    its (position, head) query and (key, KV head h / 4) key, times 1/8, and -inf
+    exactly where the key is past the row's position."""
+    inp = W.edge(5, 3)
+    S = oracle.score_matrix(inp.q, inp.k, inp.P)
+    assert S.shape == (W.HQ, 5, 8)
+    for h in (0, 3, 4, 17, 31):
+        for i in range(5):
+            for j in range(8):
+                if j > inp.P + i:
+                    assert S[h, i, j] == -math.inf
+                else:
+                    dot = sum(float(inp.q[i, h, d]) * float(inp.k[j, h // 4, d]) for d in range(W.D))
+                    assert abs(S[h, i, j] - dot / 8.0) <= 1e-14
+
+
+def test_probability_matrix_rows_and_pipeline_equal_the_oracle():
+    """Rows of the probability workspace sum to 1, are exactly 0 above the
+    diagonal and exactly 1 on a single-token row; multiplied by V they give the
+    C oracle's attention, which is computed by a different route (two passes
+    per row, no matrix)."""
+    for inp in (W.edge(1, 0), W.edge(17, 31), W.edge(33, 0, variant="ramp"), W.tiny()):
+        Pm = oracle.probability_matrix(oracle.score_matrix(inp.q, inp.k, inp.P))
+        np.testing.assert_allclose(Pm.sum(axis=-1), 1.0, rtol=0, atol=1e-13)
+        above = np.arange(inp.P + inp.C)[None, :] > (inp.P + np.arange(inp.C))[:, None]
+        assert (Pm[:, above] == 0).all()
+        if inp.C == 1 and inp.P == 0:
+            assert (Pm[:, 0, 0] == 1.0).all()
+        v = inp.v.astype(np.float64)
+        out = np.stack([Pm[h] @ v[:, h // 4, :] for h in range(W.HQ)], axis=1)
+        np.testing.assert_allclose(out, oracle.prefill(inp), rtol=1e-12, atol=1e-13)
