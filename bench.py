@@ -64,6 +64,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--path", default="attn_prefill",
                     choices=["attn_prefill", "attn_prefill_ffma", "attn_reference_prefill"])
+    ap.add_argument("--kv", choices=["fp32", "bf16"], default="fp32",
+                    help="bf16: the K/V cache in bf16 (attn_prefill_bf16kv)")
     ap.add_argument("--workload", choices=["serve", "long", "decode", "matrix"], default="serve",
                     help="decode: one decode step of 16 sequences x 16384 cached tokens (paged); "
                          "matrix: the three-kernel score-matrix pipeline at T = 512, 1024, 2048")
@@ -191,7 +193,7 @@ def load_peaks():
 
 def kernel_source_hash(path_name: str) -> str:
     """Hash of the kernel source a profile was taken on (traffic goes stale with it)."""
-    fname = {"attn_prefill": "tc.cu", "attn_prefill_ffma": "ffma.cu",
+    fname = {"attn_prefill": "tc.cu", "attn_prefill_bf16kv": "tc_bf16.cu", "attn_prefill_ffma": "ffma.cu",
              "attn_reference_prefill": "reference.cu"}[path_name]
     src = os.path.join(ROOT, "chunked_prefill_gqa_gb300", "csrc", fname)
     if not os.path.exists(src):
@@ -215,7 +217,13 @@ def profiled_traffic(path_name: str, workload: str):
 
 def roofline(path_name: str, kernel: str, flops: float, ms: float, peaks, workload: str):
     achieved = flops / (ms * 1e-3) / 1e12
-    if kernel.startswith("tcgen05-split-tf32"):
+    if kernel.startswith("tcgen05-bf16kv"):
+        peak = peaks["bf16_tflops"]
+        r = {"bound": "tensor", "peak_dtype": "bf16",
+             "peak_note": f"{peaks['source']} bf16 burst",
+             "tensor_passes": 2,
+             "frac_of_split_roof": None}
+    elif kernel.startswith("tcgen05-split-tf32"):
         peak = peaks["bf16_tflops"] * NOMINAL_TF32 / NOMINAL_BF16
         r = {"bound": "tensor", "peak_dtype": "tf32",
              "peak_note": f"{peaks['source']} bf16 burst x {NOMINAL_TF32}/{NOMINAL_BF16} (nominal tf32/bf16)",
@@ -230,7 +238,7 @@ def roofline(path_name: str, kernel: str, flops: float, ms: float, peaks, worklo
               "frac": round(achieved / peak, 4),
               "traffic": profiled_traffic(path_name, workload)})
     if "frac_of_split_roof" in r:
-        r["frac_of_split_roof"] = round(3 * achieved / peak, 4)
+        r["frac_of_split_roof"] = round(r["tensor_passes"] * achieved / peak, 4)
     return r
 
 
@@ -447,9 +455,17 @@ def main():
     out = torch.empty_like(q)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
+    if args.kv == "bf16":
+        if args.path != "attn_prefill" or args.paged:
+            raise SystemExit("--kv bf16 times attn_prefill_bf16kv on a contiguous cache only")
+        args.path = "attn_prefill_bf16kv"
+        kv = W.to_bf16(inp)
+        k = torch.from_numpy(kv.k.view(np.int16)).to(dev).view(torch.bfloat16)
+        v = torch.from_numpy(kv.v.view(np.int16)).to(dev).view(torch.bfloat16)
+        desc += "; K/V cache in bf16"
     fn = getattr(cp, args.path)
-    kernel = "tcgen05-split-tf32" if args.path == "attn_prefill" else (
-        "ffma" if args.path == "attn_prefill_ffma" else "reference")
+    kernel = {"attn_prefill": "tcgen05-split-tf32", "attn_prefill_bf16kv": "tcgen05-bf16kv",
+              "attn_prefill_ffma": "ffma"}.get(args.path, "reference")
 
     if args.paged:
         if args.path != "attn_prefill":
@@ -510,8 +526,12 @@ def main():
     e2e = None
     if not args.no_e2e and not args.paged:
         hq = torch.from_numpy(inp.q).pin_memory()
-        hk = torch.from_numpy(inp.k).pin_memory()
-        hv = torch.from_numpy(inp.v).pin_memory()
+        if args.kv == "bf16":
+            hk = torch.from_numpy(kv.k.view(np.int16)).view(torch.bfloat16).pin_memory()
+            hv = torch.from_numpy(kv.v.view(np.int16)).view(torch.bfloat16).pin_memory()
+        else:
+            hk = torch.from_numpy(inp.k).pin_memory()
+            hv = torch.from_numpy(inp.v).pin_memory()
         hout = torch.empty(out.shape, dtype=torch.float32).pin_memory()
         dq, dk, dv, dout = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(out)
 
@@ -545,12 +565,12 @@ def main():
         ok = np.array_equal(hout.numpy().view(np.uint32), out.cpu().numpy().view(np.uint32))
         e2e = {"value": world * flops / (e_ms * 1e-3) / 1e12, "unit": UNIT,
                "ms_per_step": e_ms, "steps": n_e2e,
-               "h2d_bytes_per_step": int(hq.numel() + hk.numel() + hv.numel()) * 4,
+               "h2d_bytes_per_step": int(hq.numel() * 4 + (hk.numel() + hv.numel()) * hk.element_size()),
                "d2h_bytes_per_step": int(hout.numel()) * 4,
                "matches_device_timed_output": bool(ok)}
 
     compare = None
-    if args.compare and rank == 0:
+    if args.compare and rank == 0 and args.kv == "fp32":
         compare = {}
         for other in ("attn_prefill_ffma", "attn_reference_prefill"):
             if other == args.path:
@@ -587,7 +607,7 @@ def main():
             "value": round(value, 4), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32", "data": "synthetic",
+            "dtype": "bf16" if args.kv == "bf16" else "f32", "data": "synthetic",
             "config": {"workload": desc, "C": C, "P": P, "hq": W.HQ, "hkv": W.HKV, "d": W.D,
                        "path": args.path, "kernel": kernel,
                        "flops_per_step": flops,

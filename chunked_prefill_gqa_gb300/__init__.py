@@ -38,7 +38,7 @@ MAX_TOKENS = 1 << 24
 PAGE = 16
 
 # Every symbol the header declares (the CPU tests check the library exports them).
-EXPORTS = ("attn_prefill", "attn_full_causal", "attn_prefill_paged", "attn_decode_paged",
+EXPORTS = ("attn_prefill", "attn_prefill_bf16kv", "attn_full_causal", "attn_prefill_paged", "attn_decode_paged",
            "attn_decode_workspace_bytes", "attn_decode_paged_noalloc",
            "attn_naive_workspace_bytes", "attn_naive_scores", "attn_naive_softmax", "attn_naive_weighted_sum",
            "attn_naive_prefill", "attn_prefill_ffma", "attn_reference_prefill", "attn_selftest_timeout", "attn_get_device_error", "attn_strerror", "attn_version")
@@ -73,6 +73,8 @@ def load():
                 fn = getattr(lib, name)
                 fn.restype = ci
                 fn.argtypes = [vp, vp, vp, vp, ci, ci, vp]
+            lib.attn_prefill_bf16kv.restype = ci
+            lib.attn_prefill_bf16kv.argtypes = [vp, vp, vp, vp, ci, ci, vp]
             lib.attn_prefill_paged.restype = ci
             lib.attn_prefill_paged.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, vp]
             lib.attn_decode_paged.restype = ci
@@ -155,6 +157,26 @@ def _call(name, q, k, v, out, P, stream):
 def attn_prefill(q, kCache, vCache, out, P: int, stream=None):
     """out <- causal GQA attention of chunk q at offset P (tensor-core path)."""
     return _call("attn_prefill", q, kCache, vCache, out, P, stream)
+
+
+def attn_prefill_bf16kv(q, kCache, vCache, out, P: int, stream=None):
+    """attn_prefill against a bf16 K/V cache: kCache, vCache are contiguous
+    torch.bfloat16 (or int16/uint16 bit patterns) CUDA tensors [P + C][8][64];
+    q and out fp32 [C][32][64]."""
+    import torch
+    C = q.shape[0]
+    for name, t, shape in (("q", q, (C, HQ, D)), ("out", out, (C, HQ, D))):
+        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous() or tuple(t.shape) != shape:
+            raise ValueError(f"{name} must be a contiguous float32 CUDA tensor of shape {shape}")
+    for name, t in (("kCache", kCache), ("vCache", vCache)):
+        if (t.dtype not in (torch.bfloat16, torch.int16, torch.uint16) or not t.is_cuda or not t.is_contiguous()
+                or tuple(t.shape) != (P + C, HKV, D)):
+            raise ValueError(f"{name} must be a contiguous bfloat16 CUDA tensor of shape ({P + C}, {HKV}, {D})")
+    rc = load().attn_prefill_bf16kv(_ptr(q), _ptr(kCache), _ptr(vCache), _ptr(out), C, int(P),
+                                    _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_prefill_bf16kv")
+    return out
 
 
 def attn_full_causal(q, k, v, out, stream=None):

@@ -103,6 +103,15 @@ extern "C" int attn_prefill(const float* q, const float* kCache, const float* vC
   return launch_tc(p, stream);
 }
 
+extern "C" int attn_prefill_bf16kv(const float* q, const uint16_t* kCache, const uint16_t* vCache, float* out,
+                                   int C, int P, cudaStream_t stream) {
+  Problem p{};
+  const int rc = prepare(q, reinterpret_cast<const float*>(kCache), reinterpret_cast<const float*>(vCache), out,
+                         C, P, &p);
+  if (rc != ATTN_OK || C == 0) return rc;
+  return launch_tc_bf16(p, stream);
+}
+
 extern "C" int attn_full_causal(const float* q, const float* k, const float* v, float* out, int T,
                                 cudaStream_t stream) {
   return attn_prefill(q, k, v, out, T, 0, stream);
@@ -288,5 +297,5 @@ extern "C" const char* attn_strerror(int code) {
 }
 
 extern "C" const char* attn_version(void) {
-  return "libattnprefill: tcgen05 split-TF32 prefill (contiguous and paged), split-KV GQA decode, FFMA, score-matrix and reference kernels, sm_103a";
+  return "libattnprefill: tcgen05 split-TF32 prefill (contiguous and paged), tcgen05 bf16-K/V prefill, split-KV GQA decode, FFMA, score-matrix and reference kernels, sm_103a";
 }

@@ -1,0 +1,544 @@
+// tc_bf16.cu -- flash prefill against a BF16 K/V cache on the sm_103a tensor
+// cores (tcgen05 kind::f16, TMEM accumulators, TMA staging).
+//
+// The operation is the one of tc.cu (causal GQA attention of a chunk at
+// positions P..P+C-1, scale 1/8, online softmax; "Inference Attention 2: Flash
+// Prefill Against a Cached Prefix", Lesson) with the cache held in bf16, the
+// production cache precision the pages name ("FlashAttention and inference
+// kernels", inference: a KV cache in BF16). The result is the exact attention
+// over the stored bf16 keys and values to fp32 accuracy:
+//   * K and V are bf16 already, so they are tensor-core operands as they land:
+//     K as a K-major operand, V as an MN-major operand ([key][d] rows), with no
+//     conversion or transpose pass.
+//   * Q (fp32) and P (fp32 probabilities) are split into two bf16 terms,
+//     hi = x with its 16 low bits cleared and lo = x - hi rounded to bf16, so
+//     hi + lo carries 16 significant bits (relative error <= 2^-17). Each
+//     product runs as two MMAs into one fp32 accumulator:
+//       S  = Q_hi K^T + Q_lo K^T          (4 + 4 MMAs of 128 x 128 x 16)
+//       O += P_hi V   + P_lo V            (8 + 8 MMAs of 128 x 64 x 16)
+// Q, P and the accumulators live in TMEM; P hi/lo overwrite the S columns they
+// came from, two bf16 per 32-bit column.
+//
+// Work unit (as in tc.cu): 32 chunk positions x the 4 query heads of one KV
+// head = 128 rows, one TMEM lane each. Keys come in tiles of 128; tiles past the
+// unit's last visible key are never loaded; only diagonal tiles are masked.
+//
+// Warp roles (12 warps):
+//   0-7  softmax: warp w owns TMEM lanes 32 (w % 4) .. + 31 and keys
+//        64 (w / 4) .. + 63 of every tile; the two warps of a row set exchange
+//        partial maxima and sums through shared memory. They split Q into TMEM,
+//        run the online softmax, write P hi/lo, rescale O when the reference
+//        maximum moves, and write the output.
+//   8    K producer, 9 V producer: one TMA load per 16 KB tile.
+//   10   QK issuer (allocates TMEM): QK(n) once K(n) landed and S buffer n % 3
+//        is free (PV(n-3) complete).
+//   11   PV issuer: PV(n) once P(n) is written and V(n) landed.
+// Three S buffers let QK run two tiles ahead of the softmax. Every wait is
+// bounded; on expiry the kernel records ATTN_ETIMEOUT, winds down and frees TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "tc_ptx.cuh"
+
+namespace attn {
+namespace {
+
+using namespace tc;
+
+constexpr int kBq = 32;           // chunk positions per unit
+constexpr int kM = kBq * kGroup;  // 128 rows = TMEM lanes
+constexpr int kBc = 128;          // keys per tile
+constexpr int kStages = 3;        // K and V rings
+constexpr int kNumS = 3;          // S / P buffers in TMEM
+
+constexpr int kSoftmaxWarps = 8;
+constexpr int kKProducerWarp = 8;
+constexpr int kVProducerWarp = 9;
+constexpr int kQkWarp = 10;
+constexpr int kPvWarp = 11;
+constexpr int kThreads = 32 * (kPvWarp + 1);
+
+// TMEM columns (32-bit each).
+constexpr uint32_t kColQhi = 0;   // 64 bf16 per row = 32 columns
+constexpr uint32_t kColQlo = 32;
+constexpr uint32_t kColS = 64;    // three 128-column S buffers; P hi | P lo (64 columns each) overwrite them
+constexpr uint32_t kColO = 448;   // 64 fp32 columns
+constexpr uint32_t kTmemCols = 512;
+
+// Shared memory (byte offsets from a 1024-aligned base). A tile is 128 keys x
+// 64 bf16 = 128 rows of 128 bytes in the 128-byte swizzle.
+constexpr uint32_t kTileBytes = kBc * kD * 2;  // 16 KB
+constexpr uint32_t kSmemK = 0;
+constexpr uint32_t kSmemV = kSmemK + kStages * kTileBytes;
+constexpr uint32_t kSmemBar = kSmemV + kStages * kTileBytes;
+constexpr uint32_t kNumBars = 7 * kStages + 1 + 2 + 4;
+constexpr uint32_t kSmemRed = kSmemBar + kNumBars * 8 + 16;  // [2 tile parities][2 key halves][128 rows]
+constexpr uint32_t kSmemLsum = kSmemRed + 2 * 2 * 128 * 4;   // [2 key halves][128 rows]
+constexpr uint32_t kSmemTotal = kSmemLsum + 2 * 128 * 4;
+constexpr uint32_t kSmemAlloc = kSmemTotal + 1024;
+
+static_assert(kSmemAlloc <= 232448, "exceeds the 227 KB per-block shared memory limit");
+static_assert(kM == 128 && kD == 64 && kBc == 128, "the MMA shapes below assume 128 x 128 x 64");
+static_assert(kColS + kNumS * 128 <= kColO && kColO + kD <= kTmemCols, "TMEM layout");
+
+constexpr uint32_t kIdescQK = idesc_bf16(128, 128, false);
+constexpr uint32_t kIdescPV = idesc_bf16(128, 64, true);
+constexpr float kStaleLog2 = 8.0f;  // see tc.cu: a stale reference maximum keeps p <= 2^8
+
+struct Params {
+  Problem p;
+  int n_units;
+  int n_qtiles;
+  unsigned long long timeout_ns;
+};
+
+struct Bars {
+  uint64_t* kfull;   // [kStages] TMA K landed
+  uint64_t* kempty;  // [kStages] QK done with the stage
+  uint64_t* vfull;   // [kStages] TMA V landed
+  uint64_t* vempty;  // [kStages] PV done with the stage
+  uint64_t* sfull;   // [kNumS] S written (MMA commit)
+  uint64_t* pfull;   // [kNumS] P written and O rescaled (softmax warps)
+  uint64_t* odone;   // [kNumS] PV(n) complete, barrier n % 3
+  uint64_t* qready;  // Q hi/lo in TMEM
+  uint64_t* drain;   // [2] MMA issuers' drain on abort
+  uint64_t* pair;    // [4] row-set exchanges of the softmax warps
+};
+
+__device__ __forceinline__ Bars carve_bars(uint8_t* base) {
+  uint64_t* b = reinterpret_cast<uint64_t*>(base + kSmemBar);
+  Bars r;
+  r.kfull = b; b += kStages;
+  r.kempty = b; b += kStages;
+  r.vfull = b; b += kStages;
+  r.vempty = b; b += kStages;
+  r.sfull = b; b += kNumS;
+  r.pfull = b; b += kNumS;
+  r.odone = b; b += kNumS;
+  r.qready = b++;
+  r.drain = b; b += 2;
+  r.pair = b; b += 4;
+  return r;
+}
+
+__device__ __forceinline__ int unit_index(int k, int cta, int grid) {
+  return k * grid + ((k & 1) ? (grid - 1 - cta) : cta);
+}
+
+struct Unit {
+  int t0, g, ntiles;
+};
+__device__ __forceinline__ Unit decode_unit(int u, const Params& prm) {
+  Unit w;
+  const int qt = prm.n_qtiles - 1 - u / kHKV;  // longest units first
+  w.g = u % kHKV;
+  w.t0 = qt * kBq;
+  const int nkeys = unit_keys(prm.p.P, prm.p.C, w.t0, kBq);
+  w.ntiles = (nkeys + kBc - 1) / kBc;
+  return w;
+}
+
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Params& prm,
+                                         volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > prm.timeout_ns) {
+      record_error(prm.p.err, kDevErrTimeout);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity, const Params& prm,
+                                              volatile int* abort_flag) {
+  const bool ok = wait_bar(bar, parity, prm, abort_flag);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// hi/lo bf16 split of 2n values into n packed words each.
+template <int N>
+__device__ __forceinline__ void split_pack(const float* x, uint32_t* hi, uint32_t* lo) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    const float a = x[2 * i], b = x[2 * i + 1];
+    hi[i] = pack_bf16_trunc(a, b);
+    lo[i] = pack_bf16_rn(a - bf16_trunc(a), b - bf16_trunc(b));
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+               const Params prm) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const Bars bars = carve_bars(smem);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kSmemBar + kNumBars * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSmemBar + kNumBars * 8 + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars.kfull[s], 1);
+      mbar_init(&bars.kempty[s], 1);
+      mbar_init(&bars.vfull[s], 1);
+      mbar_init(&bars.vempty[s], 1);
+    }
+    for (int b = 0; b < kNumS; ++b) {
+      mbar_init(&bars.sfull[b], 1);
+      mbar_init(&bars.pfull[b], kSoftmaxWarps);
+      mbar_init(&bars.odone[b], 1);
+    }
+    mbar_init(bars.qready, kSoftmaxWarps);
+    mbar_init(&bars.drain[0], 1);
+    mbar_init(&bars.drain[1], 1);
+    for (int q = 0; q < 4; ++q) mbar_init(&bars.pair[q], 2);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kQkWarp) {
+    tmem_alloc(tmem_holder, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kKProducerWarp && lane == 0) tma_prefetch_desc(&tmk);
+  if (warp == kVProducerWarp && lane == 0) tma_prefetch_desc(&tmv);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  const int cta = blockIdx.x, grid = gridDim.x;
+  const Problem& p = prm.p;
+
+  if (warp == kKProducerWarp || warp == kVProducerWarp) {
+    // ------------------------------------------------------------ producers
+    const bool is_k = warp == kKProducerWarp;
+    if (lane == 0) {
+      int n = 0;
+      for (int k = 0;; ++k) {
+        const int u = unit_index(k, cta, grid);
+        if (u >= prm.n_units) break;
+        const Unit w = decode_unit(u, prm);
+        for (int j = 0; j < w.ntiles; ++j, ++n) {
+          const int st = n % kStages;
+          uint64_t* freed = is_k ? &bars.kempty[st] : &bars.vempty[st];
+          if (n >= kStages && !wait_bar(freed, ((n / kStages) - 1) & 1, prm, abort_flag)) goto producer_done;
+          uint64_t* full = is_k ? &bars.kfull[st] : &bars.vfull[st];
+          uint8_t* dst = smem + (is_k ? kSmemK : kSmemV) + st * kTileBytes;
+          mbar_arrive_expect_tx(full, kTileBytes);
+          tma_load_2d(dst, is_k ? &tmk : &tmv, full, w.g * kD, j * kBc);
+        }
+      }
+    producer_done:
+      if (*abort_flag) {
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 200000ull) __nanosleep(1000);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kQkWarp || warp == kPvWarp) {
+    // ---------------------------------------------------------- MMA issuers
+    const bool is_qk = warp == kQkWarp;
+    if (lane == 0) {
+      int n = 0, lu = 0;
+      for (int k = 0;; ++k) {
+        const int u = unit_index(k, cta, grid);
+        if (u >= prm.n_units) break;
+        const Unit w = decode_unit(u, prm);
+        if (is_qk) {
+          if (!wait_bar(bars.qready, lu & 1, prm, abort_flag)) goto mma_done;
+          tc_fence_after();
+        }
+        for (int j = 0; j < w.ntiles; ++j, ++n) {
+          const int b = n % kNumS;
+          const int st = n % kStages;
+          if (is_qk) {
+            // S buffer b is free once PV(n-3) has read P(n-3) from it; odone[b]
+            // cannot be further ahead, since PV(n) needs S(n), issued below.
+            if (!wait_bar(&bars.kfull[st], (n / kStages) & 1, prm, abort_flag)) goto mma_done;
+            if (n >= kNumS && !wait_bar(&bars.odone[b], ((n / kNumS) - 1) & 1, prm, abort_flag)) goto mma_done;
+            tc_fence_after();
+            const uint32_t kb = smem_u32(smem + kSmemK + st * kTileBytes);
+            const uint32_t d = tmem + kColS + b * 128;
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+              mma_f16_ts(d, tmem + kColQhi + s * 8, sdesc_sw128(kb + s * 32), kIdescQK, s > 0);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+              mma_f16_ts(d, tmem + kColQlo + s * 8, sdesc_sw128(kb + s * 32), kIdescQK, 1);
+            mma_commit(&bars.sfull[b]);
+            mma_commit(&bars.kempty[st]);
+          } else {
+            if (!wait_bar(&bars.pfull[b], (n / kNumS) & 1, prm, abort_flag)) goto mma_done;
+            if (!wait_bar(&bars.vfull[st], (n / kStages) & 1, prm, abort_flag)) goto mma_done;
+            tc_fence_after();
+            const uint32_t vb = smem_u32(smem + kSmemV + st * kTileBytes);
+            const uint32_t phi = tmem + kColS + b * 128;
+            const bool first = j == 0;
+#pragma unroll
+            for (int s = 0; s < 8; ++s)  // 16 keys per step: 2048 bytes of V rows
+              mma_f16_ts(tmem + kColO, phi + s * 8, sdesc_sw128_mn(vb + s * 2048), kIdescPV,
+                         (first && s == 0) ? 0u : 1u);
+#pragma unroll
+            for (int s = 0; s < 8; ++s)
+              mma_f16_ts(tmem + kColO, phi + 64 + s * 8, sdesc_sw128_mn(vb + s * 2048), kIdescPV, 1);
+            mma_commit(&bars.odone[b]);
+            mma_commit(&bars.vempty[st]);
+          }
+        }
+        ++lu;
+      }
+    mma_done:
+      if (*abort_flag) {
+        uint64_t* drain = &bars.drain[is_qk ? 0 : 1];
+        mma_commit(drain);
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < prm.timeout_ns) {
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------------------------- softmax (warps 0-7)
+    const int rq = warp & 3;         // TMEM lanes 32 rq .. + 31
+    const int kh = warp >> 2;        // keys 64 kh .. + 63 of every tile; head dims 32 kh .. + 31
+    const int row = rq * 32 + lane;
+    const uint32_t lane_tmem = tmem + ((uint32_t)(rq * 32) << 16);
+    float* red = reinterpret_cast<float*>(smem + kSmemRed);
+    float* lred = reinterpret_cast<float*>(smem + kSmemLsum);
+    const float c = kLog2e * kScale;
+    const float stale = kStaleLog2 / c;
+    int n = 0;
+
+    uint32_t pc = 0;
+    auto pair_sync = [&]() -> bool {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.pair[rq]);
+      const bool ok = wait_bar_warp(&bars.pair[rq], pc & 1, prm, abort_flag);
+      ++pc;
+      return ok;
+    };
+
+    // This warp's 32 head dims of the row's query, split into bf16 hi/lo.
+    auto load_q = [&](const Unit& w) {
+      const int pos = w.t0 + (row >> 2);
+      const float* src = p.q + ((size_t)pos * kHQ + w.g * kGroup + (row & 3)) * kD + kh * 32;
+      float x[32];
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (pos < p.C) v = __ldg(reinterpret_cast<const float4*>(src + i));
+        x[i] = v.x;
+        x[i + 1] = v.y;
+        x[i + 2] = v.z;
+        x[i + 3] = v.w;
+      }
+      uint32_t hi[16], lo[16];
+      split_pack<16>(x, hi, lo);
+      tmem_st16(lane_tmem + kColQhi + kh * 16, hi);
+      tmem_st16(lane_tmem + kColQlo + kh * 16, lo);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars.qready);
+    };
+
+    bool q_loaded = false;
+    for (int k = 0;; ++k) {
+      const int u = unit_index(k, cta, grid);
+      if (u >= prm.n_units) break;
+      const Unit w = decode_unit(u, prm);
+      if (!q_loaded) load_q(w);
+      q_loaded = false;
+      float m_ref = -INFINITY, l = 0.f;
+      const int pos = w.t0 + (row >> 2);
+      const int limit = p.P + pos;
+      for (int j = 0; j < w.ntiles; ++j, ++n) {
+        const int b = n % kNumS;
+        const int j0 = j * kBc + kh * 64;
+        const uint32_t sbuf = lane_tmem + kColS + b * 128;
+        if (!wait_bar_warp(&bars.sfull[b], (n / kNumS) & 1, prm, abort_flag)) goto softmax_done;
+        tc_fence_after();
+        float s[64];
+        tmem_ld32(sbuf + kh * 64, *reinterpret_cast<float(*)[32]>(&s[0]));
+        tmem_ld32(sbuf + kh * 64 + 32, *reinterpret_cast<float(*)[32]>(&s[32]));
+        tmem_wait_ld();
+        if (j * kBc + kBc - 1 > p.P + w.t0) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            if (j0 + i > limit) s[i] = -INFINITY;
+        }
+        float mt = s[0];
+#pragma unroll
+        for (int i = 1; i < 64; ++i) mt = fmaxf(mt, s[i]);
+        {
+          // Both warps of the row set have read their S columns once they meet
+          // here, so P may overwrite any of the buffer's columns afterwards.
+          float* slot = red + (n & 1) * 256;
+          slot[kh * 128 + row] = mt;
+          if (!pair_sync()) goto softmax_done;
+          mt = fmaxf(mt, slot[(kh ^ 1) * 128 + row]);
+        }
+        float alpha = 1.f;
+        if (m_ref == -INFINITY || mt > m_ref + stale) {
+          const float m_new = fmaxf(m_ref, mt);
+          alpha = (m_ref == -INFINITY) ? 0.f : ex2((m_ref - m_new) * c);
+          m_ref = m_new;
+        }
+        const float mc = m_ref == -INFINITY ? 0.f : m_ref * c;
+        float lsum = 0.f;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          s[i] = ex2(fmaf(s[i], c, -mc));
+          lsum += s[i];
+        }
+        {
+          uint32_t hi[32], lo[32];
+          split_pack<32>(s, hi, lo);
+          tmem_st32(sbuf + kh * 32, *reinterpret_cast<float(*)[32]>(hi));
+          tmem_st32(sbuf + 64 + kh * 32, *reinterpret_cast<float(*)[32]>(lo));
+        }
+        l = fmaf(l, alpha, lsum);
+        tmem_wait_st();
+        // O is rescaled only when the reference maximum moved, after PV(n-1)
+        // completes (odone[(n-1) % 3] cannot be a phase further: PV(n+2) needs
+        // P(n+2) from these warps).
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          const int pb = (n - 1) % kNumS;
+          if (!wait_bar_warp(&bars.odone[pb], ((n - 1) / kNumS) & 1, prm, abort_flag)) goto softmax_done;
+          tc_fence_after();
+          float o[32];
+          tmem_ld32(lane_tmem + kColO + kh * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= alpha;
+          tmem_st32(lane_tmem + kColO + kh * 32, o);
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.pfull[b]);
+      }
+      {
+        const int u_next = unit_index(k + 1, cta, grid);
+        if (u_next < prm.n_units) {
+          load_q(decode_unit(u_next, prm));
+          q_loaded = true;
+        }
+      }
+      lred[kh * 128 + row] = l;
+      if (!pair_sync()) goto softmax_done;
+      l += lred[(kh ^ 1) * 128 + row];
+      {
+        const int pb = (n - 1) % kNumS;
+        if (!wait_bar_warp(&bars.odone[pb], ((n - 1) / kNumS) & 1, prm, abort_flag)) goto softmax_done;
+      }
+      tc_fence_after();
+      {
+        float a[32];
+        tmem_ld32(lane_tmem + kColO + kh * 32, a);
+        tmem_wait_ld();
+        if (pos < p.C) {
+          float* dst = p.out + ((size_t)pos * kHQ + w.g * kGroup + (row & 3)) * kD + kh * 32;
+          const float inv = 1.f / l;
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(dst + i) = make_float4(a[i] * inv, a[i + 1] * inv, a[i + 2] * inv,
+                                                              a[i + 3] * inv);
+        }
+      }
+      tc_fence_before();
+    }
+  softmax_done:;
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kQkWarp) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// k or v [rows][8][64] bf16 as a 2-D tensor (head * 64 + d, row); a box is one
+// head's 64 values (128 bytes, one swizzle row) x 128 rows.
+int encode_bf16_map(const void* base, int rows, CUtensorMap* map) {
+  auto enc = encoder();
+  if (!enc) return ATTN_ETMA;
+  const cuuint32_t ones[2] = {1, 1};
+  const cuuint64_t dims[2] = {(cuuint64_t)kHKV * kD, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)kHKV * kD * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kD, (cuuint32_t)kBc};
+  if (enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, ones,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return ATTN_ETMA;
+  return ATTN_OK;
+}
+
+struct DevState {
+  bool ready = false;
+  int num_sms = 0;
+};
+DevState g_state[64];
+
+}  // namespace
+
+int launch_tc_bf16(const Problem& p, cudaStream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ECUDA;
+  DevState& st = g_state[dev];
+  if (!st.ready) {
+    if (cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return ATTN_ECUDA;
+    if (cudaFuncSetAttribute(tc_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc) !=
+        cudaSuccess)
+      return ATTN_ECUDA;
+    st.ready = true;
+  }
+  alignas(64) CUtensorMap mk, mv;
+  int rc = encode_bf16_map(p.k, p.P + p.C, &mk);
+  if (rc == ATTN_OK) rc = encode_bf16_map(p.v, p.P + p.C, &mv);
+  if (rc != ATTN_OK) return rc;
+  Params prm;
+  prm.p = p;
+  prm.n_qtiles = (p.C + kBq - 1) / kBq;
+  prm.n_units = prm.n_qtiles * kHKV;
+  prm.timeout_ns = 2000000000ull;
+  const int grid = prm.n_units < st.num_sms ? prm.n_units : st.num_sms;
+  tc_bf16_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(mk, mv, prm);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ELAUNCH;
+}
+
+}  // namespace attn

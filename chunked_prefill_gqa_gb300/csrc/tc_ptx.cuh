@@ -131,6 +131,14 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&r)[32]) {
         "=r"(u[29]), "=r"(u[30]), "=r"(u[31])
       : "r"(taddr));
 }
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&u)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+      ::"r"(taddr), "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]), "r"(u[5]), "r"(u[6]), "r"(u[7]),
+        "r"(u[8]), "r"(u[9]), "r"(u[10]), "r"(u[11]), "r"(u[12]), "r"(u[13]), "r"(u[14]), "r"(u[15])
+      : "memory");
+}
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&r)[32]) {
   const uint32_t* u = reinterpret_cast<const uint32_t*>(r);
   asm volatile(
@@ -170,6 +178,40 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
   return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// Shared-memory descriptor of an MN-major 16-bit operand in the 128-byte
+// swizzled canonical layout: each 128-byte row holds 64 consecutive M/N
+// elements of one K index, 8 K rows form a 1024-byte swizzle atom, and atoms
+// follow each other along K every 1024 bytes (stride-dimension offset). The
+// leading-dimension offset (the next 64 M/N elements) is also set to 1024: an
+// operand of N = 64 spans a single atom along N and never uses it.
+__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((smem_addr & 0x3FFFF) >> 4);
+  d |= (uint64_t)(1024 >> 4) << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor for kind::f16 with bf16 A and B and fp32 accumulate;
+// A K-major, B K-major or (b_mn_major) MN-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[tmem] * B[smem], kind::f16 (A and B both bf16 here).
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T
 __device__ __forceinline__ void mma_tf32_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                             uint32_t accumulate) {
@@ -204,6 +246,20 @@ __host__ __device__ constexpr uint32_t sw128(uint32_t off) { return off ^ (((off
 // The high part of the split: fp32 with the 13 low mantissa bits cleared,
 // exactly representable in tf32. x - hi is exact in fp32.
 __device__ __forceinline__ float tf32_hi(float x) { return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u); }
+
+// Two fp32 values as one 32-bit word of two bf16, element `lo_elem` in bits
+// [0,16) and `hi_elem` in bits [16,32), each rounded to nearest even.
+__device__ __forceinline__ uint32_t pack_bf16_rn(float lo_elem, float hi_elem) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi_elem), "f"(lo_elem));
+  return r;
+}
+// The upper 16 bits of two fp32 values (bf16 by truncation), packed the same way.
+__device__ __forceinline__ uint32_t pack_bf16_trunc(float lo_elem, float hi_elem) {
+  return __byte_perm(__float_as_uint(lo_elem), __float_as_uint(hi_elem), 0x7632);
+}
+// x with its 16 low bits cleared: the value pack_bf16_trunc keeps.
+__device__ __forceinline__ float bf16_trunc(float x) { return __uint_as_float(__float_as_uint(x) & 0xFFFF0000u); }
 
 }  // namespace tc
 }  // namespace attn

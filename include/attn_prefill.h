@@ -42,6 +42,8 @@
 #ifndef ATTN_PREFILL_H
 #define ATTN_PREFILL_H
 
+#include <stddef.h>
+#include <stdint.h>
 #include <cuda_runtime_api.h>
 
 #ifdef __cplusplus
@@ -88,6 +90,22 @@ extern "C" {
  */
 int attn_prefill(const float *q, const float *kCache, const float *vCache, float *out,
                  int C, int P, cudaStream_t stream);
+
+/*
+ * attn_prefill_bf16kv -- attn_prefill with the K/V cache held in bf16, the
+ * production cache precision ("FlashAttention and inference kernels",
+ * inference: the KV cache in BF16). kCache and vCache are [P + C][8][64] bf16
+ * values given as their 16-bit patterns (uint16_t; sign, 8 exponent bits, 7
+ * fraction bits); q and out are fp32 as for attn_prefill. The result is the
+ * attention over the stored bf16 keys and values to the fp32 tolerance of
+ * attn_prefill: K and V enter the tcgen05 kind::f16 MMAs exactly as stored,
+ * while q and the probabilities are each split into two bf16 terms (16
+ * significant bits together) whose products are accumulated in fp32. Half the
+ * K/V bytes of attn_prefill and no conversion pass. Same sizes, alignment and
+ * errors as attn_prefill.
+ */
+int attn_prefill_bf16kv(const float *q, const uint16_t *kCache, const uint16_t *vCache, float *out,
+                        int C, int P, cudaStream_t stream);
 
 /*
  * attn_prefill_paged -- attn_prefill against a paged K/V cache ("FlashAttention

@@ -164,6 +164,20 @@ def probability_matrix(S) -> np.ndarray:
     return E / E.sum(axis=-1, keepdims=True)
 
 
+def bf16_to_float(bits) -> np.ndarray:
+    """bf16 bit patterns (uint16) as the fp32 values they encode: a bf16 is
+    the upper half of the IEEE binary32 with the same sign, exponent and leading
+    fraction bits, so the value is the binary32 whose low 16 bits are zero."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+def prefill_bf16kv(q, k_bits, v_bits, P: int, rows=None, threads: int = 0) -> np.ndarray:
+    """The oracle for a bf16 K/V cache: the exact attention (scale 1/8) over
+    the values the stored bf16 keys and values encode."""
+    return attention(q, bf16_to_float(k_bits), bf16_to_float(v_bits), P, 0.125, rows=rows, threads=threads)
+
+
 def violations(got, ref, atol: float = ATOL, rtol: float = RTOL) -> np.ndarray:
     """Boolean mask of elements failing |got - ref| <= atol + rtol * |ref| (NaN fails)."""
     got = np.asarray(got, dtype=np.float64)

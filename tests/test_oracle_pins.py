@@ -156,3 +156,31 @@ def test_probability_matrix_rows_and_pipeline_equal_the_oracle():
         v = inp.v.astype(np.float64)
         out = np.stack([Pm[h] @ v[:, h // 4, :] for h in range(W.HQ)], axis=1)
         np.testing.assert_allclose(out, oracle.prefill(inp), rtol=1e-12, atol=1e-13)
+
+
+def test_bf16_decoding_follows_the_format():
+    """bf16 = sign, 8 exponent bits (bias 127), 7 fraction bits: values fixed by
+    that definition, including a subnormal, the largest finite, infinity and -0."""
+    bits = np.array([0x3F80, 0xC000, 0x3F81, 0x4080, 0x0001, 0x7F7F, 0x7F80, 0x8000, 0x3EAB], dtype=np.uint16)
+    want = [1.0, -2.0, 1.0 + 2.0 ** -7, 4.0, 2.0 ** -133, (2.0 - 2.0 ** -7) * 2.0 ** 127, math.inf, -0.0,
+            (1.0 + 43.0 / 128.0) * 2.0 ** -2]
+    got = oracle.bf16_to_float(bits)
+    for g, w in zip(got.tolist(), want):
+        assert g == w and math.copysign(1.0, g) == math.copysign(1.0, w)
+
+
+def test_bf16_inputs_are_truncations_and_oracle_uses_their_values():
+    """The workload's bf16 bits keep the upper half of each fp32 value (the
+    difference is below 2^-7 relative and never rounds up), and the bf16 oracle
+    equals the fp32 oracle run on the decoded values."""
+    inp = W.edge(17, 31)
+    kv = W.to_bf16(inp)
+    kd = oracle.bf16_to_float(kv.k).astype(np.float64)
+    k = inp.k.astype(np.float64)
+    assert (np.abs(kd) <= np.abs(k)).all() and (np.abs(k - kd) <= 2.0 ** -7 * np.abs(k)).all()
+    ref = oracle.prefill_bf16kv(inp.q, kv.k, kv.v, inp.P)
+    np.testing.assert_array_equal(
+        ref, oracle.attention(inp.q, kd.astype(np.float32), oracle.bf16_to_float(kv.v), inp.P))
+    # planted 4.0 survives exactly, so planted rows still score 128
+    t = W.tiny()
+    assert (oracle.bf16_to_float(W.to_bf16(t).k)[t.k == 4.0] == 4.0).all()

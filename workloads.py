@@ -287,3 +287,21 @@ def decode_batch(ctx_lens, seed: int = 1, spare_pages: int = 3, planted=()) -> D
         k_pages[table[b, t // PAGE], t % PAGE] = k
         v_pages[table[b, t // PAGE], t % PAGE] = v
     return DecodeBatch(q=q, k_pages=k_pages, v_pages=v_pages, table=table, ctx=ctx)
+
+
+def bf16_bits(x: np.ndarray) -> np.ndarray:
+    """The bf16 bit patterns of fp32 values by truncation: the upper 16 bits of
+    each value (sign, exponent, 7 fraction bits). An encoding of the inputs,
+    not part of the method; both sides receive the same bits."""
+    return (np.ascontiguousarray(x, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+@dataclass
+class Bf16KV:
+    """A workload's K/V cache as bf16 bit patterns [P + C][8][64] (uint16)."""
+    k: np.ndarray
+    v: np.ndarray
+
+
+def to_bf16(inp: Inputs) -> Bf16KV:
+    return Bf16KV(k=bf16_bits(inp.k), v=bf16_bits(inp.v))
