@@ -63,7 +63,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--path", default="attn_prefill",
-                    choices=["attn_prefill", "attn_prefill_ffma", "attn_reference_prefill"])
+                    choices=["attn_prefill", "attn_prefill_bf16x3", "attn_prefill_ffma", "attn_reference_prefill"])
     ap.add_argument("--kv", choices=["fp32", "bf16"], default="fp32",
                     help="bf16: the K/V cache in bf16 (attn_prefill_bf16kv)")
     ap.add_argument("--workload", choices=["serve", "long", "decode", "matrix"], default="serve",
@@ -193,7 +193,7 @@ def load_peaks():
 
 def kernel_source_hash(path_name: str) -> str:
     """Hash of the kernel source a profile was taken on (traffic goes stale with it)."""
-    fname = {"attn_prefill": "tc.cu", "attn_prefill_bf16kv": "tc_bf16.cu", "attn_prefill_ffma": "ffma.cu",
+    fname = {"attn_prefill": "tc.cu", "attn_prefill_bf16kv": "tc_bf16.cu", "attn_prefill_bf16x3": "tc_bf16.cu", "attn_prefill_ffma": "ffma.cu",
              "attn_reference_prefill": "reference.cu"}[path_name]
     src = os.path.join(ROOT, "chunked_prefill_gqa_gb300", "csrc", fname)
     if not os.path.exists(src):
@@ -217,11 +217,11 @@ def profiled_traffic(path_name: str, workload: str):
 
 def roofline(path_name: str, kernel: str, flops: float, ms: float, peaks, workload: str):
     achieved = flops / (ms * 1e-3) / 1e12
-    if kernel.startswith("tcgen05-bf16kv"):
+    if kernel.startswith("tcgen05-bf16"):
         peak = peaks["bf16_tflops"]
         r = {"bound": "tensor", "peak_dtype": "bf16",
              "peak_note": f"{peaks['source']} bf16 burst",
-             "tensor_passes": 2,
+             "tensor_passes": 3 if kernel.startswith("tcgen05-bf16x3") else 2,
              "frac_of_split_roof": None}
     elif kernel.startswith("tcgen05-split-tf32"):
         peak = peaks["bf16_tflops"] * NOMINAL_TF32 / NOMINAL_BF16
@@ -465,6 +465,7 @@ def main():
         desc += "; K/V cache in bf16"
     fn = getattr(cp, args.path)
     kernel = {"attn_prefill": "tcgen05-split-tf32", "attn_prefill_bf16kv": "tcgen05-bf16kv",
+              "attn_prefill_bf16x3": "tcgen05-bf16x3",
               "attn_prefill_ffma": "ffma"}.get(args.path, "reference")
 
     if args.paged:

@@ -38,7 +38,7 @@ MAX_TOKENS = 1 << 24
 PAGE = 16
 
 # Every symbol the header declares (the CPU tests check the library exports them).
-EXPORTS = ("attn_prefill", "attn_prefill_bf16kv", "attn_full_causal", "attn_prefill_paged", "attn_decode_paged",
+EXPORTS = ("attn_prefill", "attn_prefill_bf16x3", "attn_prefill_bf16kv", "attn_full_causal", "attn_prefill_paged", "attn_decode_paged",
            "attn_decode_workspace_bytes", "attn_decode_paged_noalloc",
            "attn_naive_workspace_bytes", "attn_naive_scores", "attn_naive_softmax", "attn_naive_weighted_sum",
            "attn_naive_prefill", "attn_prefill_ffma", "attn_reference_prefill", "attn_selftest_timeout", "attn_get_device_error", "attn_strerror", "attn_version")
@@ -68,7 +68,7 @@ def load():
                     "(there is no fallback implementation)")
             lib = ctypes.CDLL(LIB_PATH)
             vp, ci = ctypes.c_void_p, ctypes.c_int
-            for name in ("attn_prefill", "attn_prefill_ffma", "attn_reference_prefill",
+            for name in ("attn_prefill", "attn_prefill_bf16x3", "attn_prefill_ffma", "attn_reference_prefill",
                          "attn_selftest_timeout"):
                 fn = getattr(lib, name)
                 fn.restype = ci
@@ -157,6 +157,11 @@ def _call(name, q, k, v, out, P, stream):
 def attn_prefill(q, kCache, vCache, out, P: int, stream=None):
     """out <- causal GQA attention of chunk q at offset P (tensor-core path)."""
     return _call("attn_prefill", q, kCache, vCache, out, P, stream)
+
+
+def attn_prefill_bf16x3(q, kCache, vCache, out, P: int, stream=None):
+    """attn_prefill on the bf16 tensor-core path (three of four split products)."""
+    return _call("attn_prefill_bf16x3", q, kCache, vCache, out, P, stream)
 
 
 def attn_prefill_bf16kv(q, kCache, vCache, out, P: int, stream=None):

@@ -103,6 +103,14 @@ extern "C" int attn_prefill(const float* q, const float* kCache, const float* vC
   return launch_tc(p, stream);
 }
 
+extern "C" int attn_prefill_bf16x3(const float* q, const float* kCache, const float* vCache, float* out, int C,
+                                   int P, cudaStream_t stream) {
+  Problem p{};
+  const int rc = prepare(q, kCache, vCache, out, C, P, &p);
+  if (rc != ATTN_OK || C == 0) return rc;
+  return launch_tc_bf16x3(p, stream);
+}
+
 extern "C" int attn_prefill_bf16kv(const float* q, const uint16_t* kCache, const uint16_t* vCache, float* out,
                                    int C, int P, cudaStream_t stream) {
   Problem p{};

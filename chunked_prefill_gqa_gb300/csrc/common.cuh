@@ -69,6 +69,8 @@ constexpr size_t kDecodeScratchBytes = size_t(4) << 20;
 cudaError_t decode_scratch(float** ptr);
 // BF16 K/V cache (tc_bf16.cu): p.k / p.v point at [P + C][8][64] bf16 caches.
 int launch_tc_bf16(const Problem& p, cudaStream_t stream);
+// fp32 K/V cache through the same kernel, K/V split into bf16 pairs in place.
+int launch_tc_bf16x3(const Problem& p, cudaStream_t stream);
 // Paged K/V: p.k / p.v point at [num_pages * 16][8][64] page pools.
 int launch_tc_paged(const Problem& p, const int* table, int num_pages, cudaStream_t stream);
 

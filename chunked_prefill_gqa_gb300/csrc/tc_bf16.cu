@@ -1,38 +1,44 @@
-// tc_bf16.cu -- flash prefill against a BF16 K/V cache on the sm_103a tensor
-// cores (tcgen05 kind::f16, TMEM accumulators, TMA staging).
+// tc_bf16.cu -- flash prefill on the sm_103a tensor cores with bf16 operands
+// (tcgen05 kind::f16, TMEM accumulators, TMA staging), for a K/V cache held in
+// bf16 or in fp32.
 //
 // The operation is the one of tc.cu (causal GQA attention of a chunk at
 // positions P..P+C-1, scale 1/8, online softmax; "Inference Attention 2: Flash
-// Prefill Against a Cached Prefix", Lesson) with the cache held in bf16, the
-// production cache precision the pages name ("FlashAttention and inference
-// kernels", inference: a KV cache in BF16). The result is the exact attention
-// over the stored bf16 keys and values to fp32 accuracy:
-//   * K and V are bf16 already, so they are tensor-core operands as they land:
-//     K as a K-major operand, V as an MN-major operand ([key][d] rows), with no
-//     conversion or transpose pass.
-//   * Q (fp32) and P (fp32 probabilities) are split into two bf16 terms,
-//     hi = x with its 16 low bits cleared and lo = x - hi rounded to bf16, so
-//     hi + lo carries 16 significant bits (relative error <= 2^-17). Each
-//     product runs as two MMAs into one fp32 accumulator:
-//       S  = Q_hi K^T + Q_lo K^T          (4 + 4 MMAs of 128 x 128 x 16)
-//       O += P_hi V   + P_lo V            (8 + 8 MMAs of 128 x 64 x 16)
-// Q, P and the accumulators live in TMEM; P hi/lo overwrite the S columns they
-// came from, two bf16 per 32-bit column.
+// Prefill Against a Cached Prefix", Lesson). Every fp32 operand x is carried as
+// two bf16 terms, x = x1 + x2 (16 significant bits together), and products
+// accumulate in fp32 on the tensor cores:
+//   bf16 cache ("FlashAttention and inference kernels", inference: the KV cache
+//   in BF16): K and V are operands exactly as stored, so
+//       S  = q1 K^T + q2 K^T                 (4 + 4 MMAs of 128 x 128 x 16)
+//       O += p1 V   + p2 V                   (8 + 8 MMAs of 128 x 64 x 16)
+//   fp32 cache: converter warps split each landed K/V tile in place into
+//   [x1 | x2], and each product keeps three of its four terms,
+//       S  = q1 k1^T + q1 k2^T + q2 k1^T     (3 x 4 MMAs)
+//       O += p1 v1   + p1 v2   + p2 v1       (3 x 8 MMAs)
+//   dropping only x2 y2, below 2^-15 of |x y| (hi rounded to nearest: |x2| <=
+//   2^-8 |x|; p1 truncated: |p2| < 2^-7 p); the kept terms carry the residual
+//   of each split, at most 2^-9 |x2|.
+// K is a K-major operand and V an MN-major one ([key][d] rows, 128-byte
+// swizzle), so V needs no transpose. q, P and the accumulators live in TMEM; P
+// (p1 | p2) overwrites the S columns it came from, two bf16 per 32-bit column.
 //
 // Work unit (as in tc.cu): 32 chunk positions x the 4 query heads of one KV
-// head = 128 rows, one TMEM lane each. Keys come in tiles of 128; tiles past the
-// unit's last visible key are never loaded; only diagonal tiles are masked.
+// head = 128 rows, one TMEM lane each. Keys come in tiles of 128; tiles past
+// the unit's last visible key are never loaded; only diagonal tiles are masked.
 //
-// Warp roles (12 warps):
-//   0-7  softmax: warp w owns TMEM lanes 32 (w % 4) .. + 31 and keys
-//        64 (w / 4) .. + 63 of every tile; the two warps of a row set exchange
-//        partial maxima and sums through shared memory. They split Q into TMEM,
-//        run the online softmax, write P hi/lo, rescale O when the reference
-//        maximum moves, and write the output.
-//   8    K producer, 9 V producer: one TMA load per 16 KB tile.
-//   10   QK issuer (allocates TMEM): QK(n) once K(n) landed and S buffer n % 3
-//        is free (PV(n-3) complete).
-//   11   PV issuer: PV(n) once P(n) is written and V(n) landed.
+// Warp roles:
+//   0-7   softmax: warp w owns TMEM lanes 32 (w % 4) .. + 31 and keys
+//         64 (w / 4) .. + 63 of every tile; the two warps of a row set exchange
+//         partial maxima and sums through shared memory. They split q into
+//         TMEM, run the online softmax, write p1/p2, rescale O when the
+//         reference maximum moves, and write the output.
+//   8     K producer, 9 V producer: TMA loads of whole tiles.
+//   10    QK issuer (allocates TMEM): QK(n) once K(n) is ready and S buffer
+//         n % 3 is free (PV(n-3) complete).
+//   11    PV issuer: PV(n) once P(n) is written and V(n) is ready.
+//   12-15 (fp32 cache) converters: 12-13 split K tiles, 14-15 V tiles, each
+//         warp 64 keys; a lane owns one key and rewrites, in place, exactly
+//         the two 128-byte rows it read.
 // Three S buffers let QK run two tiles ahead of the softmax. Every wait is
 // bounded; on expiry the kernel records ATTN_ETIMEOUT, winds down and frees TMEM.
 #include <cuda.h>
@@ -57,28 +63,39 @@ constexpr int kKProducerWarp = 8;
 constexpr int kVProducerWarp = 9;
 constexpr int kQkWarp = 10;
 constexpr int kPvWarp = 11;
-constexpr int kThreads = 32 * (kPvWarp + 1);
+constexpr int kFirstConvWarp = 12;  // fp32 cache only
+constexpr int kConvWarpsPerOperand = 2;
+template <bool kF32>
+constexpr int threads_of() {
+  return 32 * (kF32 ? kFirstConvWarp + 2 * kConvWarpsPerOperand : kPvWarp + 1);
+}
 
 // TMEM columns (32-bit each).
 constexpr uint32_t kColQhi = 0;   // 64 bf16 per row = 32 columns
 constexpr uint32_t kColQlo = 32;
-constexpr uint32_t kColS = 64;    // three 128-column S buffers; P hi | P lo (64 columns each) overwrite them
+constexpr uint32_t kColS = 64;    // three 128-column S buffers; p1 | p2 (64 columns each) overwrite them
 constexpr uint32_t kColO = 448;   // 64 fp32 columns
 constexpr uint32_t kTmemCols = 512;
 
-// Shared memory (byte offsets from a 1024-aligned base). A tile is 128 keys x
-// 64 bf16 = 128 rows of 128 bytes in the 128-byte swizzle.
-constexpr uint32_t kTileBytes = kBc * kD * 2;  // 16 KB
-constexpr uint32_t kSmemK = 0;
-constexpr uint32_t kSmemV = kSmemK + kStages * kTileBytes;
-constexpr uint32_t kSmemBar = kSmemV + kStages * kTileBytes;
-constexpr uint32_t kNumBars = 7 * kStages + 1 + 2 + 4;
-constexpr uint32_t kSmemRed = kSmemBar + kNumBars * 8 + 16;  // [2 tile parities][2 key halves][128 rows]
-constexpr uint32_t kSmemLsum = kSmemRed + 2 * 2 * 128 * 4;   // [2 key halves][128 rows]
-constexpr uint32_t kSmemTotal = kSmemLsum + 2 * 128 * 4;
-constexpr uint32_t kSmemAlloc = kSmemTotal + 1024;
+// Shared memory (byte offsets from a 1024-aligned base). A bf16 operand tile
+// is 128 keys x 64 values = 128 rows of 128 bytes in the 128-byte swizzle
+// (16 KB). With an fp32 cache a stage is 32 KB: TMA lands d 0-31 and d 32-63
+// as two such 16 KB regions, and the converters overwrite them with x1 and x2.
+constexpr uint32_t kOperandBytes = kBc * kD * 2;  // 16 KB
+template <bool kF32>
+struct Layout {
+  static constexpr uint32_t kStageBytes = kF32 ? 2 * kOperandBytes : kOperandBytes;
+  static constexpr uint32_t kSmemK = 0;
+  static constexpr uint32_t kSmemV = kSmemK + kStages * kStageBytes;
+  static constexpr uint32_t kSmemBar = kSmemV + kStages * kStageBytes;
+  static constexpr uint32_t kNumBars = 9 * kStages + 1 + 2 + 4;
+  static constexpr uint32_t kSmemRed = kSmemBar + kNumBars * 8 + 16;  // [2 tile parities][2 key halves][128 rows]
+  static constexpr uint32_t kSmemLsum = kSmemRed + 2 * 2 * 128 * 4;   // [2 key halves][128 rows]
+  static constexpr uint32_t kSmemTotal = kSmemLsum + 2 * 128 * 4;
+  static constexpr uint32_t kSmemAlloc = kSmemTotal + 1024;
+  static_assert(kSmemAlloc <= 232448, "exceeds the 227 KB per-block shared memory limit");
+};
 
-static_assert(kSmemAlloc <= 232448, "exceeds the 227 KB per-block shared memory limit");
 static_assert(kM == 128 && kD == 64 && kBc == 128, "the MMA shapes below assume 128 x 128 x 64");
 static_assert(kColS + kNumS * 128 <= kColO && kColO + kD <= kTmemCols, "TMEM layout");
 
@@ -95,6 +112,8 @@ struct Params {
 
 struct Bars {
   uint64_t* kfull;   // [kStages] TMA K landed
+  uint64_t* kconv;   // [kStages] K split into k1 | k2 (fp32 cache)
+  uint64_t* vconv;   // [kStages] V split into v1 | v2 (fp32 cache)
   uint64_t* kempty;  // [kStages] QK done with the stage
   uint64_t* vfull;   // [kStages] TMA V landed
   uint64_t* vempty;  // [kStages] PV done with the stage
@@ -106,10 +125,13 @@ struct Bars {
   uint64_t* pair;    // [4] row-set exchanges of the softmax warps
 };
 
+template <bool kF32>
 __device__ __forceinline__ Bars carve_bars(uint8_t* base) {
-  uint64_t* b = reinterpret_cast<uint64_t*>(base + kSmemBar);
+  uint64_t* b = reinterpret_cast<uint64_t*>(base + Layout<kF32>::kSmemBar);
   Bars r;
   r.kfull = b; b += kStages;
+  r.kconv = b; b += kStages;
+  r.vconv = b; b += kStages;
   r.kempty = b; b += kStages;
   r.vfull = b; b += kStages;
   r.vempty = b; b += kStages;
@@ -168,9 +190,10 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// hi/lo bf16 split of 2n values into n packed words each.
+// bf16 split of 2n values into n packed words each: x1 truncated (fast, for
+// the probabilities) or rounded to nearest (q, K, V), x2 = x - x1 rounded.
 template <int N>
-__device__ __forceinline__ void split_pack(const float* x, uint32_t* hi, uint32_t* lo) {
+__device__ __forceinline__ void split_pack_trunc(const float* x, uint32_t* hi, uint32_t* lo) {
 #pragma unroll
   for (int i = 0; i < N; ++i) {
     const float a = x[2 * i], b = x[2 * i + 1];
@@ -178,13 +201,26 @@ __device__ __forceinline__ void split_pack(const float* x, uint32_t* hi, uint32_
     lo[i] = pack_bf16_rn(a - bf16_trunc(a), b - bf16_trunc(b));
   }
 }
+template <int N>
+__device__ __forceinline__ void split_pack_rn(const float* x, uint32_t* hi, uint32_t* lo) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    float h0, h1;
+    hi[i] = pack_bf16_rn_keep(x[2 * i], x[2 * i + 1], h0, h1);
+    lo[i] = pack_bf16_rn(x[2 * i] - h0, x[2 * i + 1] - h1);
+  }
+}
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool kF32>
+__global__ void __launch_bounds__(threads_of<kF32>(), 1)
 tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                const Params prm) {
+  using L = Layout<kF32>;
+  constexpr uint32_t kSmemK = L::kSmemK, kSmemV = L::kSmemV, kSmemBar = L::kSmemBar, kNumBars = L::kNumBars;
+  constexpr uint32_t kSmemRed = L::kSmemRed, kSmemLsum = L::kSmemLsum, kStageBytes = L::kStageBytes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  const Bars bars = carve_bars(smem);
+  const Bars bars = carve_bars<kF32>(smem);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kSmemBar + kNumBars * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSmemBar + kNumBars * 8 + 4);
 
@@ -194,6 +230,8 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars.kfull[s], 1);
+      mbar_init(&bars.kconv[s], kConvWarpsPerOperand);
+      mbar_init(&bars.vconv[s], kConvWarpsPerOperand);
       mbar_init(&bars.kempty[s], 1);
       mbar_init(&bars.vfull[s], 1);
       mbar_init(&bars.vempty[s], 1);
@@ -238,9 +276,14 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
           uint64_t* freed = is_k ? &bars.kempty[st] : &bars.vempty[st];
           if (n >= kStages && !wait_bar(freed, ((n / kStages) - 1) & 1, prm, abort_flag)) goto producer_done;
           uint64_t* full = is_k ? &bars.kfull[st] : &bars.vfull[st];
-          uint8_t* dst = smem + (is_k ? kSmemK : kSmemV) + st * kTileBytes;
-          mbar_arrive_expect_tx(full, kTileBytes);
-          tma_load_2d(dst, is_k ? &tmk : &tmv, full, w.g * kD, j * kBc);
+          uint8_t* dst = smem + (is_k ? kSmemK : kSmemV) + st * kStageBytes;
+          mbar_arrive_expect_tx(full, kStageBytes);
+          if (kF32) {  // d 0-31 and d 32-63 of the head, 128 rows each
+            tma_load_2d(dst, is_k ? &tmk : &tmv, full, w.g * kD, j * kBc);
+            tma_load_2d(dst + kOperandBytes, is_k ? &tmk : &tmv, full, w.g * kD + 32, j * kBc);
+          } else {
+            tma_load_2d(dst, is_k ? &tmk : &tmv, full, w.g * kD, j * kBc);
+          }
         }
       }
     producer_done:
@@ -269,14 +312,20 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
           if (is_qk) {
             // S buffer b is free once PV(n-3) has read P(n-3) from it; odone[b]
             // cannot be further ahead, since PV(n) needs S(n), issued below.
-            if (!wait_bar(&bars.kfull[st], (n / kStages) & 1, prm, abort_flag)) goto mma_done;
+            if (!wait_bar(kF32 ? &bars.kconv[st] : &bars.kfull[st], (n / kStages) & 1, prm, abort_flag))
+              goto mma_done;
             if (n >= kNumS && !wait_bar(&bars.odone[b], ((n / kNumS) - 1) & 1, prm, abort_flag)) goto mma_done;
             tc_fence_after();
-            const uint32_t kb = smem_u32(smem + kSmemK + st * kTileBytes);
+            const uint32_t kb = smem_u32(smem + kSmemK + st * kStageBytes);
             const uint32_t d = tmem + kColS + b * 128;
 #pragma unroll
             for (int s = 0; s < 4; ++s)
               mma_f16_ts(d, tmem + kColQhi + s * 8, sdesc_sw128(kb + s * 32), kIdescQK, s > 0);
+            if (kF32) {
+#pragma unroll
+              for (int s = 0; s < 4; ++s)
+                mma_f16_ts(d, tmem + kColQhi + s * 8, sdesc_sw128(kb + kOperandBytes + s * 32), kIdescQK, 1);
+            }
 #pragma unroll
             for (int s = 0; s < 4; ++s)
               mma_f16_ts(d, tmem + kColQlo + s * 8, sdesc_sw128(kb + s * 32), kIdescQK, 1);
@@ -284,15 +333,21 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
             mma_commit(&bars.kempty[st]);
           } else {
             if (!wait_bar(&bars.pfull[b], (n / kNumS) & 1, prm, abort_flag)) goto mma_done;
-            if (!wait_bar(&bars.vfull[st], (n / kStages) & 1, prm, abort_flag)) goto mma_done;
+            if (!wait_bar(kF32 ? &bars.vconv[st] : &bars.vfull[st], (n / kStages) & 1, prm, abort_flag))
+              goto mma_done;
             tc_fence_after();
-            const uint32_t vb = smem_u32(smem + kSmemV + st * kTileBytes);
+            const uint32_t vb = smem_u32(smem + kSmemV + st * kStageBytes);
             const uint32_t phi = tmem + kColS + b * 128;
             const bool first = j == 0;
 #pragma unroll
             for (int s = 0; s < 8; ++s)  // 16 keys per step: 2048 bytes of V rows
               mma_f16_ts(tmem + kColO, phi + s * 8, sdesc_sw128_mn(vb + s * 2048), kIdescPV,
                          (first && s == 0) ? 0u : 1u);
+            if (kF32) {
+#pragma unroll
+              for (int s = 0; s < 8; ++s)
+                mma_f16_ts(tmem + kColO, phi + s * 8, sdesc_sw128_mn(vb + kOperandBytes + s * 2048), kIdescPV, 1);
+            }
 #pragma unroll
             for (int s = 0; s < 8; ++s)
               mma_f16_ts(tmem + kColO, phi + 64 + s * 8, sdesc_sw128_mn(vb + s * 2048), kIdescPV, 1);
@@ -312,6 +367,58 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
       }
     }
     __syncwarp();
+  } else if (warp >= kFirstConvWarp) {
+    // ---------------------------------------------- converters (fp32 cache)
+    // Lane = one key. Its fp32 row lies in two 128-byte rows (d 0-31 in the
+    // first region, d 32-63 in the second); x1 of the key goes to the same row
+    // of the first region and x2 to the same row of the second, so each lane
+    // rewrites exactly the bytes it read. 16-byte accesses of a quarter-warp hit
+    // 8 consecutive rows at one logical chunk: 8 distinct bank groups under the
+    // swizzle.
+    if (kF32) {
+      const bool is_k = warp < kFirstConvWarp + kConvWarpsPerOperand;
+      const int cw = (warp - kFirstConvWarp) % kConvWarpsPerOperand;
+      int n = 0;
+      for (int k = 0;; ++k) {
+        const int u = unit_index(k, cta, grid);
+        if (u >= prm.n_units) break;
+        const Unit w = decode_unit(u, prm);
+        for (int j = 0; j < w.ntiles; ++j, ++n) {
+          const int st = n % kStages;
+          if (!wait_bar_warp(is_k ? &bars.kfull[st] : &bars.vfull[st], (n / kStages) & 1, prm, abort_flag))
+            goto conv_done;
+          uint8_t* base = smem + (is_k ? kSmemK : kSmemV) + st * kStageBytes;
+#pragma unroll 1
+          for (int r = 0; r < 2; ++r) {
+            const uint32_t key = (uint32_t)(64 * cw + 32 * r + lane);
+            float x[64];
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int c4 = 0; c4 < 8; ++c4) {
+                const float4 v = *reinterpret_cast<const float4*>(base + h * kOperandBytes +
+                                                                  sw128(key * 128u + c4 * 16u));
+                x[h * 32 + c4 * 4 + 0] = v.x;
+                x[h * 32 + c4 * 4 + 1] = v.y;
+                x[h * 32 + c4 * 4 + 2] = v.z;
+                x[h * 32 + c4 * 4 + 3] = v.w;
+              }
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+              uint32_t hi[4], lo[4];
+              split_pack_rn<4>(x + c8 * 8, hi, lo);
+              const uint32_t off = sw128(key * 128u + c8 * 16u);
+              *reinterpret_cast<uint4*>(base + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+              *reinterpret_cast<uint4*>(base + kOperandBytes + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(is_k ? &bars.kconv[st] : &bars.vconv[st]);
+        }
+      }
+    }
+  conv_done:;
   } else {
     // -------------------------------------------------- softmax (warps 0-7)
     const int rq = warp & 3;         // TMEM lanes 32 rq .. + 31
@@ -348,7 +455,7 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
         x[i + 3] = v.w;
       }
       uint32_t hi[16], lo[16];
-      split_pack<16>(x, hi, lo);
+      split_pack_rn<16>(x, hi, lo);
       tmem_st16(lane_tmem + kColQhi + kh * 16, hi);
       tmem_st16(lane_tmem + kColQlo + kh * 16, lo);
       tmem_wait_st();
@@ -402,15 +509,16 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
         const float mc = m_ref == -INFINITY ? 0.f : m_ref * c;
         float lsum = 0.f;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          s[i] = ex2(fmaf(s[i], c, -mc));
-          lsum += s[i];
-        }
-        {
-          uint32_t hi[32], lo[32];
-          split_pack<32>(s, hi, lo);
-          tmem_st32(sbuf + kh * 32, *reinterpret_cast<float(*)[32]>(hi));
-          tmem_st32(sbuf + 64 + kh * 32, *reinterpret_cast<float(*)[32]>(lo));
+        for (int half = 0; half < 2; ++half) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            s[half * 32 + i] = ex2(fmaf(s[half * 32 + i], c, -mc));
+            lsum += s[half * 32 + i];
+          }
+          uint32_t hi[16], lo[16];
+          split_pack_trunc<16>(s + half * 32, hi, lo);
+          tmem_st16(sbuf + kh * 32 + half * 16, hi);
+          tmem_st16(sbuf + 64 + kh * 32 + half * 16, lo);
         }
         l = fmaf(l, alpha, lsum);
         tmem_wait_st();
@@ -491,45 +599,44 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return fn;
 }
 
-// k or v [rows][8][64] bf16 as a 2-D tensor (head * 64 + d, row); a box is one
-// head's 64 values (128 bytes, one swizzle row) x 128 rows.
-int encode_bf16_map(const void* base, int rows, CUtensorMap* map) {
+// k or v [rows][8][64] as a 2-D tensor (head * 64 + d, row); a box is 128
+// bytes of one head's values (64 bf16, or 32 fp32: one swizzle row) x 128 rows.
+int encode_kv_tile_map(const void* base, int rows, bool f32, CUtensorMap* map) {
   auto enc = encoder();
   if (!enc) return ATTN_ETMA;
   const cuuint32_t ones[2] = {1, 1};
   const cuuint64_t dims[2] = {(cuuint64_t)kHKV * kD, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)kHKV * kD * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)kD, (cuuint32_t)kBc};
-  if (enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, ones,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+  const cuuint64_t strides[1] = {(cuuint64_t)kHKV * kD * (f32 ? 4 : 2)};
+  const cuuint32_t box[2] = {(cuuint32_t)(f32 ? 32 : 64), (cuuint32_t)kBc};
+  if (enc(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+          dims, strides, box, ones, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return ATTN_ETMA;
   return ATTN_OK;
 }
 
 struct DevState {
-  bool ready = false;
+  bool ready[2] = {false, false};
   int num_sms = 0;
 };
 DevState g_state[64];
 
-}  // namespace
-
-int launch_tc_bf16(const Problem& p, cudaStream_t stream) {
+template <bool kF32>
+int launch_impl(const Problem& p, cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ECUDA;
   DevState& st = g_state[dev];
-  if (!st.ready) {
+  if (!st.ready[kF32]) {
     if (cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return ATTN_ECUDA;
-    if (cudaFuncSetAttribute(tc_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(tc_bf16_kernel<kF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)Layout<kF32>::kSmemAlloc) != cudaSuccess)
       return ATTN_ECUDA;
-    st.ready = true;
+    st.ready[kF32] = true;
   }
   alignas(64) CUtensorMap mk, mv;
-  int rc = encode_bf16_map(p.k, p.P + p.C, &mk);
-  if (rc == ATTN_OK) rc = encode_bf16_map(p.v, p.P + p.C, &mv);
+  int rc = encode_kv_tile_map(p.k, p.P + p.C, kF32, &mk);
+  if (rc == ATTN_OK) rc = encode_kv_tile_map(p.v, p.P + p.C, kF32, &mv);
   if (rc != ATTN_OK) return rc;
   Params prm;
   prm.p = p;
@@ -537,8 +644,14 @@ int launch_tc_bf16(const Problem& p, cudaStream_t stream) {
   prm.n_units = prm.n_qtiles * kHKV;
   prm.timeout_ns = 2000000000ull;
   const int grid = prm.n_units < st.num_sms ? prm.n_units : st.num_sms;
-  tc_bf16_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(mk, mv, prm);
+  tc_bf16_kernel<kF32><<<grid, threads_of<kF32>(), Layout<kF32>::kSmemAlloc, stream>>>(mk, mv, prm);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ELAUNCH;
 }
+
+}  // namespace
+
+int launch_tc_bf16(const Problem& p, cudaStream_t stream) { return launch_impl<false>(p, stream); }
+
+int launch_tc_bf16x3(const Problem& p, cudaStream_t stream) { return launch_impl<true>(p, stream); }
 
 }  // namespace attn

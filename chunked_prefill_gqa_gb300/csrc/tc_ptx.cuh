@@ -254,6 +254,14 @@ __device__ __forceinline__ uint32_t pack_bf16_rn(float lo_elem, float hi_elem) {
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi_elem), "f"(lo_elem));
   return r;
 }
+// Round-to-nearest-even bf16 split of two fp32 values: hi (packed) and the
+// fp32 value of each half, so that x - hi is exact in fp32.
+__device__ __forceinline__ uint32_t pack_bf16_rn_keep(float e0, float e1, float& h0, float& h1) {
+  const uint32_t r = pack_bf16_rn(e0, e1);
+  h0 = __uint_as_float(r << 16);
+  h1 = __uint_as_float(r & 0xFFFF0000u);
+  return r;
+}
 // The upper 16 bits of two fp32 values (bf16 by truncation), packed the same way.
 __device__ __forceinline__ uint32_t pack_bf16_trunc(float lo_elem, float hi_elem) {
   return __byte_perm(__float_as_uint(lo_elem), __float_as_uint(hi_elem), 0x7632);

@@ -92,6 +92,17 @@ int attn_prefill(const float *q, const float *kCache, const float *vCache, float
                  int C, int P, cudaStream_t stream);
 
 /*
+ * attn_prefill_bf16x3 -- attn_prefill (fp32 cache, same arguments, layouts and
+ * errors) on the bf16 tensor-core path: each fp32 operand is carried as two
+ * bf16 terms x = x1 + x2 (x1 rounded to nearest, x2 the rounded remainder) and
+ * each product keeps x1 y1 + x1 y2 + x2 y1 in fp32, dropping x2 y2 (below
+ * 2^-15 of |x y|). The K/V split runs in shared memory, in place, on each tile
+ * as it lands; V needs no transpose.
+ */
+int attn_prefill_bf16x3(const float *q, const float *kCache, const float *vCache, float *out,
+                        int C, int P, cudaStream_t stream);
+
+/*
  * attn_prefill_bf16kv -- attn_prefill with the K/V cache held in bf16, the
  * production cache precision ("FlashAttention and inference kernels",
  * inference: the KV cache in BF16). kCache and vCache are [P + C][8][64] bf16
