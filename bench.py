@@ -193,7 +193,9 @@ def load_peaks():
 
 def kernel_source_hash(path_name: str) -> str:
     """Hash of the kernel source a profile was taken on (traffic goes stale with it)."""
-    fname = {"attn_prefill": "tc.cu", "attn_prefill_bf16kv": "tc_bf16.cu", "attn_prefill_bf16x3": "tc_bf16.cu", "attn_prefill_ffma": "ffma.cu",
+    fname = {"attn_prefill": "tc.cu", "attn_prefill_bf16kv": "tc_bf16.cu", "attn_prefill_bf16x3": "tc_bf16.cu",
+             "attn_decode_paged": "decode.cu", "attn_naive_scores": "naive.cu", "attn_naive_softmax": "naive.cu",
+             "attn_naive_weighted_sum": "naive.cu", "attn_prefill_ffma": "ffma.cu",
              "attn_reference_prefill": "reference.cu"}[path_name]
     src = os.path.join(ROOT, "chunked_prefill_gqa_gb300", "csrc", fname)
     if not os.path.exists(src):
@@ -327,8 +329,10 @@ def run_decode(args):
             "config": {"workload": "decode step, 16 x 16384 tokens, shuffled 16-token pages",
                        "kv_bytes_per_step": kv_bytes, "tflops": round(flops / (ms * 1e-3) / 1e12, 3),
                        "l2": "K/V (1 GiB) larger than L2"},
-            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": None},
+            "roofline": {"bound": "hbm", "kernel": "decode_split_kernel + decode_merge_kernel",
+                         "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / peaks["hbm_gbs"], 4),
+                         "traffic": profiled_traffic("attn_decode_paged", "decode")},
             "gpu_launches": 2 * args.steps}
     print(json.dumps(line))
     return 0
@@ -400,7 +404,7 @@ def run_matrix(args):
         rl = {"bound": "alu", "kernel": f"naive_{dom}_kernel", "achieved": a, "peak": round(ffma_peak, 2),
               "unit": "TFLOP/s", "frac": round(a / ffma_peak, 4),
               "peak_note": f"152 SMs x 128 FFMA/clk x 2 flop x {peaks['sm_max_mhz']:.0f} MHz"}
-    rl["traffic"] = None
+    rl["traffic"] = profiled_traffic("attn_naive_" + dom, "matrix")
     line = {"metric": "score-matrix pipeline attention time, full prompt T=2048 (32q/8kv, d=64)",
             "value": last["pipeline_ms"], "unit": "ms", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": last["pipeline_ms"], "higher_is_better": False, "scaling": "weak",
