@@ -561,16 +561,17 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
           tmem_ld32(sbuf + 64, t);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) s[i] += t[i];
+          for (int i = 0; i < 32; i += 2) add2(s[i], s[i + 1], s[i], s[i + 1], t[i], t[i + 1]);
         }
         if (j * kBc + kBc - 1 > p.P + w.t0) {
 #pragma unroll
           for (int i = 0; i < 32; ++i)
             if (j0 + i > limit) s[i] = -INFINITY;
         }
-        float mt = s[0];
+        float mt = max3(s[0], s[1], s[2]);
 #pragma unroll
-        for (int i = 1; i < 32; ++i) mt = fmaxf(mt, s[i]);
+        for (int i = 3; i < 31; i += 2) mt = max3(mt, s[i], s[i + 1]);
+        mt = fmaxf(mt, s[31]);
         {
           float* slot = red + (n & 1) * 256;
           slot[kh * 128 + row] = mt;
@@ -587,13 +588,18 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
         float lsum = 0.f;
         {
           float hi[32], lo[32];
+          float l0 = 0.f, l1 = 0.f;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float pj = ex2(fmaf(s[i], c, -mc));
-            lsum += pj;
-            hi[i] = tf32_hi(pj);
-            lo[i] = pj - hi[i];
+          for (int i = 0; i < 32; i += 2) {
+            float a0, a1;
+            fma2(a0, a1, s[i], s[i + 1], c, c, -mc, -mc);
+            const float p0 = ex2(a0), p1 = ex2(a1);
+            add2(l0, l1, l0, l1, p0, p1);
+            hi[i] = tf32_hi(p0);
+            hi[i + 1] = tf32_hi(p1);
+            fma2(lo[i], lo[i + 1], hi[i], hi[i + 1], -1.f, -1.f, p0, p1);  // p - hi, exact
           }
+          lsum = l0 + l1;
           tmem_st32(sbuf, hi);
           tmem_st32(sbuf + 64, lo);
         }

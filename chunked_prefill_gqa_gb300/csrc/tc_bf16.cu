@@ -198,7 +198,9 @@ __device__ __forceinline__ void split_pack_trunc(const float* x, uint32_t* hi, u
   for (int i = 0; i < N; ++i) {
     const float a = x[2 * i], b = x[2 * i + 1];
     hi[i] = pack_bf16_trunc(a, b);
-    lo[i] = pack_bf16_rn(a - bf16_trunc(a), b - bf16_trunc(b));
+    float ra, rb;
+    fma2(ra, rb, bf16_trunc(a), bf16_trunc(b), -1.f, -1.f, a, b);  // x - x1, exact
+    lo[i] = pack_bf16_rn(ra, rb);
   }
 }
 template <int N>
@@ -489,9 +491,10 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
           for (int i = 0; i < 64; ++i)
             if (j0 + i > limit) s[i] = -INFINITY;
         }
-        float mt = s[0];
+        float mt = max3(s[0], s[1], s[2]);
 #pragma unroll
-        for (int i = 1; i < 64; ++i) mt = fmaxf(mt, s[i]);
+        for (int i = 3; i < 63; i += 2) mt = max3(mt, s[i], s[i + 1]);
+        mt = fmaxf(mt, s[63]);
         {
           // Both warps of the row set have read their S columns once they meet
           // here, so P may overwrite any of the buffer's columns afterwards.
@@ -507,20 +510,23 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
           m_ref = m_new;
         }
         const float mc = m_ref == -INFINITY ? 0.f : m_ref * c;
-        float lsum = 0.f;
+        float l0 = 0.f, l1 = 0.f;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            s[half * 32 + i] = ex2(fmaf(s[half * 32 + i], c, -mc));
-            lsum += s[half * 32 + i];
+          for (int i = 0; i < 32; i += 2) {
+            float* x = s + half * 32 + i;
+            fma2(x[0], x[1], x[0], x[1], c, c, -mc, -mc);
+            x[0] = ex2(x[0]);
+            x[1] = ex2(x[1]);
+            add2(l0, l1, l0, l1, x[0], x[1]);
           }
           uint32_t hi[16], lo[16];
           split_pack_trunc<16>(s + half * 32, hi, lo);
           tmem_st16(sbuf + kh * 32 + half * 16, hi);
           tmem_st16(sbuf + 64 + kh * 32 + half * 16, lo);
         }
-        l = fmaf(l, alpha, lsum);
+        l = fmaf(l, alpha, l0 + l1);
         tmem_wait_st();
         // O is rescaled only when the reference maximum moved, after PV(n-1)
         // completes (odone[(n-1) % 3] cannot be a phase further: PV(n+2) needs
