@@ -245,6 +245,28 @@ def roofline(path_name: str, kernel: str, flops: float, ms: float, peaks, worklo
 
 
 # ----------------------------------------------------------------------------
+# Replicas: one process per GPU, each timing its own copy of the workload
+# ----------------------------------------------------------------------------
+
+def max_over_ranks(x: float, device) -> float:
+    """The largest of every rank's x (the slowest replica's timed region), or
+    x itself outside torch.distributed."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(world: int, flops_per_step: float, slowest_ms_total: float, steps: int) -> float:
+    """Whole-job TFLOP/s: every rank processed `flops_per_step` per step, and
+    the job took as long as the slowest rank's timed region."""
+    return world * flops_per_step / (slowest_ms_total / steps * 1e-3) / 1e12
+
+
+# ----------------------------------------------------------------------------
 # The reference arm: the oracle on the host cores
 # ----------------------------------------------------------------------------
 
@@ -518,13 +540,9 @@ def main():
         raise RuntimeError(f"device error in the timed region: {cp.strerror(err)}")
     launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms_mean = sum(launch_ms) / len(launch_ms)
-    kernel_ms_total = sum(launch_ms)
-    if world > 1:
-        t = torch.tensor([kernel_ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        kernel_ms_total = float(t.item())
+    kernel_ms_total = max_over_ranks(sum(launch_ms), dev)
     ms_per_step = kernel_ms_total / args.steps
-    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    value = replica_throughput(world, flops, kernel_ms_total, args.steps)
 
     # End to end through the same entry point: pinned host inputs copied in,
     # the result copied out, every step inside the timed region.
@@ -561,12 +579,7 @@ def main():
             e2e_step()
             ee[i].record(stream)
         torch.cuda.synchronize()
-        e_ms = sum(a.elapsed_time(b) for a, b in zip(es, ee))
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e_ms /= n_e2e
+        e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in zip(es, ee)), dev) / n_e2e
         ok = np.array_equal(hout.numpy().view(np.uint32), out.cpu().numpy().view(np.uint32))
         e2e = {"value": world * flops / (e_ms * 1e-3) / 1e12, "unit": UNIT,
                "ms_per_step": e_ms, "steps": n_e2e,
