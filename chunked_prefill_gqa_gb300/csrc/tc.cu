@@ -24,23 +24,23 @@
 //   S  = S'[:, :64] + S'[:, 64:]            (summed by the softmax warps)
 //   O' += P_hi [V_hi^T; V_lo^T]^T (N = 128) then O'[:, :64] += P_lo V_hi^T
 //   O  = O'[:, :64] + O'[:, 64:]            (summed in the epilogue)
-// Q and P are TMEM operands (P hi and P lo overwrite the S columns they came
-// from); K and V^T are 128-byte-swizzled K-major shared-memory operands.
+// Q hi/lo and K, V^T are 128-byte-swizzled K-major shared-memory operands; P
+// is a TMEM operand (P hi and P lo overwrite the S columns they came from).
+// TMEM holds three S buffers (QK runs up to two tiles ahead of the softmax)
+// and O'.
 //
-// Warp roles (16 warps):
-//   0-7   softmax: warp w owns TMEM lanes 32 (w % 4) .. + 31 (one row per
-//         thread) and the keys 32 (w / 4) .. + 31 of every tile; the two
-//         warps of a row set exchange their partial row maxima through shared
-//         memory. They load and split Q into TMEM at the start of a unit, run
-//         the online softmax, write P hi/lo, rescale O when the reference
-//         maximum moves, and write the output.
-//   8     K producer: TMA loads of K tiles into the K ring.
-//   9     QK issuer: allocates TMEM; one lane issues QK(n) as soon as K(n) is
-//         converted and S buffer n & 1 is free (PV(n-2) complete).
-//   10    V producer: TMA loads of V tiles into the raw V ring.
-//   11-12 K converters: K lo next to each K tile (one d-half each).
-//   13-14 V converters: raw V -> V^T hi / V^T lo (one d-half each).
-//   15    PV issuer: one lane issues PV(n) as soon as P(n) and V^T(n) are ready.
+// Warp roles (12 warps):
+//   0-3   softmax: warp w owns TMEM lanes 32 w .. + 31 (one row per thread)
+//         and all 64 keys of every tile. They split Q into shared memory at the
+//         start of a unit, run the online softmax, write P hi/lo, rescale O
+//         when the reference maximum moves, and write the output.
+//   4     K producer: TMA loads of K tiles into the K ring.
+//   5     QK issuer: allocates TMEM; one lane issues QK(n) as soon as K(n) is
+//         converted and S buffer n % 3 is free (PV(n-3) complete).
+//   6     V producer: TMA loads of V tiles into the raw V ring.
+//   7-8   K converters: K lo next to each K tile (one d-half each).
+//   9-10  V converters: raw V -> V^T hi / V^T lo (one d-half each).
+//   11    PV issuer: one lane issues PV(n) as soon as P(n) and V^T(n) are ready.
 // The two issuers are separate threads so that neither stream of MMAs waits
 // behind the other's inputs: the tensor core's issue queue is shallow, and a
 // single issuer that blocks on one condition leaves the pipe idle.
@@ -60,25 +60,24 @@ using namespace tc;
 constexpr int kBq = 32;           // chunk positions per unit
 constexpr int kM = kBq * kGroup;  // 128 rows = TMEM lanes
 constexpr int kBc = 64;           // keys per tile
-constexpr int kKStages = 3;       // K ring: [K | K lo] per d-half region
-constexpr int kVRawStages = 3;    // raw V landing ring
+constexpr int kKStages = 2;       // K ring: [K | K lo] per d-half region
+constexpr int kVRawStages = 2;    // raw V landing ring
 constexpr int kVStages = 2;       // V^T ring: [V^T hi | V^T lo] per key-half region
+constexpr int kNumS = 3;          // S / P buffers in TMEM
 
-constexpr int kSoftmaxWarps = 8;
-constexpr int kKProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kVProducerWarp = 10;
-constexpr int kFirstKConvWarp = 11;
+constexpr int kSoftmaxWarps = 4;
+constexpr int kKProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kVProducerWarp = 6;
+constexpr int kFirstKConvWarp = 7;
 constexpr int kKConvWarps = 2;
-constexpr int kFirstVConvWarp = 13;
+constexpr int kFirstVConvWarp = 9;
 constexpr int kVConvWarps = 2;
 constexpr int kPvWarp = kFirstVConvWarp + kVConvWarps;
 constexpr int kThreads = 32 * (kPvWarp + 1);
 
 // TMEM columns (fp32, one per column).
-constexpr uint32_t kColQhi = 0;
-constexpr uint32_t kColQlo = 64;
-constexpr uint32_t kColS = 128;  // two 128-column S buffers; P hi | P lo overwrite them
+constexpr uint32_t kColS = 0;    // three 128-column S buffers; P hi | P lo overwrite them
 constexpr uint32_t kColO = 384;  // O' = [P_hi V_hi + P_lo V_hi | P_hi V_lo]
 constexpr uint32_t kTmemCols = 512;
 
@@ -90,14 +89,14 @@ constexpr uint32_t kHalf = 64 * 128;                     // 8 KB: 64 rows
 constexpr uint32_t kKStageBytes = 2 * kRegion;           // 2 d-half regions
 constexpr uint32_t kVRawBytes = 2 * kHalf;               // 2 d-half regions of 64 keys
 constexpr uint32_t kVStageBytes = 2 * kRegion;           // 2 key-half regions
-constexpr uint32_t kSmemK = 0;
+constexpr uint32_t kSmemQ = 0;                           // Q hi (two d-half regions), then Q lo
+constexpr uint32_t kQTermBytes = 2 * kRegion;             // 32 KB per term
+constexpr uint32_t kSmemK = kSmemQ + 2 * kQTermBytes;
 constexpr uint32_t kSmemVRaw = kSmemK + kKStages * kKStageBytes;
 constexpr uint32_t kSmemVT = kSmemVRaw + kVRawStages * kVRawBytes;
 constexpr uint32_t kSmemBar = kSmemVT + kVStages * kVStageBytes;
-constexpr uint32_t kNumBars = 3 * kKStages + 2 * kVRawStages + 2 * kVStages + 2 + 2 + 2 + 1 + 2 + 4;
-constexpr uint32_t kSmemRed = kSmemBar + kNumBars * 8 + 16;  // [2 tile parities][2 key halves][128 rows]
-constexpr uint32_t kSmemLsum = kSmemRed + 2 * 2 * 128 * 4;   // [2 key halves][128 rows]
-constexpr uint32_t kSmemTotal = kSmemLsum + 2 * 128 * 4;
+constexpr uint32_t kNumBars = 3 * kKStages + 2 * kVRawStages + 2 * kVStages + 3 * kNumS + 1 + 2;
+constexpr uint32_t kSmemTotal = kSmemBar + kNumBars * 8 + 16;
 constexpr uint32_t kSmemAlloc = kSmemTotal + 1024;  // slack to align the base
 
 static_assert(kSmemAlloc <= 232448, "exceeds the 227 KB per-block shared memory limit");
@@ -133,12 +132,11 @@ struct Bars {
   uint64_t* vrfree;  // [kVRawStages] V converters done reading raw V
   uint64_t* vconv;   // [kVStages] V^T hi/lo written
   uint64_t* vempty;  // [kVStages] PV done with the stage (MMA commit)
-  uint64_t* sfull;   // [2] S buffer written (MMA commit)
-  uint64_t* pfull;   // [2] P hi/lo written and O rescaled (softmax warps)
-  uint64_t* odone;   // [2] PV(n) done, barrier n & 1 (MMA commit)
-  uint64_t* qready;  // Q hi/lo in TMEM (softmax warps)
+  uint64_t* sfull;   // [kNumS] S buffer written (MMA commit)
+  uint64_t* pfull;   // [kNumS] P hi/lo written and O rescaled (softmax warps)
+  uint64_t* odone;   // [kNumS] PV(n) done, barrier n % 3 (MMA commit)
+  uint64_t* qready;  // Q hi/lo in shared memory (softmax warps)
   uint64_t* drain;   // [2] drain of each MMA issuer on abort (QK, PV)
-  uint64_t* pair;    // [4] the two softmax warps of a row quarter exchange partial results
 };
 
 __device__ __forceinline__ Bars carve_bars(uint8_t* base) {
@@ -151,12 +149,11 @@ __device__ __forceinline__ Bars carve_bars(uint8_t* base) {
   r.vrfree = b; b += kVRawStages;
   r.vconv = b; b += kVStages;
   r.vempty = b; b += kVStages;
-  r.sfull = b; b += 2;
-  r.pfull = b; b += 2;
-  r.odone = b; b += 2;
+  r.sfull = b; b += kNumS;
+  r.pfull = b; b += kNumS;
+  r.odone = b; b += kNumS;
   r.qready = b++;
   r.drain = b; b += 2;
-  r.pair = b; b += 4;
   return r;
 }
 
@@ -241,16 +238,14 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
       mbar_init(&bars.vconv[s], kVConvWarps);
       mbar_init(&bars.vempty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kNumS; ++b) {
       mbar_init(&bars.sfull[b], 1);
       mbar_init(&bars.pfull[b], kSoftmaxWarps);
+      mbar_init(&bars.odone[b], 1);
     }
-    mbar_init(&bars.odone[0], 1);
-    mbar_init(&bars.odone[1], 1);
     mbar_init(bars.qready, kSoftmaxWarps);
     mbar_init(&bars.drain[0], 1);
     mbar_init(&bars.drain[1], 1);
-    for (int q = 0; q < 4; ++q) mbar_init(&bars.pair[q], 2);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -339,33 +334,36 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
         }
         for (int j = 0; j < w.ntiles; ++j, ++n) {
           if (is_qk) {
-            // QK(n): K(n) converted; S buffer n & 1 free once PV(n-2) has read
-            // P(n-2) from it (odone[n & 1] is at most one phase past PV(n-2):
+            // QK(n): K(n) converted; S buffer n % 3 free once PV(n-3) has read
+            // P(n-3) from it (odone[n % 3] is at most one phase past PV(n-3):
             // PV(n) needs S(n), which is issued only below).
             const int ks = n % kKStages;
+            const int sb = n % kNumS;
             if (!wait_bar(&bars.kconv[ks], (n / kKStages) & 1, prm, abort_flag)) goto mma_done;
-            if (n >= 2 && !wait_bar(&bars.odone[n & 1], ((n >> 1) - 1) & 1, prm, abort_flag)) goto mma_done;
+            if (n >= kNumS && !wait_bar(&bars.odone[sb], ((n / kNumS) - 1) & 1, prm, abort_flag)) goto mma_done;
             tc_fence_after();
             const uint32_t kb = smem_u32(smem + kSmemK + ks * kKStageBytes);
-            const uint32_t d = tmem + kColS + (n & 1) * 128;
+            const uint32_t qb = smem_u32(smem + kSmemQ);
+            const uint32_t d = tmem + kColS + sb * 128;
 #pragma unroll
             for (int s = 0; s < 8; ++s)  // [Q_hi K_hi^T | Q_hi K_lo^T]
-              mma_tf32_ts(d, tmem + kColQhi + s * 8, sdesc_sw128(kb + (s >> 2) * kRegion + (s & 3) * 32),
-                          kIdescN128, s > 0);
+              mma_tf32_ss(d, sdesc_sw128(qb + (s >> 2) * kRegion + (s & 3) * 32),
+                          sdesc_sw128(kb + (s >> 2) * kRegion + (s & 3) * 32), kIdescN128, s > 0);
 #pragma unroll
             for (int s = 0; s < 8; ++s)  // += Q_lo K_hi^T into the first half
-              mma_tf32_ts(d, tmem + kColQlo + s * 8, sdesc_sw128(kb + (s >> 2) * kRegion + (s & 3) * 32),
-                          kIdescN64, 1);
-            mma_commit(&bars.sfull[n & 1]);
+              mma_tf32_ss(d, sdesc_sw128(qb + kQTermBytes + (s >> 2) * kRegion + (s & 3) * 32),
+                          sdesc_sw128(kb + (s >> 2) * kRegion + (s & 3) * 32), kIdescN64, 1);
+            mma_commit(&bars.sfull[sb]);
             mma_commit(&bars.kempty[ks]);
           } else {
             // PV(n): P(n) written by the softmax warps, V^T(n) converted.
             const int vs = n % kVStages;
-            if (!wait_bar(&bars.pfull[n & 1], (n >> 1) & 1, prm, abort_flag)) goto mma_done;
+            const int sb = n % kNumS;
+            if (!wait_bar(&bars.pfull[sb], (n / kNumS) & 1, prm, abort_flag)) goto mma_done;
             if (!wait_bar(&bars.vconv[vs], (n / kVStages) & 1, prm, abort_flag)) goto mma_done;
             tc_fence_after();
             const uint32_t vt = smem_u32(smem + kSmemVT + vs * kVStageBytes);
-            const uint32_t phi = tmem + kColS + (n & 1) * 128;
+            const uint32_t phi = tmem + kColS + sb * 128;
             const uint32_t plo = phi + 64;
             const bool first = j == 0;
 #pragma unroll
@@ -376,7 +374,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
             for (int s = 0; s < 8; ++s)  // += P_lo V_hi into the first half
               mma_tf32_ts(tmem + kColO, plo + s * 8, sdesc_sw128(vt + (s >> 2) * kRegion + (s & 3) * 32),
                           kIdescN64, 1);
-            mma_commit(&bars.odone[n & 1]);
+            mma_commit(&bars.odone[sb]);
             mma_commit(&bars.vempty[vs]);
           }
         }
@@ -491,50 +489,34 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
     }
   vconv_done:;
   } else {
-    // -------------------------------------------------- softmax (warps 0-7)
-    const int rq = warp & 3;           // row quarter: TMEM lanes 32 rq .. 32 rq + 31
-    const int kh = warp >> 2;          // key half of every tile: keys 32 kh .. 32 kh + 31
+    // -------------------------------------------------- softmax (warps 0-3)
+    const int rq = warp;               // TMEM lanes 32 rq .. 32 rq + 31
     const int row = rq * 32 + lane;    // TMEM lane = row of the unit
     const uint32_t lane_tmem = tmem + ((uint32_t)(rq * 32) << 16);
-    float* red = reinterpret_cast<float*>(smem + kSmemRed);    // partial maxima
-    float* lred = reinterpret_cast<float*>(smem + kSmemLsum);  // partial sums
     const float c = kLog2e * kScale;     // exp(s / 8) = 2^(s c)
     const float stale = kStaleLog2 / c;  // in raw-score units
     int n = 0;
 
-    // The two warps of a row set exchange partial results through shared
-    // memory and meet on the mbarrier pair[rq] (one arrival per warp, bounded
-    // wait). Neither warp can get two exchanges ahead of its partner, so the
-    // phase parity identifies the exchange.
-    uint32_t pc = 0;  // exchanges done
-    auto pair_sync = [&]() -> bool {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.pair[rq]);
-      const bool ok = wait_bar_warp(&bars.pair[rq], pc & 1, prm, abort_flag);
-      ++pc;
-      return ok;
-    };
-
-    // This warp's half of the row's query (zeros past the chunk), split into TMEM.
+    // The row's query (zeros past the chunk), split into tf32 hi and lo and
+    // written to the two Q operand regions of shared memory, row `row`, under
+    // the 128-byte swizzle (a quarter-warp's 16-byte stores fall in 8
+    // distinct bank groups).
     auto load_q = [&](const Unit& w) {
       const int pos = w.t0 + (row >> 2);
-      const float* src = p.q + ((size_t)pos * kHQ + w.g * kGroup + (row & 3)) * kD + kh * 32;
-      float hi[32], lo[32];
+      const float* src = p.q + ((size_t)pos * kHQ + w.g * kGroup + (row & 3)) * kD;
 #pragma unroll
-      for (int i = 0; i < 32; i += 4) {
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (pos < p.C) v = __ldg(reinterpret_cast<const float4*>(src + i));
-        const float xs[4] = {v.x, v.y, v.z, v.w};
+      for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          hi[i + t] = tf32_hi(xs[t]);
-          lo[i + t] = xs[t] - hi[i + t];
+        for (int c4 = 0; c4 < 8; ++c4) {
+          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (pos < p.C) v = __ldg(reinterpret_cast<const float4*>(src + h * 32 + c4 * 4));
+          const float4 hi = make_float4(tf32_hi(v.x), tf32_hi(v.y), tf32_hi(v.z), tf32_hi(v.w));
+          const uint32_t off = (uint32_t)h * kRegion + sw128((uint32_t)row * 128u + (uint32_t)c4 * 16u);
+          *reinterpret_cast<float4*>(smem + kSmemQ + off) = hi;
+          *reinterpret_cast<float4*>(smem + kSmemQ + kQTermBytes + off) =
+              make_float4(v.x - hi.x, v.y - hi.y, v.z - hi.z, v.w - hi.w);
         }
-      }
-      tmem_st32(lane_tmem + kColQhi + kh * 32, hi);
-      tmem_st32(lane_tmem + kColQlo + kh * 32, lo);
-      tmem_wait_st();
-      tc_fence_before();
+      fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bars.qready);
     };
@@ -546,38 +528,38 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
       const Unit w = decode_unit(u, prm);
       if (!q_loaded) load_q(w);
       q_loaded = false;
-      float m_ref = -INFINITY, l = 0.f;  // l: this warp's share of the row sum
+      float m_ref = -INFINITY, l = 0.f;
       const int pos = w.t0 + (row >> 2);
       const int limit = p.P + pos;  // last visible key of this row
       for (int j = 0; j < w.ntiles; ++j, ++n) {
-        const int j0 = j * kBc + kh * 32;  // first key of this warp's half
-        const uint32_t sbuf = lane_tmem + kColS + (n & 1) * 128 + kh * 32;
-        if (!wait_bar_warp(&bars.sfull[n & 1], (n >> 1) & 1, prm, abort_flag)) goto softmax_done;
+        const int j0 = j * kBc;
+        const int sb = n % kNumS;
+        const uint32_t sbuf = lane_tmem + kColS + sb * 128;
+        if (!wait_bar_warp(&bars.sfull[sb], (n / kNumS) & 1, prm, abort_flag)) goto softmax_done;
         tc_fence_after();
-        float s[32];
-        {
+        // S = S'[:, 0:64] + S'[:, 64:128] for the tile's 64 keys.
+        float s[64];
+        tmem_ld32(sbuf, *reinterpret_cast<float(*)[32]>(&s[0]));
+        tmem_ld32(sbuf + 32, *reinterpret_cast<float(*)[32]>(&s[32]));
+        tmem_wait_ld();
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
           float t[32];
-          tmem_ld32(sbuf, s);
-          tmem_ld32(sbuf + 64, t);
+          tmem_ld32(sbuf + 64 + half * 32, t);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) add2(s[i], s[i + 1], s[i], s[i + 1], t[i], t[i + 1]);
+          for (int i = 0; i < 32; i += 2)
+            add2(s[half * 32 + i], s[half * 32 + i + 1], s[half * 32 + i], s[half * 32 + i + 1], t[i], t[i + 1]);
         }
-        if (j * kBc + kBc - 1 > p.P + w.t0) {
+        if (j0 + kBc - 1 > p.P + w.t0) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
+          for (int i = 0; i < 64; ++i)
             if (j0 + i > limit) s[i] = -INFINITY;
         }
         float mt = max3(s[0], s[1], s[2]);
 #pragma unroll
-        for (int i = 3; i < 31; i += 2) mt = max3(mt, s[i], s[i + 1]);
-        mt = fmaxf(mt, s[31]);
-        {
-          float* slot = red + (n & 1) * 256;
-          slot[kh * 128 + row] = mt;
-          if (!pair_sync()) goto softmax_done;
-          mt = fmaxf(mt, slot[(kh ^ 1) * 128 + row]);
-        }
+        for (int i = 3; i < 63; i += 2) mt = max3(mt, s[i], s[i + 1]);
+        mt = fmaxf(mt, s[63]);
         float alpha = 1.f;
         if (m_ref == -INFINITY || mt > m_ref + stale) {
           const float m_new = fmaxf(m_ref, mt);
@@ -585,50 +567,50 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
           m_ref = m_new;
         }
         const float mc = m_ref == -INFINITY ? 0.f : m_ref * c;
-        float lsum = 0.f;
-        {
+        float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
           float hi[32], lo[32];
-          float l0 = 0.f, l1 = 0.f;
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
             float a0, a1;
-            fma2(a0, a1, s[i], s[i + 1], c, c, -mc, -mc);
+            fma2(a0, a1, s[half * 32 + i], s[half * 32 + i + 1], c, c, -mc, -mc);
             const float p0 = ex2(a0), p1 = ex2(a1);
             add2(l0, l1, l0, l1, p0, p1);
             hi[i] = tf32_hi(p0);
             hi[i + 1] = tf32_hi(p1);
             fma2(lo[i], lo[i + 1], hi[i], hi[i + 1], -1.f, -1.f, p0, p1);  // p - hi, exact
           }
-          lsum = l0 + l1;
-          tmem_st32(sbuf, hi);
-          tmem_st32(sbuf + 64, lo);
+          tmem_st32(sbuf + half * 32, hi);
+          tmem_st32(sbuf + 64 + half * 32, lo);
         }
-        l = fmaf(l, alpha, lsum);
+        l = fmaf(l, alpha, l0 + l1);
         tmem_wait_st();
         // O is rescaled only when the reference maximum moved; PV(n-1) must be
         // complete first. Skipping this wait otherwise is safe for the parity
-        // bookkeeping: PV(n+1) cannot run before these warps release P(n+1), so
-        // odone[(n-1) & 1] is at most one phase past the one waited for here.
-        // Both warps of a row set take the same decision (same m_ref, same mt).
+        // bookkeeping: PV(n+2) cannot run before these warps release P(n+2), so
+        // odone[(n-1) % 3] is at most one phase past the one waited for here.
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-          if (!wait_bar_warp(&bars.odone[(n - 1) & 1], ((n - 1) >> 1) & 1, prm, abort_flag)) goto softmax_done;
+          const int pb = (n - 1) % kNumS;
+          if (!wait_bar_warp(&bars.odone[pb], ((n - 1) / kNumS) & 1, prm, abort_flag)) goto softmax_done;
           tc_fence_after();
 #pragma unroll
-          for (int part = 0; part < 2; ++part) {  // O' columns 64 kh .. 64 kh + 63
+          for (int part = 0; part < 4; ++part) {  // O' columns 32 part .. + 31
             float o[32];
-            tmem_ld32(lane_tmem + kColO + kh * 64 + part * 32, o);
+            tmem_ld32(lane_tmem + kColO + part * 32, o);
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] *= alpha;
-            tmem_st32(lane_tmem + kColO + kh * 64 + part * 32, o);
+            tmem_st32(lane_tmem + kColO + part * 32, o);
           }
           tmem_wait_st();
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars.pfull[n & 1]);
+        if (lane == 0) mbar_arrive(&bars.pfull[sb]);
       }
-      // The next unit's Q can go into TMEM now: its last QK has completed.
+      // The next unit's Q can go into shared memory now: its last QK has
+      // completed (its S was just consumed).
       {
         const int u_next = unit_index(k + 1, cta, grid);
         if (u_next < prm.n_units) {
@@ -636,21 +618,21 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
           q_loaded = true;
         }
       }
-      // Epilogue: the row sum is the two warps' shares; wait for the last PV,
-      // add the two stacked halves of O', one division per element. This warp
-      // writes head dimensions 32 kh .. 32 kh + 31.
-      lred[kh * 128 + row] = l;
-      if (!pair_sync()) goto softmax_done;
-      l += lred[(kh ^ 1) * 128 + row];
-      if (!wait_bar_warp(&bars.odone[(n - 1) & 1], ((n - 1) >> 1) & 1, prm, abort_flag)) goto softmax_done;
-      tc_fence_after();
+      // Epilogue: wait for the last PV, add the two stacked halves of O', one
+      // division per element.
       {
+        const int pb = (n - 1) % kNumS;
+        if (!wait_bar_warp(&bars.odone[pb], ((n - 1) / kNumS) & 1, prm, abort_flag)) goto softmax_done;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int dh = 0; dh < 2; ++dh) {
         float a[32], b[32];
-        tmem_ld32(lane_tmem + kColO + kh * 32, a);
-        tmem_ld32(lane_tmem + kColO + 64 + kh * 32, b);
+        tmem_ld32(lane_tmem + kColO + dh * 32, a);
+        tmem_ld32(lane_tmem + kColO + 64 + dh * 32, b);
         tmem_wait_ld();
         if (pos < p.C) {
-          float* dst = p.out + ((size_t)pos * kHQ + w.g * kGroup + (row & 3)) * kD + kh * 32;
+          float* dst = p.out + ((size_t)pos * kHQ + w.g * kGroup + (row & 3)) * kD + dh * 32;
 #pragma unroll
           for (int i = 0; i < 32; i += 4)
             *reinterpret_cast<float4*>(dst + i) =
@@ -658,9 +640,6 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
                             (a[i + 3] + b[i + 3]) / l);
         }
       }
-      // The next write of this warp's share (the next unit's epilogue) comes
-      // after at least one more exchange, which the partner only joins after
-      // reading this one.
       tc_fence_before();
     }
   softmax_done:;
