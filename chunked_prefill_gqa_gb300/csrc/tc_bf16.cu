@@ -55,7 +55,8 @@ using namespace tc;
 constexpr int kBq = 32;           // chunk positions per unit
 constexpr int kM = kBq * kGroup;  // 128 rows = TMEM lanes
 constexpr int kBc = 128;          // keys per tile
-constexpr int kStages = 3;        // K and V rings
+template <bool kF32>
+constexpr int stages_of() { return kF32 ? 3 : 4; }  // K and V rings (the fp32 stage is twice the size)
 constexpr int kNumS = 3;          // S / P buffers in TMEM
 
 constexpr int kSoftmaxWarps = 8;
@@ -84,6 +85,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOperandBytes = kBc * kD * 2;  // 16 KB
 template <bool kF32>
 struct Layout {
+  static constexpr int kStages = stages_of<kF32>();
   static constexpr uint32_t kStageBytes = kF32 ? 2 * kOperandBytes : kOperandBytes;
   static constexpr uint32_t kSmemK = 0;
   static constexpr uint32_t kSmemV = kSmemK + kStages * kStageBytes;
@@ -128,6 +130,7 @@ struct Bars {
 template <bool kF32>
 __device__ __forceinline__ Bars carve_bars(uint8_t* base) {
   uint64_t* b = reinterpret_cast<uint64_t*>(base + Layout<kF32>::kSmemBar);
+  constexpr int kStages = Layout<kF32>::kStages;
   Bars r;
   r.kfull = b; b += kStages;
   r.kconv = b; b += kStages;
@@ -220,6 +223,7 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
   using L = Layout<kF32>;
   constexpr uint32_t kSmemK = L::kSmemK, kSmemV = L::kSmemV, kSmemBar = L::kSmemBar, kNumBars = L::kNumBars;
   constexpr uint32_t kSmemRed = L::kSmemRed, kSmemLsum = L::kSmemLsum, kStageBytes = L::kStageBytes;
+  constexpr int kStages = L::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const Bars bars = carve_bars<kF32>(smem);
