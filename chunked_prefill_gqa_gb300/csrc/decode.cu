@@ -29,10 +29,11 @@ namespace {
 
 constexpr int kTile = 64;            // keys per staged tile
 constexpr int kThreads = 128;
+constexpr int kWarps = kThreads / 32;
 constexpr int kLdK = 68;             // padded K row (floats): 16-byte loads of 8 consecutive keys hit 8 bank groups
 constexpr int kPartFloats = kGroup * kD + 2 * kGroup;  // O_s for 4 heads, then m_s[4], l_s[4]
 constexpr size_t kSplitSmem =
-    sizeof(float) * (2 * kTile * kLdK + 2 * kTile * kD + kGroup * kD + kGroup * kTile);  // 69,632 B
+    sizeof(float) * (2 * kTile * kLdK + 2 * kTile * kD + kGroup * kD + 2 * kGroup * kTile + kGroup);  // 70,672 B
 
 __device__ __forceinline__ void cp_async16(float* dst, const float* src, bool valid) {
   const unsigned s = (unsigned)__cvta_generic_to_shared(dst);
@@ -89,7 +90,9 @@ decode_split_kernel(DecodeArgs a) {
   float* const vs0 = dsm + 2 * kTile * kLdK;       // two V tiles
   float (*qs)[kD] = reinterpret_cast<float (*)[kD]>(dsm + 2 * kTile * kLdK + 2 * kTile * kD);
   float (*sc)[kTile] = reinterpret_cast<float (*)[kTile]>(dsm + 2 * kTile * kLdK + 2 * kTile * kD + kGroup * kD);
-  // sc: scores, then probabilities
+  // sc: the tile's scores [head][key]; pk: its probabilities [key][head]; al: alpha per head
+  float (*pk)[kGroup] = reinterpret_cast<float (*)[kGroup]>(&sc[0][0] + kGroup * kTile);
+  float* al = &pk[0][0] + kTile * kGroup;
 
   const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -119,9 +122,14 @@ decode_split_kernel(DecodeArgs a) {
 
   // Score layout: thread (key = tid % 64, head pair = tid / 64).
   const int skey = tid & 63, hp = (tid >> 6) * 2;
-  // Output layout: warp = head, lane owns head dimensions 2 lane, 2 lane + 1.
-  const int oh = warp;
-  float m = -INFINITY, l = 0.f, o0 = 0.f, o1 = 0.f;
+  // Softmax: warp = head (m and l live in warp `warp`'s registers for head `warp`).
+  // Weighted sum: warp w takes keys 16 w .. 16 w + 15 of every tile for all four
+  // heads, lane = head dims 2 lane, 2 lane + 1; the four warps' sums share each
+  // head's reference maximum and are added at the end.
+  float m = -INFINITY, l = 0.f;
+  float o[kGroup][2];
+#pragma unroll
+  for (int h = 0; h < kGroup; ++h) o[h][0] = o[h][1] = 0.f;
 
   const int ntiles = (k1 - k0 + kTile - 1) / kTile;
   load_tile(a, b, g, k0, k1, ks0, vs0, tid);
@@ -156,9 +164,10 @@ decode_split_kernel(DecodeArgs a) {
     }
     __syncthreads();
 
-    // Online update for head oh (one warp): tile max, rescale, probabilities.
+    // Online update for head `warp`: tile max, alpha, probabilities.
     {
-      const float s0 = sc[oh][lane], s1 = sc[oh][lane + 32];
+      const int h = warp;
+      const float s0 = sc[h][lane], s1 = sc[h][lane + 32];
       float mx = fmaxf(s0, s1);
 #pragma unroll
       for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
@@ -169,33 +178,68 @@ decode_split_kernel(DecodeArgs a) {
 #pragma unroll
       for (int off = 16; off >= 1; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
       l = fmaf(l, alpha, ps);
-      o0 *= alpha;
-      o1 *= alpha;
       m = mnew;
-      __syncwarp();
-      sc[oh][lane] = p0;
-      sc[oh][lane + 32] = p1;
-      __syncwarp();
-      const float* vb = vs0 + buf * kTile * kD + 2 * lane;
-#pragma unroll 8
-      for (int j = 0; j < kTile; ++j) {
-        const float pj = sc[oh][j];
+      pk[lane][h] = p0;
+      pk[lane + 32][h] = p1;
+      if (lane == 0) al[h] = alpha;
+    }
+    __syncthreads();
+
+    // O_w += P V over this warp's 16 keys, all four heads.
+    {
+      const float4 a4 = *reinterpret_cast<const float4*>(al);
+      o[0][0] *= a4.x; o[0][1] *= a4.x;
+      o[1][0] *= a4.y; o[1][1] *= a4.y;
+      o[2][0] *= a4.z; o[2][1] *= a4.z;
+      o[3][0] *= a4.w; o[3][1] *= a4.w;
+      const float* vb = vs0 + buf * kTile * kD + (16 * warp) * kD + 2 * lane;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float4 p4 = *reinterpret_cast<const float4*>(&pk[16 * warp + j][0]);
         const float2 vv = *reinterpret_cast<const float2*>(vb + j * kD);
-        o0 = fmaf(pj, vv.x, o0);
-        o1 = fmaf(pj, vv.y, o1);
+        o[0][0] = fmaf(p4.x, vv.x, o[0][0]);
+        o[0][1] = fmaf(p4.x, vv.y, o[0][1]);
+        o[1][0] = fmaf(p4.y, vv.x, o[1][0]);
+        o[1][1] = fmaf(p4.y, vv.y, o[1][1]);
+        o[2][0] = fmaf(p4.z, vv.x, o[2][0]);
+        o[2][1] = fmaf(p4.z, vv.y, o[2][1]);
+        o[3][0] = fmaf(p4.w, vv.x, o[3][0]);
+        o[3][1] = fmaf(p4.w, vv.y, o[3][1]);
       }
     }
-    __syncthreads();  // before the next tile overwrites sc, ks, vs
+    __syncthreads();  // before the next tile overwrites sc, pk, al, ks, vs
   }
 
-  if (!part) {
-    float2* dst = reinterpret_cast<float2*>(a.out + ((size_t)b * kHQ + g * kGroup + oh) * kD + 2 * lane);
-    *dst = make_float2(o0 / l, o1 / l);
-  } else {
-    *reinterpret_cast<float2*>(part + oh * kD + 2 * lane) = make_float2(o0 / l, o1 / l);
-    if (lane == 0) {
-      part[kGroup * kD + oh] = m;
-      part[kGroup * kD + kGroup + oh] = l;
+  // Sum the four warps' accumulators (the first K tile buffer is free now),
+  // then one division per element by the head's l.
+  float* acc = ks0;  // [4 warps][4 heads][64]
+#pragma unroll
+  for (int h = 0; h < kGroup; ++h)
+    *reinterpret_cast<float2*>(acc + (warp * kGroup + h) * kD + 2 * lane) = make_float2(o[h][0], o[h][1]);
+  if (lane == 0) {
+    al[warp] = l;  // head `warp`'s l (al is no longer needed)
+    sc[0][warp] = m;
+  }
+  __syncthreads();
+  {
+    const int h = tid >> 5, dl = tid & 31;  // thread = (head, pair of head dims)
+    float O0 = 0.f, O1 = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float2 x = *reinterpret_cast<const float2*>(acc + (w * kGroup + h) * kD + 2 * dl);
+      O0 += x.x;
+      O1 += x.y;
+    }
+    const float lh = al[h], mh = sc[0][h];
+    if (!part) {
+      *reinterpret_cast<float2*>(a.out + ((size_t)b * kHQ + g * kGroup + h) * kD + 2 * dl) =
+          make_float2(O0 / lh, O1 / lh);
+    } else {
+      *reinterpret_cast<float2*>(part + h * kD + 2 * dl) = make_float2(O0 / lh, O1 / lh);
+      if (dl == 0) {
+        part[kGroup * kD + h] = mh;
+        part[kGroup * kD + kGroup + h] = lh;
+      }
     }
   }
 }
