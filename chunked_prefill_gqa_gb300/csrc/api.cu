@@ -3,6 +3,7 @@
 // kernel launchers. No entry point allocates device memory.
 #include <cstdint>
 #include <cstdio>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -21,12 +22,14 @@ struct DeviceState {
   unsigned* err = nullptr;  // device address of g_error_word on this device
 };
 DeviceState g_devices[kMaxDevices];
+std::mutex g_devices_mu;  // first use of a device may come from several host threads
 
 // Looks up (once per device) whether the current device is sm_103 and where
 // its error word lives. Returns an ATTN_* code.
 int current_device(DeviceState** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ECUDA;
+  std::lock_guard<std::mutex> lock(g_devices_mu);
   DeviceState& st = g_devices[dev];
   if (!st.checked) {
     int major = 0, minor = 0;

@@ -319,10 +319,12 @@ cudaError_t launch_decode(const float* q, const float* k_pages, const float* v_p
                           const int* ctx_lens, float* out, float* parts, int B, int max_blocks, int num_pages,
                           int max_context, int split_len, int splits, unsigned* err, cudaStream_t stream) {
   static bool configured[64] = {};  // the shared-memory opt-in is per device
+  static std::mutex mu;
   int dev = 0;
   cudaError_t e0 = cudaGetDevice(&dev);
   if (e0 != cudaSuccess) return e0;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
   if (!configured[dev]) {
     e0 = cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSplitSmem);
     if (e0 != cudaSuccess) return e0;

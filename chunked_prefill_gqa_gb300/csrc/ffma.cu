@@ -17,6 +17,8 @@
 // lanes that share rg. K and V tiles arrive by cp.async into a two-stage
 // ring; the probabilities go through shared memory, transposed, to the PV
 // product.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace attn {
@@ -221,10 +223,12 @@ ffma_kernel(Problem p, int n_qtiles) {
 
 cudaError_t launch_ffma(const Problem& p, cudaStream_t stream) {
   static bool configured[64] = {};  // the attribute is set once per device
+  static std::mutex mu;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
   if (!configured[dev]) {
     e = cudaFuncSetAttribute(ffma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;

@@ -49,6 +49,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
@@ -692,19 +694,25 @@ struct TcDeviceState {
   int num_sms = 0;
 };
 TcDeviceState g_tc_state[64];
+std::mutex g_tc_state_mu;
 
 int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long timeout_ns, int fault,
                    const int* table = nullptr, int num_pages = 0) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ECUDA;
-  TcDeviceState& st = g_tc_state[dev];
-  if (!st.ready) {
-    if (cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return ATTN_ECUDA;
-    if (cudaFuncSetAttribute(tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc) !=
-        cudaSuccess)
-      return ATTN_ECUDA;
-    st.ready = true;
+  int num_sms = 0;
+  {
+    std::lock_guard<std::mutex> lock(g_tc_state_mu);
+    TcDeviceState& st = g_tc_state[dev];
+    if (!st.ready) {
+      if (cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return ATTN_ECUDA;
+      if (cudaFuncSetAttribute(tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc) !=
+          cudaSuccess)
+        return ATTN_ECUDA;
+      st.ready = true;
+    }
+    num_sms = st.num_sms;
   }
   alignas(64) CUtensorMap mk, mv;
   const int rows = table ? num_pages * kPage : p.P + p.C;
@@ -720,7 +728,7 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
   prm.fault_skip_first_k = fault;
   prm.table = table;
   prm.num_pages = num_pages;
-  const int grid = prm.n_units < st.num_sms ? prm.n_units : st.num_sms;
+  const int grid = prm.n_units < num_sms ? prm.n_units : num_sms;
   tc_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(mk, mv, prm);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ELAUNCH;
 }

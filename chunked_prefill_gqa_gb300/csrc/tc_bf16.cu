@@ -44,6 +44,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
@@ -630,19 +632,25 @@ struct DevState {
   int num_sms = 0;
 };
 DevState g_state[64];
+std::mutex g_state_mu;
 
 template <bool kF32>
 int launch_impl(const Problem& p, cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ECUDA;
-  DevState& st = g_state[dev];
-  if (!st.ready[kF32]) {
-    if (cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return ATTN_ECUDA;
-    if (cudaFuncSetAttribute(tc_bf16_kernel<kF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)Layout<kF32>::kSmemAlloc) != cudaSuccess)
-      return ATTN_ECUDA;
-    st.ready[kF32] = true;
+  int num_sms = 0;
+  {
+    std::lock_guard<std::mutex> lock(g_state_mu);
+    DevState& st = g_state[dev];
+    if (!st.ready[kF32]) {
+      if (cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return ATTN_ECUDA;
+      if (cudaFuncSetAttribute(tc_bf16_kernel<kF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)Layout<kF32>::kSmemAlloc) != cudaSuccess)
+        return ATTN_ECUDA;
+      st.ready[kF32] = true;
+    }
+    num_sms = st.num_sms;
   }
   alignas(64) CUtensorMap mk, mv;
   int rc = encode_kv_tile_map(p.k, p.P + p.C, kF32, &mk);
@@ -653,7 +661,7 @@ int launch_impl(const Problem& p, cudaStream_t stream) {
   prm.n_qtiles = (p.C + kBq - 1) / kBq;
   prm.n_units = prm.n_qtiles * kHKV;
   prm.timeout_ns = 2000000000ull;
-  const int grid = prm.n_units < st.num_sms ? prm.n_units : st.num_sms;
+  const int grid = prm.n_units < num_sms ? prm.n_units : num_sms;
   tc_bf16_kernel<kF32><<<grid, threads_of<kF32>(), Layout<kF32>::kSmemAlloc, stream>>>(mk, mv, prm);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ELAUNCH;
 }

@@ -41,7 +41,9 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_strerror_and_version(lib):
     cp._lib = None
-    for code in range(-9, 1):
+    codes = [v for k, v in vars(cp).items() if k.startswith("ATTN_E") or k == "ATTN_OK"]
+    assert sorted(codes) == list(range(-11, 1))
+    for code in codes:
         assert cp.strerror(code) and "unknown" not in cp.strerror(code)
     assert "unknown" in cp.strerror(-99)
     assert "sm_103a" in cp.version()
@@ -74,3 +76,42 @@ def test_product_path_does_not_import_the_oracle():
             if fn.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, fn)).read()
                 assert "oracle" not in text.lower().replace("oracle-free", ""), os.path.join(dirpath, fn)
+
+
+def test_header_and_binding_codes_agree():
+    """Every ATTN_E* code and size constant in the header has the same value in
+    the binding."""
+    text = open(os.path.join(ROOT, "include", "attn_prefill.h")).read()
+    defs = dict(re.findall(r"#define (ATTN_\w+)\s+(-?\d+)", text))
+    for name, val in defs.items():
+        if name.startswith("ATTN_E") or name == "ATTN_OK":
+            assert getattr(cp, name) == int(val), name
+    assert cp.PAGE == int(defs["ATTN_PAGE"])
+    assert cp.DECODE_SCRATCH_BYTES == 4 << 20 and "(4u << 20)" in text
+
+
+def test_size_helpers_reject_bad_sizes_without_a_gpu(lib):
+    lib.attn_naive_workspace_bytes.restype = ctypes.c_size_t
+    lib.attn_naive_workspace_bytes.argtypes = [ctypes.c_int, ctypes.c_int]
+    assert lib.attn_naive_workspace_bytes(-1, 0) == 0
+    assert lib.attn_naive_workspace_bytes(17, 5) == 32 * 17 * 22 * 4
+    lib.attn_decode_workspace_bytes.restype = ctypes.c_size_t
+    lib.attn_decode_workspace_bytes.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    assert lib.attn_decode_workspace_bytes(0, 100, 0) == 0
+    assert lib.attn_decode_workspace_bytes(4, -1, 0) == 0
+
+
+def test_decode_and_matrix_argument_checks_return_before_any_cuda_call():
+    good = 0x10000
+    f = cp.raw("attn_decode_paged")
+    assert f(good, good, good, good, good, good, -1, 1, 1, 16, 0, None, 0, None) == cp.ATTN_EINVAL
+    assert f(good, good, good, good, good, good, 2, 0, 1, 16, 0, None, 0, None) == cp.ATTN_EINVAL
+    assert f(good, good, good, good, good, good, 2, 1, 1, 17, 0, None, 0, None) == cp.ATTN_ERANGE  # > 16 * maxBlocks
+    assert f(None, None, None, None, None, None, 0, 1, 1, 16, 0, None, 0, None) == cp.ATTN_OK
+    g = cp.raw("attn_decode_paged_noalloc")
+    assert g(good, good, good, good, good, good, 70000, 1, 1, 16, 0, None) == cp.ATTN_ERANGE
+    assert g(None, good, good, good, good, good, 2, 1, 1, 16, 0, None) == cp.ATTN_EINVAL
+    h = cp.raw("attn_naive_prefill")
+    assert h(good, good, good, good, good, 1 << 30, -1, 0, None) == cp.ATTN_EINVAL
+    assert h(None, None, None, None, None, 0, 0, 7, None) == cp.ATTN_OK
+    assert cp.raw("attn_prefill_bf16kv")(good, good + 2, good, good, 4, 0, None) == cp.ATTN_EALIGN
