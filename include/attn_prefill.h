@@ -17,15 +17,21 @@
  *   out     [C][32][64]       written, never read (it may hold garbage or NaN)
  *
  * Ownership. Every pointer is a DEVICE pointer owned by the caller, on the
- * current CUDA device. The library allocates no device memory per call and
- * takes no workspace: there is no score matrix anywhere (the contract has no
- * workspace argument). q, kCache and vCache are only read.
+ * current CUDA device. The library allocates no device memory per call. The
+ * prefill entry points take no workspace: there is no score matrix anywhere
+ * (the contract has no workspace argument). q, kCache and vCache are only
+ * read. Two families outside that contract take a caller-owned workspace,
+ * described with them: split-KV decode (its segment partials) and the
+ * score-matrix pipeline (the matrix itself).
  *
  * Execution. Every compute entry point validates its arguments on the host,
  * enqueues its kernel(s) on `stream` and returns; completion is observed by
  * synchronising the stream. A NULL stream is the legacy default stream.
  * Calls on different streams may overlap; each call reads only its inputs and
- * writes only its out.
+ * writes only its out (and its own workspace), except attn_decode_paged_noalloc,
+ * whose calls share one library buffer. The first call on a device performs a
+ * one-time set-up (device check, kernel attributes), safe from several host
+ * threads at once.
  *
  * Errors. 0 means enqueued. A negative return is one of ATTN_E* below and
  * means nothing was enqueued (argument errors) or the launch failed. A kernel
