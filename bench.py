@@ -74,8 +74,9 @@ def parse_args():
     ap.add_argument("--seed", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--compare", action="store_true",
-                    help="also time the FFMA path and the starter reference on the same inputs")
+    ap.add_argument("--no-compare", action="store_true",
+                    help="skip timing the FFMA path and the starter reference on the same inputs "
+                         "(the page's SPEEDUP of the kernel over its starter design)")
     return ap.parse_args()
 
 
@@ -588,7 +589,7 @@ def main():
                "matches_device_timed_output": bool(ok)}
 
     compare = None
-    if args.compare and rank == 0 and args.kv == "fp32":
+    if not args.no_compare and rank == 0 and args.kv == "fp32" and not args.paged:
         compare = {}
         for other in ("attn_prefill_ffma", "attn_reference_prefill"):
             if other == args.path:
@@ -617,6 +618,10 @@ def main():
         cpu = {"value": f / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"all {len(rows)} of {C} chunk rows, all 32 heads (the whole step), "
                          f"{dt:.2f} s wall on {threads} threads"}
+        rows1 = sample_rows_for_cpu(C, 64)
+        f1, dt1 = cpu_oracle_sample(inp, rows1, 1)
+        cpu["single_thread"] = {"value": f1 / dt1 / 1e12, "unit": UNIT, "cores": 1,
+                                "sample": f"{len(rows1)} of {C} chunk rows (every 64th + last), {dt1:.2f} s"}
 
     if rank == 0:
         peaks = load_peaks()
@@ -629,6 +634,8 @@ def main():
             "config": {"workload": desc, "C": C, "P": P, "hq": W.HQ, "hkv": W.HKV, "d": W.D,
                        "path": args.path, "kernel": kernel,
                        "flops_per_step": flops,
+                       "launch_ms_median": round(statistics.median(launch_ms), 5),
+                       "launch_ms_min": round(min(launch_ms), 5),
                        "l2": "flushed before every timed step (256 MiB write)",
                        "parallelism": f"replicas x{world}"},
             "roofline": roofline(args.path, kernel, flops, ms_mean, peaks,
