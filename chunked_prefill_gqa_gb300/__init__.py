@@ -38,7 +38,8 @@ MAX_TOKENS = 1 << 24
 PAGE = 16
 
 # Every symbol the header declares (the CPU tests check the library exports them).
-EXPORTS = ("attn_prefill", "attn_prefill_bf16x3", "attn_prefill_bf16kv", "attn_full_causal", "attn_prefill_paged", "attn_decode_paged",
+EXPORTS = ("attn_prefill", "attn_prefill_bf16x3", "attn_prefill_bf16kv", "attn_prefill_host",
+           "attn_prefill_bf16x3_host", "attn_prefill_bf16kv_host", "attn_full_causal", "attn_prefill_paged", "attn_decode_paged",
            "attn_decode_workspace_bytes", "attn_decode_paged_noalloc",
            "attn_naive_workspace_bytes", "attn_naive_scores", "attn_naive_softmax", "attn_naive_weighted_sum",
            "attn_naive_prefill", "attn_prefill_ffma", "attn_reference_prefill", "attn_selftest_timeout", "attn_get_device_error", "attn_strerror", "attn_version")
@@ -75,6 +76,10 @@ def load():
                 fn.argtypes = [vp, vp, vp, vp, ci, ci, vp]
             lib.attn_prefill_bf16kv.restype = ci
             lib.attn_prefill_bf16kv.argtypes = [vp, vp, vp, vp, ci, ci, vp]
+            for name in ("attn_prefill_host", "attn_prefill_bf16x3_host", "attn_prefill_bf16kv_host"):
+                fn = getattr(lib, name)
+                fn.restype = ci
+                fn.argtypes = [vp] * 8 + [ci, ci, vp]
             lib.attn_prefill_paged.restype = ci
             lib.attn_prefill_paged.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, vp]
             lib.attn_decode_paged.restype = ci
@@ -182,6 +187,53 @@ def attn_prefill_bf16kv(q, kCache, vCache, out, P: int, stream=None):
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_prefill_bf16kv")
     return out
+
+
+def _check_host_call(host, dev, C, P, kv_dtypes):
+    import torch
+    shapes = ((C, HQ, D), (P + C, HKV, D), (P + C, HKV, D), (C, HQ, D))
+    names = ("q", "kCache", "vCache", "out")
+    for i, (name, shape) in enumerate(zip(names, shapes)):
+        dtypes = kv_dtypes if i in (1, 2) else (torch.float32,)
+        for where, t, on_gpu in (("_host", host[i], False), ("_dev", dev[i], True)):
+            if not isinstance(t, torch.Tensor):
+                raise TypeError(f"{name}{where} must be a torch.Tensor")
+            if t.dtype not in dtypes or t.is_cuda != on_gpu or not t.is_contiguous() or tuple(t.shape) != shape:
+                raise ValueError(f"{name}{where} must be a contiguous {'CUDA' if on_gpu else 'CPU'} tensor "
+                                 f"of dtype {dtypes[0]} and shape {shape}")
+
+
+def _call_host(name, host, dev, P, stream, kv_dtypes):
+    C = host[0].shape[0]
+    _check_host_call(host, dev, C, P, kv_dtypes)
+    rc = getattr(load(), name)(*[_ptr(t) for t in host], *[_ptr(t) for t in dev], C, int(P), _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, name)
+    return host[3]
+
+
+def attn_prefill_host(q_host, k_host, v_host, out_host, q_dev, k_dev, v_dev, out_dev, P: int, stream=None):
+    """attn_prefill from CPU tensors (pin them for copy/compute overlap) through
+    the caller's CUDA tensors of the same shapes; returns out_host, complete
+    once the stream is synchronised."""
+    import torch
+    return _call_host("attn_prefill_host", (q_host, k_host, v_host, out_host), (q_dev, k_dev, v_dev, out_dev), P,
+                      stream, (torch.float32,))
+
+
+def attn_prefill_bf16x3_host(q_host, k_host, v_host, out_host, q_dev, k_dev, v_dev, out_dev, P: int, stream=None):
+    """attn_prefill_bf16x3 from CPU tensors, as attn_prefill_host."""
+    import torch
+    return _call_host("attn_prefill_bf16x3_host", (q_host, k_host, v_host, out_host), (q_dev, k_dev, v_dev, out_dev),
+                      P, stream, (torch.float32,))
+
+
+def attn_prefill_bf16kv_host(q_host, k_host, v_host, out_host, q_dev, k_dev, v_dev, out_dev, P: int, stream=None):
+    """attn_prefill_bf16kv from CPU tensors, as attn_prefill_host; the K/V
+    tensors (host and device) are bfloat16 or their int16/uint16 patterns."""
+    import torch
+    return _call_host("attn_prefill_bf16kv_host", (q_host, k_host, v_host, out_host), (q_dev, k_dev, v_dev, out_dev),
+                      P, stream, (torch.bfloat16, torch.int16, torch.uint16))
 
 
 def attn_full_causal(q, k, v, out, stream=None):

@@ -93,10 +93,143 @@ int naive_prepare(int C, int P, DeviceState** st) {
   return current_device(st);
 }
 
+// ---------------------------------------------------------------------------
+// Host-buffer calls: the chunk is run as up to kMaxSlices consecutive
+// sub-chunks of whole 32-row query tiles. Sub-chunk s (rows r0 .. r1-1) is the
+// prefill of those rows against positions 0 .. P+r1-1, the same rows of the
+// whole call's result. Its copy-in adds only its query rows and the K/V rows
+// past the previous sub-chunk's end, so copy-in of s+1 and copy-out of s-1
+// overlap the compute of s.
+constexpr int kMaxSlices = 4;
+constexpr int kSliceRows = 512;  // 128 units, under one wave of 152 SMs
+
+struct HostPipe {
+  std::mutex mu;  // held for a whole enqueue: every call re-records the events
+  bool made = false;
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t start = nullptr, done = nullptr;
+  cudaEvent_t loaded[kMaxSlices] = {}, computed[kMaxSlices] = {};
+};
+HostPipe g_pipes[kMaxDevices];
+
+// Slice boundaries: n = clamp(C / 512, 1, 4) slices, slice s ending after
+// floor((s + 1) tiles / n) query tiles, so later slices take the spare tiles.
+int plan_slices(int C, int bounds[kMaxSlices + 1]) {
+  const int tiles = (C + 31) / 32;
+  int n = C / kSliceRows;
+  n = n < 1 ? 1 : (n > kMaxSlices ? kMaxSlices : n);
+  if (n > tiles) n = tiles;
+  bounds[0] = 0;
+  for (int s = 0; s < n; ++s) {
+    const long long end = (long long)(s + 1) * tiles / n * 32;
+    bounds[s + 1] = end < C ? (int)end : C;
+  }
+  return n;
+}
+
+// The current device's pipe, its streams and events made on first use.
+// Called with pipe->mu held.
+int make_pipe(HostPipe* hp) {
+  if (hp->made) return ATTN_OK;
+  if (cudaStreamCreateWithFlags(&hp->in, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&hp->out, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&hp->start, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&hp->done, cudaEventDisableTiming) != cudaSuccess)
+    return ATTN_ECUDA;
+  for (int s = 0; s < kMaxSlices; ++s)
+    if (cudaEventCreateWithFlags(&hp->loaded[s], cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&hp->computed[s], cudaEventDisableTiming) != cudaSuccess)
+      return ATTN_ECUDA;
+  hp->made = true;
+  return ATTN_OK;
+}
+
+using Launcher = int (*)(const Problem&, cudaStream_t);
+
+// kv_row: bytes of one position of kCache (and vCache), 8 heads x 64 values.
+int run_from_host(const float* q_h, const void* k_h, const void* v_h, float* out_h, float* q_d, void* k_d,
+                  void* v_d, float* out_d, size_t kv_row, int C, int P, cudaStream_t stream, Launcher launch) {
+  if (C > 0 && (!q_h || !k_h || !v_h || !out_h)) return ATTN_EINVAL;
+  Problem p{};
+  int rc = prepare(q_d, static_cast<const float*>(k_d), static_cast<const float*>(v_d), out_d, C, P, &p);
+  if (rc != ATTN_OK || C == 0) return rc;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ECUDA;
+  HostPipe* hp = &g_pipes[dev];  // dev < kMaxDevices: prepare checked it
+  std::lock_guard<std::mutex> lock(hp->mu);
+  rc = make_pipe(hp);
+  if (rc != ATTN_OK) return rc;
+  if (cudaEventRecord(hp->start, stream) != cudaSuccess || cudaStreamWaitEvent(hp->in, hp->start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(hp->out, hp->start, 0) != cudaSuccess)
+    return ATTN_ECUDA;
+  constexpr size_t kQRow = sizeof(float) * ATTN_HQ * ATTN_D;
+  auto* kd = static_cast<char*>(k_d);
+  auto* vd = static_cast<char*>(v_d);
+  const auto* kh = static_cast<const char*>(k_h);
+  const auto* vh = static_cast<const char*>(v_h);
+  int bounds[kMaxSlices + 1];
+  const int n = plan_slices(C, bounds);
+  size_t kv0 = 0;
+  for (int s = 0; s < n && rc == ATTN_OK; ++s) {
+    const int r0 = bounds[s], r1 = bounds[s + 1];
+    const size_t q0 = (size_t)r0 * kQRow, nq = (size_t)(r1 - r0) * kQRow;
+    const size_t kv1 = ((size_t)P + r1) * kv_row;
+    if (cudaMemcpyAsync((char*)q_d + q0, (const char*)q_h + q0, nq, cudaMemcpyDefault, hp->in) != cudaSuccess ||
+        cudaMemcpyAsync(kd + kv0, kh + kv0, kv1 - kv0, cudaMemcpyDefault, hp->in) != cudaSuccess ||
+        cudaMemcpyAsync(vd + kv0, vh + kv0, kv1 - kv0, cudaMemcpyDefault, hp->in) != cudaSuccess ||
+        cudaEventRecord(hp->loaded[s], hp->in) != cudaSuccess ||
+        cudaStreamWaitEvent(stream, hp->loaded[s], 0) != cudaSuccess) {
+      rc = ATTN_ECUDA;
+      break;
+    }
+    kv0 = kv1;
+    Problem ps = p;
+    ps.q = q_d + (size_t)r0 * ATTN_HQ * ATTN_D;
+    ps.out = out_d + (size_t)r0 * ATTN_HQ * ATTN_D;
+    ps.C = r1 - r0;
+    ps.P = P + r0;
+    rc = launch(ps, stream);
+    if (rc != ATTN_OK) break;
+    if (cudaEventRecord(hp->computed[s], stream) != cudaSuccess ||
+        cudaStreamWaitEvent(hp->out, hp->computed[s], 0) != cudaSuccess ||
+        cudaMemcpyAsync((char*)out_h + q0, (const char*)out_d + q0, nq, cudaMemcpyDefault, hp->out) != cudaSuccess)
+      rc = ATTN_ECUDA;
+  }
+  // Whatever was enqueued, `stream` waits for both library streams.
+  const bool joined = cudaEventRecord(hp->done, hp->in) == cudaSuccess &&
+                      cudaStreamWaitEvent(stream, hp->done, 0) == cudaSuccess &&
+                      cudaEventRecord(hp->done, hp->out) == cudaSuccess &&
+                      cudaStreamWaitEvent(stream, hp->done, 0) == cudaSuccess;
+  if (rc == ATTN_OK && !joined) rc = ATTN_ECUDA;
+  return rc;
+}
+
 }  // namespace
 }  // namespace attn
 
 using namespace attn;
+
+extern "C" int attn_prefill_host(const float* q_host, const float* kCache_host, const float* vCache_host,
+                                 float* out_host, float* q_dev, float* kCache_dev, float* vCache_dev,
+                                 float* out_dev, int C, int P, cudaStream_t stream) {
+  return run_from_host(q_host, kCache_host, vCache_host, out_host, q_dev, kCache_dev, vCache_dev, out_dev,
+                       sizeof(float) * ATTN_HKV * ATTN_D, C, P, stream, launch_tc);
+}
+
+extern "C" int attn_prefill_bf16x3_host(const float* q_host, const float* kCache_host, const float* vCache_host,
+                                        float* out_host, float* q_dev, float* kCache_dev, float* vCache_dev,
+                                        float* out_dev, int C, int P, cudaStream_t stream) {
+  return run_from_host(q_host, kCache_host, vCache_host, out_host, q_dev, kCache_dev, vCache_dev, out_dev,
+                       sizeof(float) * ATTN_HKV * ATTN_D, C, P, stream, launch_tc_bf16x3);
+}
+
+extern "C" int attn_prefill_bf16kv_host(const float* q_host, const uint16_t* kCache_host,
+                                        const uint16_t* vCache_host, float* out_host, float* q_dev,
+                                        uint16_t* kCache_dev, uint16_t* vCache_dev, float* out_dev, int C, int P,
+                                        cudaStream_t stream) {
+  return run_from_host(q_host, kCache_host, vCache_host, out_host, q_dev, kCache_dev, vCache_dev, out_dev,
+                       sizeof(uint16_t) * ATTN_HKV * ATTN_D, C, P, stream, launch_tc_bf16);
+}
 
 extern "C" int attn_prefill(const float* q, const float* kCache, const float* vCache, float* out,
                             int C, int P, cudaStream_t stream) {

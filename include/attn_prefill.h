@@ -17,7 +17,9 @@
  *   out     [C][32][64]       written, never read (it may hold garbage or NaN)
  *
  * Ownership. Every pointer is a DEVICE pointer owned by the caller, on the
- * current CUDA device. The library allocates no device memory per call. The
+ * current CUDA device, except the host buffers of the three *_host entry
+ * points (described with them). The library allocates no device memory per
+ * call. The
  * prefill entry points take no workspace: there is no score matrix anywhere
  * (the contract has no workspace argument). q, kCache and vCache are only
  * read. Two families outside that contract take a caller-owned workspace,
@@ -123,6 +125,56 @@ int attn_prefill_bf16x3(const float *q, const float *kCache, const float *vCache
  */
 int attn_prefill_bf16kv(const float *q, const uint16_t *kCache, const uint16_t *vCache, float *out,
                         int C, int P, cudaStream_t stream);
+
+/*
+ * attn_prefill_host, attn_prefill_bf16x3_host, attn_prefill_bf16kv_host --
+ * attn_prefill, attn_prefill_bf16x3 and attn_prefill_bf16kv starting and
+ * ending in host memory. The call copies q, kCache and vCache from the host
+ * buffers into the caller's device buffers, computes, and copies out back to
+ * the host. It applies the chunked-prefill identity one level up ("Inference
+ * Attention 2: Flash Prefill Against a Cached Prefix", Lesson: a chunk at
+ * positions P .. P+C-1 attends to every position up to its own): rows r0 ..
+ * r1-1 of the result are the prefill of those query rows against positions
+ * 0 .. P+r1-1. So the chunk runs as n = clamp(C / 512, 1, 4) sub-chunks of
+ * whole 32-row query tiles, and each copies in only its own query rows and the
+ * K/V rows the sub-chunk before it did not need. Copy-in of sub-chunk s+1 and
+ * copy-out of sub-chunk s-1 run under the compute of sub-chunk s, on two
+ * streams the library keeps per device. The result is bit-identical to the
+ * device-pointer entry point on the same inputs.
+ *
+ *   q_host, kCache_host, vCache_host   read; the layouts of attn_prefill
+ *                                      (uint16_t bf16 patterns for the
+ *                                      bf16kv cache)
+ *   out_host                           written
+ *   q_dev, kCache_dev, vCache_dev,     the caller's device buffers with the
+ *   out_dev                            same layouts; all four are written
+ *                                      (after a completed call they hold the
+ *                                      inputs and the result)
+ *
+ * Host memory should be page-locked (cudaHostAlloc or cudaHostRegister):
+ * pageable buffers are accepted but each of their copies then blocks the
+ * calling thread, so nothing overlaps. The copies use cudaMemcpyDefault, so
+ * any memory the driver can copy from or to is accepted.
+ * Ordering. The copies start after the work enqueued on `stream` before the
+ * call, and `stream` waits for the last copy-out: synchronising `stream`
+ * observes out_host complete. Calls from several host threads are serialised
+ * while they enqueue (the library's per-device streams and events are shared).
+ * Set-up. The first call on a device creates two non-blocking streams and ten
+ * events (no device memory); they live until the process ends.
+ * Errors: those of the device-pointer entry point for the device buffers and
+ * sizes; ATTN_EINVAL for a NULL host pointer with C > 0; ATTN_ECUDA when a copy
+ * or a stream or event call fails. After an error, copies may already have
+ * been enqueued; `stream` still waits for every one of them.
+ */
+int attn_prefill_host(const float *q_host, const float *kCache_host, const float *vCache_host,
+                      float *out_host, float *q_dev, float *kCache_dev, float *vCache_dev, float *out_dev,
+                      int C, int P, cudaStream_t stream);
+int attn_prefill_bf16x3_host(const float *q_host, const float *kCache_host, const float *vCache_host,
+                             float *out_host, float *q_dev, float *kCache_dev, float *vCache_dev, float *out_dev,
+                             int C, int P, cudaStream_t stream);
+int attn_prefill_bf16kv_host(const float *q_host, const uint16_t *kCache_host, const uint16_t *vCache_host,
+                             float *out_host, float *q_dev, uint16_t *kCache_dev, uint16_t *vCache_dev,
+                             float *out_dev, int C, int P, cudaStream_t stream);
 
 /*
  * attn_prefill_paged -- attn_prefill against a paged K/V cache ("FlashAttention

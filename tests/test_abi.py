@@ -101,6 +101,41 @@ def test_size_helpers_reject_bad_sizes_without_a_gpu(lib):
     assert lib.attn_decode_workspace_bytes(4, -1, 0) == 0
 
 
+@pytest.mark.parametrize("name", ["attn_prefill_host", "attn_prefill_bf16x3_host", "attn_prefill_bf16kv_host"])
+def test_host_buffer_argument_checks_return_before_any_cuda_call(name):
+    f = cp.raw(name)
+    good = 0x10000
+    host = [good] * 4
+    dev = [good] * 4
+    assert f(*host, *dev, 0, 5, None) == cp.ATTN_OK  # empty chunk: nothing is touched
+    assert f(None, None, None, None, None, None, None, None, 0, 5, None) == cp.ATTN_OK
+    assert f(*host, *dev, -1, 0, None) == cp.ATTN_EINVAL
+    assert f(*host, *dev, 4, -1, None) == cp.ATTN_EINVAL
+    assert f(*host, *dev, cp.MAX_TOKENS + 1, 0, None) == cp.ATTN_ERANGE
+    for i in range(4):
+        h = list(host); h[i] = None
+        assert f(*h, *dev, 4, 0, None) == cp.ATTN_EINVAL, i
+        d = list(dev); d[i] = None
+        assert f(*host, *d, 4, 0, None) == cp.ATTN_EINVAL, i
+        d = list(dev); d[i] = good + 4
+        assert f(*host, *d, 4, 0, None) == cp.ATTN_EALIGN, i
+
+
+def test_host_buffer_binding_checks_tensors():
+    torch = pytest.importorskip("torch")
+    C, P = 3, 2
+    q = torch.zeros(C, 32, 64)
+    kv = torch.zeros(P + C, 8, 64)
+    with pytest.raises(ValueError):  # device buffers on the CPU
+        cp.attn_prefill_host(q, kv, kv, q, q, kv, kv, q, P)
+    with pytest.raises(ValueError):  # wrong K/V shape
+        cp.attn_prefill_host(q, kv[:-1], kv, q, q, kv, kv, q, P)
+    with pytest.raises(ValueError):  # fp32 where the bf16 cache is required
+        cp.attn_prefill_bf16kv_host(q, kv, kv, q, q, kv, kv, q, P)
+    with pytest.raises(TypeError):
+        cp.attn_prefill_host(q.numpy(), kv, kv, q, q, kv, kv, q, P)
+
+
 def test_decode_and_matrix_argument_checks_return_before_any_cuda_call():
     good = 0x10000
     f = cp.raw("attn_decode_paged")
