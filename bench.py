@@ -330,16 +330,21 @@ def run_decode(args):
     stream = torch.cuda.current_stream()
     kv_bytes = sum(lens) * W.HKV * W.D * 4 * 2
     flops = 4.0 * W.D * sum(lens) * W.HQ
+    sampler = ClockSampler(0)
+    sampler.start()
     for _ in range(args.warmup):
         cp.attn_decode_paged(q, kp, vp, tb, cl, out, batch.max_context, 0, ws, stream)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     torch.cuda.synchronize()
+    t_begin = time.time()
     for i in range(args.steps):
         starts[i].record(stream)
         cp.attn_decode_paged(q, kp, vp, tb, cl, out, batch.max_context, 0, ws, stream)
         ends[i].record(stream)
     torch.cuda.synchronize()
+    t_end = time.time()
+    sampler.stop()
     if cp.attn_get_device_error() != 0:
         raise RuntimeError("device error in the decode bench")
     ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / args.steps
@@ -356,7 +361,8 @@ def run_decode(args):
                          "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(gbs / peaks["hbm_gbs"], 4),
                          "traffic": profiled_traffic("attn_decode_paged", "decode")},
-            "gpu_launches": 2 * args.steps}
+            "clocks": sampler.summary(t_begin, t_end),
+            "gpu_launches": (2 if nbytes > 0 else 1) * args.steps}
     print(json.dumps(line))
     return 0
 
@@ -378,6 +384,9 @@ def run_matrix(args):
     peaks = load_peaks()
     ffma_peak = NUM_SMS * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
     table = []
+    sampler = ClockSampler(0)
+    sampler.start()
+    t_begin = time.time()
     for T in W.FULL_T:
         inp = W.full_causal(T, seed=args.seed)
         q = torch.from_numpy(inp.q).to(dev)
@@ -417,6 +426,8 @@ def run_matrix(args):
             "weighted_sum_tflops": round(2 * 64 * visible / (ms[2] * 1e-3) / 1e12, 2)})
         del ws
         torch.cuda.empty_cache()
+    t_end = time.time()
+    sampler.stop()
     last = table[-1]
     dom = max(("scores", "softmax", "weighted_sum"), key=lambda name: last[name + "_ms"])
     if dom == "softmax":
@@ -434,7 +445,8 @@ def run_matrix(args):
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": "full causal prompts T = 512, 1024, 2048; workspace 32 x T x T fp32",
                        "l2": "flushed (256 MiB write) before every kernel", "sizes": table},
-            "roofline": rl, "gpu_launches": 4 * args.steps * len(W.FULL_T)}
+            "roofline": rl, "clocks": sampler.summary(t_begin, t_end),
+            "gpu_launches": 4 * args.steps * len(W.FULL_T)}
     print(json.dumps(line))
     return 0
 

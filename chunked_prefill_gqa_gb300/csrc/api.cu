@@ -291,10 +291,10 @@ extern "C" int attn_prefill_paged(const float* q, const float* kPages, const flo
 
 extern "C" size_t attn_decode_workspace_bytes(int B, int maxContext, int numSplits) {
   if (B <= 0 || maxContext < 0 || numSplits < 0) return 0;
-  int nsm = 0;
-  if (sm_count(&nsm) != ATTN_OK) return 0;
+  int slots = 0;
+  if (decode_slots(&slots) != ATTN_OK) return 0;
   int split_len = 0;
-  const int splits = decode_splits(B, maxContext, numSplits, nsm, &split_len);
+  const int splits = decode_splits(B, maxContext, numSplits, slots, &split_len);
   return decode_workspace_bytes(B, splits);
 }
 
@@ -311,17 +311,17 @@ extern "C" int attn_decode_paged(const float* q, const float* kPages, const floa
   DeviceState* st = nullptr;
   rc = current_device(&st);
   if (rc != ATTN_OK) return rc;
-  int nsm = 0;
-  if ((rc = sm_count(&nsm)) != ATTN_OK) return rc;
+  int slots = 0;
+  if ((rc = decode_slots(&slots)) != ATTN_OK) return rc;
   int split_len = 0;
-  const int splits = decode_splits(B, maxContext, numSplits, nsm, &split_len);
+  const int splits = decode_splits(B, maxContext, numSplits, slots, &split_len);
   const size_t need = decode_workspace_bytes(B, splits);
   if (need > 0) {
     if (!workspace || workspaceBytes < need) return ATTN_ESPACE;
     if (!aligned16(workspace)) return ATTN_EALIGN;
   }
-  return from_cuda(launch_decode(q, kPages, vPages, blockTable, contextLens, out, static_cast<float*>(workspace), B,
-                                 maxBlocks, numPages, maxContext, split_len, splits, st->err, stream));
+  return launch_decode(q, kPages, vPages, blockTable, contextLens, out, static_cast<float*>(workspace), B, maxBlocks,
+                       numPages, maxContext, split_len, splits, st->err, stream);
 }
 
 extern "C" int attn_decode_paged_noalloc(const float* q, const float* kPages, const float* vPages,
@@ -338,15 +338,15 @@ extern "C" int attn_decode_paged_noalloc(const float* q, const float* kPages, co
   DeviceState* st = nullptr;
   rc = current_device(&st);
   if (rc != ATTN_OK) return rc;
-  int nsm = 0;
-  if ((rc = sm_count(&nsm)) != ATTN_OK) return rc;
+  int slots = 0;
+  if ((rc = decode_slots(&slots)) != ATTN_OK) return rc;
   int split_len = 0;
-  const int splits = decode_splits(B, maxContext, numSplits, nsm, &split_len);
+  const int splits = decode_splits(B, maxContext, numSplits, slots, &split_len);
   if (decode_workspace_bytes(B, splits) > kDecodeScratchBytes) return ATTN_ESCRATCH;
   float* scratch = nullptr;
   if (decode_scratch(&scratch) != cudaSuccess) return ATTN_ECUDA;
-  return from_cuda(launch_decode(q, kPages, vPages, blockTable, contextLens, out, scratch, B, maxBlocks, numPages,
-                                 maxContext, split_len, splits, st->err, stream));
+  return launch_decode(q, kPages, vPages, blockTable, contextLens, out, scratch, B, maxBlocks, numPages, maxContext,
+                       split_len, splits, st->err, stream);
 }
 
 extern "C" size_t attn_naive_workspace_bytes(int C, int P) {

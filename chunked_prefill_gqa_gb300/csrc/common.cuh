@@ -48,13 +48,16 @@ cudaError_t launch_reference(const Problem& p, cudaStream_t stream);
 cudaError_t launch_ffma(const Problem& p, cudaStream_t stream);
 int launch_tc(const Problem& p, cudaStream_t stream);             // returns an ATTN_* code
 int launch_tc_fault_test(const Problem& p, cudaStream_t stream);  // skips a load, 20 ms waits
-// Decode (decode.cu): split count and segment length for B sequences of at
-// most max_context keys; workspace bytes for the partials; launch.
-int decode_splits(int B, int max_context, int splits_hint, int num_sms, int* split_len);
+// Decode (decode.cu): how many split blocks the current device holds at once
+// (first call per device sets the kernel up); split count and segment length
+// for B sequences of at most max_context keys; workspace bytes for the
+// partials; launch. The int results are ATTN_* codes.
+int decode_slots(int* slots);
+int decode_splits(int B, int max_context, int splits_hint, int slots, int* split_len);
 size_t decode_workspace_bytes(int B, int splits);
-cudaError_t launch_decode(const float* q, const float* k_pages, const float* v_pages, const int* table,
-                          const int* ctx_lens, float* out, float* parts, int B, int max_blocks, int num_pages,
-                          int max_context, int split_len, int splits, unsigned* err, cudaStream_t stream);
+int launch_decode(const float* q, const float* k_pages, const float* v_pages, const int* table,
+                  const int* ctx_lens, float* out, float* parts, int B, int max_blocks, int num_pages,
+                  int max_context, int split_len, int splits, unsigned* err, cudaStream_t stream);
 // Three-kernel score-matrix attention (naive.cu): workspace bytes, the row
 // limit of its grids, and one launcher per kernel.
 size_t naive_workspace_bytes(int C, int P);

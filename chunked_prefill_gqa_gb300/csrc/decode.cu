@@ -11,43 +11,55 @@
 // query heads that read g, so each K/V row is read once for the group ("FlashAttention
 // and inference kernels", GQA read amplification: one block per (sequence, KV
 // head) computing all four query heads). Keys [s L, min((s+1) L, ctx)) arrive
-// in 64-key tiles through a two-stage cp.async ring, each row found through
-// the block table (same page, PagedAttention: token t in slot t % 16 of page
-// table[t / 16]); m, l and the accumulator are carried across tiles. A segment
-// writes its normalised output O_s = acc / l_s with (m_s, l_s).
+// in 64-key tiles, one TMA box per 16-token page and half of the head
+// dimension, found through the block table (same page, PagedAttention: token
+// t in slot t % 16 of page table[t / 16]), into a ring of kStages tiles whose
+// mbarriers count the bytes; m, l and the accumulator are carried across
+// tiles. A segment writes its normalised output O_s = acc / l_s with (m_s, l_s).
 //
 // Merge kernel (same page, Flash-Decoding and the split-K merge exercise):
 // m = max_s m_s, w_s = e^{m_s - m} l_s, O = sum_s w_s O_s / sum_s w_s, skipping
 // segments with l_s = 0 (m_s = -inf). With one segment the split kernel writes
 // the output directly and no partials are stored.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "common.cuh"
+#include "tc_ptx.cuh"
 
 namespace attn {
 namespace {
 
-constexpr int kTile = 64;            // keys per staged tile
+constexpr int kTile = 64;                      // keys per staged tile: four 16-token pages
+constexpr int kPagesPerTile = kTile / ATTN_PAGE;
 constexpr int kThreads = 128;
 constexpr int kWarps = kThreads / 32;
-constexpr int kLdK = 68;             // padded K row (floats): 16-byte loads of 8 consecutive keys hit 8 bank groups
+constexpr int kStages = 2;                     // ring depth: one tile in flight while one is read (three blocks fit an SM)
+constexpr int kHalfBytes = kTile * 128;        // 32 of the 64 dims of 64 rows, 128-byte swizzled
+constexpr int kBoxBytes = ATTN_PAGE * 128;     // one page's rows of one d-half: a TMA box
+constexpr int kStageBytes = 4 * kHalfBytes;    // K d-halves 0, 1, then V d-halves 0, 1 (32 KB)
 constexpr int kPartFloats = kGroup * kD + 2 * kGroup;  // O_s for 4 heads, then m_s[4], l_s[4]
-constexpr size_t kSplitSmem =
-    sizeof(float) * (2 * kTile * kLdK + 2 * kTile * kD + kGroup * kD + 2 * kGroup * kTile + kGroup);  // 70,672 B
+constexpr unsigned long long kWaitNs = 2000000000ull;  // a tile that has not landed after 2 s is a fault
+constexpr int kSkip = -2147483647 - 1;         // "no page": the tile's rows past the segment
 
-__device__ __forceinline__ void cp_async16(float* dst, const float* src, bool valid) {
-  const unsigned s = (unsigned)__cvta_generic_to_shared(dst);
-  const int n = valid ? 16 : 0;  // n == 0 writes zeros and reads nothing
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(src), "r"(n) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+// Shared memory: the ring (1024-byte aligned for the swizzle), then q [4][64],
+// the tile's scores [4][64], its probabilities [64][4], alpha [4], the ring's
+// barriers.
+constexpr int kSmemQ = kStages * kStageBytes;
+constexpr int kSmemSc = kSmemQ + kGroup * kD * 4;
+constexpr int kSmemPk = kSmemSc + kGroup * kTile * 4;
+constexpr int kSmemAl = kSmemPk + kTile * kGroup * 4;
+constexpr int kSmemBar = kSmemAl + 16;
+constexpr size_t kSplitSmem = kSmemBar + 8 * kStages + 1024;  // + slack for the alignment
+
+// Byte offset of float f (0..31) of row r in a 128-byte-swizzled d-half: the
+// 16-byte chunk c of row r sits at chunk c ^ (r mod 8) (the TMA swizzle).
+__device__ __forceinline__ int swz(int r, int f) { return r * 128 + ((((f >> 2) ^ r) & 7) << 4) + (f & 3) * 4; }
 
 struct DecodeArgs {
   const float* q;          // [B][32][64]
-  const float* k_pages;    // [num_pages][16][8][64]
-  const float* v_pages;
   const int* table;        // [B][max_blocks]
   const int* ctx_lens;     // [B]
   float* out;              // [B][32][64]
@@ -56,43 +68,18 @@ struct DecodeArgs {
   unsigned* err;
 };
 
-// Stage keys [k0, k0 + 64) of KV head g of sequence b (rows at or past `end`
-// become zeros; a table entry outside [0, num_pages) is recorded and read as
-// zeros).
-__device__ __forceinline__ void load_tile(const DecodeArgs& a, int b, int g, int k0, int end, float* ks,
-                                          float* vs, int tid) {
-#pragma unroll
-  for (int it = 0; it < (kTile * kD / 4) / kThreads; ++it) {
-    const int idx = tid + it * kThreads;
-    const int key = idx >> 4, c4 = idx & 15;
-    const int t = k0 + key;
-    bool valid = t < end;
-    size_t row = 0;
-    if (valid) {
-      const int page = __ldg(a.table + (size_t)b * a.max_blocks + (t >> 4));
-      if (page < 0 || page >= a.num_pages) {
-        record_error(a.err, kDevErrBounds);
-        valid = false;
-      } else {
-        row = (size_t)page * 16 + (t & 15);
-      }
-    }
-    const size_t src = (row * kHKV + g) * kD + c4 * 4;
-    cp_async16(ks + key * kLdK + c4 * 4, a.k_pages + src, valid);
-    cp_async16(vs + key * kD + c4 * 4, a.v_pages + src, valid);
-  }
-}
-
+// mk, mv: the K and V page pools [num_pages * 16][8][64] as 2-D tensors
+// (head * 64 + d, row), boxes of 32 floats x 16 rows, 128-byte swizzle.
 __global__ void __launch_bounds__(kThreads)
-decode_split_kernel(DecodeArgs a) {
-  extern __shared__ __align__(16) float dsm[];
-  float* const ks0 = dsm;                         // two K tiles, padded rows
-  float* const vs0 = dsm + 2 * kTile * kLdK;       // two V tiles
-  float (*qs)[kD] = reinterpret_cast<float (*)[kD]>(dsm + 2 * kTile * kLdK + 2 * kTile * kD);
-  float (*sc)[kTile] = reinterpret_cast<float (*)[kTile]>(dsm + 2 * kTile * kLdK + 2 * kTile * kD + kGroup * kD);
+decode_split_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv, DecodeArgs a) {
+  extern __shared__ __align__(16) uint8_t dsm_raw[];
+  uint8_t* const dsm = dsm_raw + ((1024u - (tc::smem_u32(dsm_raw) & 1023u)) & 1023u);
+  float (*qs)[kD] = reinterpret_cast<float (*)[kD]>(dsm + kSmemQ);
   // sc: the tile's scores [head][key]; pk: its probabilities [key][head]; al: alpha per head
-  float (*pk)[kGroup] = reinterpret_cast<float (*)[kGroup]>(&sc[0][0] + kGroup * kTile);
-  float* al = &pk[0][0] + kTile * kGroup;
+  float (*sc)[kTile] = reinterpret_cast<float (*)[kTile]>(dsm + kSmemSc);
+  float (*pk)[kGroup] = reinterpret_cast<float (*)[kGroup]>(dsm + kSmemPk);
+  float* al = reinterpret_cast<float*>(dsm + kSmemAl);
+  uint64_t* full = reinterpret_cast<uint64_t*>(dsm + kSmemBar);
 
   const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -117,8 +104,48 @@ decode_split_kernel(DecodeArgs a) {
     return;
   }
 
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) tc::mbar_init(&full[i], 1);
+    tc::fence_mbar_init();
+  }
   for (int i = tid; i < kGroup * kD; i += kThreads)
     qs[i / kD][i % kD] = a.q[((size_t)b * kHQ + g * kGroup) * kD + i];
+  __syncthreads();
+
+  const int ntiles = (k1 - k0 + kTile - 1) / kTile;
+  const int* trow = a.table + (size_t)b * a.max_blocks;
+  // Warp 0, lane i < 4: the physical page of the i-th page of tile n, or kSkip
+  // when it starts at or past the segment's end (t < k1 <= ctx keeps the table
+  // index below max_blocks).
+  auto page_of = [&](int n) -> int {
+    const int t = k0 + n * kTile + lane * ATTN_PAGE;
+    if (lane >= kPagesPerTile || n >= ntiles || t >= k1) return kSkip;
+    return __ldg(trow + (t >> 4));
+  };
+  // Warp 0 fills tile n's stage: lane 0 posts the bytes of the pages present,
+  // then lane i loads page i's rows of both d-halves of K and of V (four boxes).
+  // A table entry outside [0, num_pages) is recorded and loaded from past the
+  // pool's end, which TMA fills with zeros.
+  auto issue = [&](int n, int pg) {
+    const int st = n % kStages;
+    uint8_t* stage = dsm + st * kStageBytes;
+    const bool has = pg != kSkip;
+    const unsigned npg = __popc(__ballot_sync(0xffffffffu, has));
+    if (lane == 0) tc::mbar_arrive_expect_tx(&full[st], npg * 4u * kBoxBytes);
+    __syncwarp();
+    if (has) {
+      int y = pg;
+      if (pg < 0 || pg >= a.num_pages) {
+        record_error(a.err, kDevErrBounds);
+        y = a.num_pages;
+      }
+      y *= ATTN_PAGE;
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4)
+        tc::tma_load_2d(stage + q4 * kHalfBytes + lane * kBoxBytes, q4 < 2 ? &mk : &mv, &full[st],
+                        g * kD + (q4 & 1) * 32, y);
+    }
+  };
 
   // Score layout: thread (key = tid % 64, head pair = tid / 64).
   const int skey = tid & 63, hp = (tid >> 6) * 2;
@@ -131,33 +158,43 @@ decode_split_kernel(DecodeArgs a) {
 #pragma unroll
   for (int h = 0; h < kGroup; ++h) o[h][0] = o[h][1] = 0.f;
 
-  const int ntiles = (k1 - k0 + kTile - 1) / kTile;
-  load_tile(a, b, g, k0, k1, ks0, vs0, tid);
-  cp_async_commit();
-  for (int it = 0; it < ntiles; ++it) {
-    const int buf = it & 1;
+  int pg_next = kSkip;
+  if (warp == 0) {
+    for (int n = 0; n < kStages - 1 && n < ntiles; ++n) issue(n, page_of(n));
+    pg_next = page_of(kStages - 1);
+  }
+  int it = 0;
+  bool failed = false;
+  for (; it < ntiles; ++it) {
+    const int st = it % kStages;
     const int t0 = k0 + it * kTile;
-    if (it + 1 < ntiles) {
-      load_tile(a, b, g, t0 + kTile, k1, ks0 + (buf ^ 1) * kTile * kLdK, vs0 + (buf ^ 1) * kTile * kD, tid);
-      cp_async_commit();
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
+    // The stage of tile it + kStages - 1 held tile it - 1, which every thread
+    // finished with before the previous iteration's last barrier.
+    if (warp == 0 && it + kStages - 1 < ntiles) {
+      issue(it + kStages - 1, pg_next);
+      pg_next = page_of(it + kStages);  // its latency is spent on this tile's work
     }
-    __syncthreads();
+    const bool ok = tc::mbar_wait(&full[st], (it / kStages) & 1, kWaitNs);
+    if (__syncthreads_or(!ok)) {
+      failed = true;
+      break;
+    }
+    const uint8_t* kt = dsm + st * kStageBytes;
+    const uint8_t* vt = kt + 2 * kHalfBytes;
 
     // Scores of this thread's key against two query heads, scale 1/8.
     {
-      const float* kr = ks0 + buf * kTile * kLdK + skey * kLdK;
       float d0 = 0.f, d1 = 0.f;
 #pragma unroll
       for (int d4 = 0; d4 < kD / 4; ++d4) {
-        const float4 kv = *reinterpret_cast<const float4*>(kr + d4 * 4);
+        const float4 kv =
+            *reinterpret_cast<const float4*>(kt + (d4 >> 3) * kHalfBytes + swz(skey, (d4 & 7) * 4));
         const float4 qa = *reinterpret_cast<const float4*>(&qs[hp][d4 * 4]);
         const float4 qb = *reinterpret_cast<const float4*>(&qs[hp + 1][d4 * 4]);
         d0 = fmaf(qa.x, kv.x, fmaf(qa.y, kv.y, fmaf(qa.z, kv.z, fmaf(qa.w, kv.w, d0))));
         d1 = fmaf(qb.x, kv.x, fmaf(qb.y, kv.y, fmaf(qb.z, kv.z, fmaf(qb.w, kv.w, d1))));
       }
+      // Keys past the segment read whatever the page slot holds (NaN included).
       const bool valid = t0 + skey < k1;
       sc[hp][skey] = valid ? d0 * kScale : -INFINITY;
       sc[hp + 1][skey] = valid ? d1 * kScale : -INFINITY;
@@ -185,18 +222,22 @@ decode_split_kernel(DecodeArgs a) {
     }
     __syncthreads();
 
-    // O_w += P V over this warp's 16 keys, all four heads.
+    // O_w += P V over this warp's 16 keys, all four heads. A key past the
+    // segment is skipped, not weighted by zero: its slot may hold NaN.
     {
       const float4 a4 = *reinterpret_cast<const float4*>(al);
       o[0][0] *= a4.x; o[0][1] *= a4.x;
       o[1][0] *= a4.y; o[1][1] *= a4.y;
       o[2][0] *= a4.z; o[2][1] *= a4.z;
       o[3][0] *= a4.w; o[3][1] *= a4.w;
-      const float* vb = vs0 + buf * kTile * kD + (16 * warp) * kD + 2 * lane;
+      const uint8_t* vb = vt + (lane >> 4) * kHalfBytes;
+      const int f = (2 * lane) & 31;
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        const float4 p4 = *reinterpret_cast<const float4*>(&pk[16 * warp + j][0]);
-        const float2 vv = *reinterpret_cast<const float2*>(vb + j * kD);
+        const int key = 16 * warp + j;
+        if (t0 + key >= k1) break;
+        const float4 p4 = *reinterpret_cast<const float4*>(&pk[key][0]);
+        const float2 vv = *reinterpret_cast<const float2*>(vb + swz(key, f));
         o[0][0] = fmaf(p4.x, vv.x, o[0][0]);
         o[0][1] = fmaf(p4.x, vv.y, o[0][1]);
         o[1][0] = fmaf(p4.y, vv.x, o[1][0]);
@@ -207,12 +248,24 @@ decode_split_kernel(DecodeArgs a) {
         o[3][1] = fmaf(p4.w, vv.y, o[3][1]);
       }
     }
-    __syncthreads();  // before the next tile overwrites sc, pk, al, ks, vs
+    __syncthreads();  // before tile it + kStages refills this stage and sc, pk, al are rewritten
   }
 
-  // Sum the four warps' accumulators (the first K tile buffer is free now),
-  // then one division per element by the head's l.
-  float* acc = ks0;  // [4 warps][4 heads][64]
+  if (failed) {
+    // A tile did not land in time: record it and give the copies still in
+    // flight (tiles it .. it + kStages - 2) a bounded wait before the block's
+    // shared memory is released. The output is not written.
+    if (tid == 0) {
+      record_error(a.err, kDevErrTimeout);
+      const int last = min(ntiles - 1, it + kStages - 2);
+      for (int n = it; n <= last; ++n) tc::mbar_wait(&full[n % kStages], (n / kStages) & 1, kWaitNs);
+    }
+    return;
+  }
+
+  // Sum the four warps' accumulators (stage 0 is free: every tile issued has
+  // been waited for), then one division per element by the head's l.
+  float* acc = reinterpret_cast<float*>(dsm);  // [4 warps][4 heads][64]
 #pragma unroll
   for (int h = 0; h < kGroup; ++h)
     *reinterpret_cast<float2*>(acc + (warp * kGroup + h) * kD + 2 * lane) = make_float2(o[h][0], o[h][1]);
@@ -296,13 +349,94 @@ cudaError_t decode_scratch(float** ptr) {
   return cudaSuccess;
 }
 
-int decode_splits(int B, int max_context, int splits_hint, int num_sms, int* split_len) {
+namespace {
+
+// Per device: the shared-memory opt-in and how many split blocks fit at once.
+struct DecodeDevice {
+  bool ready = false;
+  int slots = 0;  // resident split blocks on the whole device
+};
+
+int decode_device(DecodeDevice** out) {
+  constexpr int kMaxDev = 64;
+  static std::mutex mu;
+  static DecodeDevice devs[kMaxDev];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return ATTN_ECUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  DecodeDevice& d = devs[dev];
+  if (!d.ready) {
+    int sms = 0, per_sm = 0;
+    if (cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSplitSmem) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_split_kernel, kThreads, kSplitSmem) !=
+            cudaSuccess)
+      return ATTN_ECUDA;
+    d.slots = sms * (per_sm > 0 ? per_sm : 1);
+    d.ready = true;
+  }
+  *out = &d;
+  return ATTN_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      ptr = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }();
+  return fn;
+}
+
+// A page pool [num_pages * 16][8][64] fp32 as the 2-D tensor (head * 64 + d,
+// row); a box is 32 floats (one 128-byte swizzle row) x the 16 rows of a page.
+int encode_page_pool(const float* base, int num_pages, CUtensorMap* map) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return ATTN_ETMA;
+  const cuuint32_t ones[2] = {1, 1};
+  const cuuint64_t dims[2] = {(cuuint64_t)kHKV * kD, (cuuint64_t)num_pages * ATTN_PAGE};
+  const cuuint64_t strides[1] = {(cuuint64_t)kHKV * kD * 4};
+  const cuuint32_t box[2] = {32, ATTN_PAGE};
+  if (enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, ones,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return ATTN_ETMA;
+  return ATTN_OK;
+}
+
+}  // namespace
+
+int decode_slots(int* slots) {
+  DecodeDevice* d = nullptr;
+  const int rc = decode_device(&d);
+  if (rc == ATTN_OK) *slots = d->slots;
+  return rc;
+}
+
+int decode_splits(int B, int max_context, int splits_hint, int slots, int* split_len) {
   int splits = splits_hint;
   if (splits <= 0) {
-    // Enough blocks for two waves of the SMs, segments of at least 256 keys.
-    const int want = (2 * num_sms + B * kHKV - 1) / (B * kHKV);
+    // Segments of at least 256 keys, as many as fill the resident blocks
+    // best: blocks / (waves x slots), less 0.04 for each extra wave.
+    const long long pairs = (long long)B * kHKV;
     const int most = (max_context + 255) / 256;
-    splits = want < most ? want : most;
+    const int top = most < 64 ? most : 64;
+    double best_score = -1.0;
+    splits = 1;
+    for (int s = 1; s <= top && slots > 0 && pairs > 0; ++s) {
+      const long long blocks = pairs * s;
+      const long long waves = (blocks + slots - 1) / slots;
+      const double score = (double)blocks / (double)(waves * slots) - 0.04 * (double)(waves - 1);
+      if (score > best_score + 1e-9) {
+        best_score = score;
+        splits = s;
+      }
+    }
   }
   if (splits < 1) splits = 1;
   const int per = (max_context + splits - 1) / splits;
@@ -315,28 +449,25 @@ size_t decode_workspace_bytes(int B, int splits) {
   return splits <= 1 ? 0 : (size_t)B * kHKV * splits * kPartFloats * sizeof(float);
 }
 
-cudaError_t launch_decode(const float* q, const float* k_pages, const float* v_pages, const int* table,
-                          const int* ctx_lens, float* out, float* parts, int B, int max_blocks, int num_pages,
-                          int max_context, int split_len, int splits, unsigned* err, cudaStream_t stream) {
-  static bool configured[64] = {};  // the shared-memory opt-in is per device
-  static std::mutex mu;
-  int dev = 0;
-  cudaError_t e0 = cudaGetDevice(&dev);
-  if (e0 != cudaSuccess) return e0;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!configured[dev]) {
-    e0 = cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSplitSmem);
-    if (e0 != cudaSuccess) return e0;
-    configured[dev] = true;
-  }
-  DecodeArgs a{q, k_pages, v_pages, table, ctx_lens, out, splits > 1 ? parts : nullptr,
+int launch_decode(const float* q, const float* k_pages, const float* v_pages, const int* table,
+                  const int* ctx_lens, float* out, float* parts, int B, int max_blocks, int num_pages,
+                  int max_context, int split_len, int splits, unsigned* err, cudaStream_t stream) {
+  DecodeDevice* d = nullptr;
+  int rc = decode_device(&d);
+  if (rc != ATTN_OK) return rc;
+  alignas(64) CUtensorMap mk, mv;
+  if ((rc = encode_page_pool(k_pages, num_pages, &mk)) != ATTN_OK ||
+      (rc = encode_page_pool(v_pages, num_pages, &mv)) != ATTN_OK)
+    return rc;
+  DecodeArgs a{q, table, ctx_lens, out, splits > 1 ? parts : nullptr,
                B, max_blocks, num_pages, max_context, split_len, splits, err};
-  decode_split_kernel<<<dim3(splits, kHKV, B), kThreads, kSplitSmem, stream>>>(a);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || splits <= 1) return e;
-  decode_merge_kernel<<<dim3(B, kHQ), kD, 0, stream>>>(a);
-  return cudaGetLastError();
+  decode_split_kernel<<<dim3(splits, kHKV, B), kThreads, kSplitSmem, stream>>>(mk, mv, a);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ELAUNCH;
+  if (splits > 1) {
+    decode_merge_kernel<<<dim3(B, kHQ), kD, 0, stream>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ELAUNCH;
+  }
+  return ATTN_OK;
 }
 
 }  // namespace attn

@@ -213,14 +213,16 @@ int attn_prefill_paged(const float *q, const float *kPages, const float *vPages,
  * that KV head, so each K/V row is read once per group; segments are merged
  * with m = max m_s, w_s = e^(m_s - m) l_s, out = sum w_s O_s / sum w_s (same
  * page, Flash-Decoding / split-K merge), skipping empty segments.
- * numSplits: segments per sequence, 0 = chosen from B, maxContext and the SM
- * count. With more than one segment the partials need `workspace`, a device
+ * numSplits: segments per sequence, 0 = chosen from B, maxContext and how many
+ * split blocks the device holds at once (segments of at least 256 keys, as
+ * many as fill those slots best). With more than one segment the partials need `workspace`, a device
  * buffer of at least attn_decode_workspace_bytes(B, maxContext, numSplits)
  * bytes, 16-byte aligned, owned by the caller, overwritten by the call, not
  * used after the call's kernels finish. Errors: ATTN_EINVAL (NULL pointer,
  * negative size, maxBlocks or numPages < 1), ATTN_ERANGE (B > 65535,
  * maxContext > 16 * maxBlocks, sizes above ATTN_MAX_TOKENS), ATTN_EALIGN,
- * ATTN_ESPACE (workspace missing or too small). A context length outside
+ * ATTN_ESPACE (workspace missing or too small), ATTN_ETMA (the page pools'
+ * tensor maps could not be encoded). A context length outside
  * [0, maxContext] or a page index outside [0, numPages) is recorded as
  * ATTN_EBOUNDS in the device error word and clamped / read as zeros. B == 0 is
  * a no-op.
