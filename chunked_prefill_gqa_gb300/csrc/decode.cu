@@ -380,6 +380,8 @@ int decode_device(DecodeDevice** out) {
   return ATTN_OK;
 }
 
+// The driver's tensor-map encoder, looked up once (a function-local static is
+// initialised once even when the first calls come from several threads).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void* ptr = nullptr;
