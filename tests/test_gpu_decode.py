@@ -113,3 +113,34 @@ def test_workspace_and_bounds_errors(cp):
     cp.attn_decode_paged(q, kp, vp, tb, cl, out, 500, 4, ws[: cp.attn_decode_workspace_bytes(2, 500, 4) // 4 + 4])
     assert cp.attn_get_device_error() == cp.ATTN_EBOUNDS
     assert cp.attn_get_device_error() == 0
+
+
+@pytest.mark.parametrize("splits", [0, 1, 3])
+def test_table_entry_out_of_range_reads_zeros(cp, splits):
+    """A block-table entry outside [0, numPages) is recorded as ATTN_EBOUNDS and
+    its 16 tokens read as zero keys and values (scores 0, no value), as the
+    header states; the next call on the same context is correct again."""
+    batch = W.decode_batch([40, 300], seed=12)
+    n_pages = batch.k_pages.shape[0]
+    table = batch.table.copy()
+    table[0, 1] = n_pages + 5   # tokens 16..31 of sequence 0
+    table[1, 7] = -7            # tokens 112..127 of sequence 1
+    want = np.zeros(batch.q.shape, dtype=np.float64)
+    for b, T in enumerate(batch.ctx.tolist()):
+        k = np.zeros((T, W.HKV, W.D), dtype=np.float32)
+        v = np.zeros((T, W.HKV, W.D), dtype=np.float32)
+        for t in range(T):
+            page = table[b, t // W.PAGE]
+            if 0 <= page < n_pages:
+                k[t] = batch.k_pages[page, t % W.PAGE]
+                v[t] = batch.v_pages[page, t % W.PAGE]
+        want[b] = oracle.attention(batch.q[b:b + 1], k, v, T - 1)[0]
+    bad = W.DecodeBatch(q=batch.q, k_pages=batch.k_pages, v_pages=batch.v_pages, table=table, ctx=batch.ctx)
+    assert cp.attn_get_device_error() == 0
+    got, _ = run_decode(cp, bad, splits)
+    assert cp.attn_get_device_error() == cp.ATTN_EBOUNDS
+    assert cp.attn_get_device_error() == 0
+    check(got, want, f"bad table entries, splits={splits}")
+    got, _ = run_decode(cp, batch, splits)
+    assert cp.attn_get_device_error() == 0
+    check(got, reference(batch), "after a bounds error")
