@@ -42,7 +42,8 @@ EXPORTS = ("attn_prefill", "attn_prefill_bf16x3", "attn_prefill_bf16kv", "attn_p
            "attn_prefill_bf16x3_host", "attn_prefill_bf16kv_host", "attn_full_causal", "attn_prefill_paged", "attn_decode_paged",
            "attn_decode_workspace_bytes", "attn_decode_paged_noalloc",
            "attn_naive_workspace_bytes", "attn_naive_scores", "attn_naive_softmax", "attn_naive_weighted_sum",
-           "attn_naive_prefill", "attn_prefill_ffma", "attn_reference_prefill", "attn_selftest_timeout", "attn_get_device_error", "attn_strerror", "attn_version")
+           "attn_naive_prefill", "attn_prefill_ffma", "attn_reference_prefill", "attn_selftest_timeout",
+           "attn_selftest_decode_timeout", "attn_get_device_error", "attn_strerror", "attn_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -82,8 +83,10 @@ def load():
                 fn.argtypes = [vp] * 8 + [ci, ci, vp]
             lib.attn_prefill_paged.restype = ci
             lib.attn_prefill_paged.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, vp]
-            lib.attn_decode_paged.restype = ci
-            lib.attn_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, vp, ctypes.c_size_t, vp]
+            for name in ("attn_decode_paged", "attn_selftest_decode_timeout"):
+                fn = getattr(lib, name)
+                fn.restype = ci
+                fn.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, vp, ctypes.c_size_t, vp]
             lib.attn_decode_paged_noalloc.restype = ci
             lib.attn_decode_paged_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, vp]
             lib.attn_decode_workspace_bytes.restype = ctypes.c_size_t
@@ -302,15 +305,28 @@ def attn_decode_paged(q, kPages, vPages, blockTable, contextLens, out, max_conte
         raise ValueError("blockTable must be an int32 CUDA tensor [B][maxBlocks]")
     if contextLens.dtype != torch.int32 or not contextLens.is_cuda or contextLens.numel() != B:
         raise ValueError("contextLens must be an int32 CUDA tensor [B]")
-    blockTable = blockTable.contiguous()
+    return _decode_call("attn_decode_paged", q, kPages, vPages, blockTable.contiguous(), contextLens, out,
+                        max_context, num_splits, workspace, stream)
+
+
+def _decode_call(name, q, kPages, vPages, blockTable, contextLens, out, max_context, num_splits, workspace, stream):
     ws_ptr = None if workspace is None else workspace.data_ptr()
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = load().attn_decode_paged(_ptr(q), _ptr(kPages), _ptr(vPages), _ptr(blockTable), _ptr(contextLens),
-                                  _ptr(out), B, blockTable.shape[1], kPages.shape[0], int(max_context),
-                                  int(num_splits), ws_ptr, ws_bytes, _stream_handle(stream))
+    rc = getattr(load(), name)(_ptr(q), _ptr(kPages), _ptr(vPages), _ptr(blockTable), _ptr(contextLens),
+                               _ptr(out), q.shape[0], blockTable.shape[1], kPages.shape[0], int(max_context),
+                               int(num_splits), ws_ptr, ws_bytes, _stream_handle(stream))
     if rc != ATTN_OK:
-        raise AttnError(rc, "attn_decode_paged")
+        raise AttnError(rc, name)
     return out
+
+
+def attn_selftest_decode_timeout(q, kPages, vPages, blockTable, contextLens, out, max_context: int,
+                                 num_splits: int = 0, workspace=None, stream=None):
+    """Failure-path test of the decode kernel (arguments as attn_decode_paged):
+    every block's first K/V tile is withheld, its wait expires after 20 ms and
+    ATTN_ETIMEOUT is recorded; read it with attn_get_device_error()."""
+    return _decode_call("attn_selftest_decode_timeout", q, kPages, vPages, blockTable.contiguous(), contextLens, out,
+                        max_context, num_splits, workspace, stream)
 
 
 def _check_decode_args(q, kPages, vPages, blockTable, contextLens, out):

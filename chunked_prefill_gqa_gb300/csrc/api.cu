@@ -298,10 +298,11 @@ extern "C" size_t attn_decode_workspace_bytes(int B, int maxContext, int numSpli
   return decode_workspace_bytes(B, splits);
 }
 
-extern "C" int attn_decode_paged(const float* q, const float* kPages, const float* vPages,
-                                 const int* blockTable, const int* contextLens, float* out, int B,
-                                 int maxBlocks, int numPages, int maxContext, int numSplits, void* workspace,
-                                 size_t workspaceBytes, cudaStream_t stream) {
+namespace attn {
+namespace {
+int decode_paged(const float* q, const float* kPages, const float* vPages, const int* blockTable,
+                 const int* contextLens, float* out, int B, int maxBlocks, int numPages, int maxContext,
+                 int numSplits, void* workspace, size_t workspaceBytes, cudaStream_t stream, int fault) {
   int rc = decode_shape_ok(B, maxBlocks, numPages, maxContext, numSplits);
   if (rc != ATTN_OK || B == 0) return rc;
   if (!q || !kPages || !vPages || !blockTable || !contextLens || !out) return ATTN_EINVAL;
@@ -321,7 +322,26 @@ extern "C" int attn_decode_paged(const float* q, const float* kPages, const floa
     if (!aligned16(workspace)) return ATTN_EALIGN;
   }
   return launch_decode(q, kPages, vPages, blockTable, contextLens, out, static_cast<float*>(workspace), B, maxBlocks,
-                       numPages, maxContext, split_len, splits, st->err, stream);
+                       numPages, maxContext, split_len, splits, st->err, stream, fault);
+}
+}  // namespace
+}  // namespace attn
+
+extern "C" int attn_decode_paged(const float* q, const float* kPages, const float* vPages,
+                                 const int* blockTable, const int* contextLens, float* out, int B,
+                                 int maxBlocks, int numPages, int maxContext, int numSplits, void* workspace,
+                                 size_t workspaceBytes, cudaStream_t stream) {
+  return decode_paged(q, kPages, vPages, blockTable, contextLens, out, B, maxBlocks, numPages, maxContext, numSplits,
+                      workspace, workspaceBytes, stream, 0);
+}
+
+extern "C" int attn_selftest_decode_timeout(const float* q, const float* kPages, const float* vPages,
+                                            const int* blockTable, const int* contextLens, float* out, int B,
+                                            int maxBlocks, int numPages, int maxContext, int numSplits,
+                                            void* workspace, size_t workspaceBytes, cudaStream_t stream) {
+  if (B < 1 || maxContext < 1) return ATTN_EINVAL;  // no tile, nothing to withhold
+  return decode_paged(q, kPages, vPages, blockTable, contextLens, out, B, maxBlocks, numPages, maxContext, numSplits,
+                      workspace, workspaceBytes, stream, 1);
 }
 
 extern "C" int attn_decode_paged_noalloc(const float* q, const float* kPages, const float* vPages,

@@ -55,9 +55,11 @@ int launch_tc_fault_test(const Problem& p, cudaStream_t stream);  // skips a loa
 int decode_slots(int* slots);
 int decode_splits(int B, int max_context, int splits_hint, int slots, int* split_len);
 size_t decode_workspace_bytes(int B, int splits);
+// fault != 0 (failure-path test): the first tile of every block is never
+// loaded and every wait is limited to 20 ms (2 s otherwise).
 int launch_decode(const float* q, const float* k_pages, const float* v_pages, const int* table,
                   const int* ctx_lens, float* out, float* parts, int B, int max_blocks, int num_pages,
-                  int max_context, int split_len, int splits, unsigned* err, cudaStream_t stream);
+                  int max_context, int split_len, int splits, unsigned* err, cudaStream_t stream, int fault = 0);
 // Three-kernel score-matrix attention (naive.cu): workspace bytes, the row
 // limit of its grids, and one launcher per kernel.
 size_t naive_workspace_bytes(int C, int P);

@@ -41,7 +41,6 @@ constexpr int kHalfBytes = kTile * 128;        // 32 of the 64 dims of 64 rows, 
 constexpr int kBoxBytes = ATTN_PAGE * 128;     // one page's rows of one d-half: a TMA box
 constexpr int kStageBytes = 4 * kHalfBytes;    // K d-halves 0, 1, then V d-halves 0, 1 (32 KB)
 constexpr int kPartFloats = kGroup * kD + 2 * kGroup;  // O_s for 4 heads, then m_s[4], l_s[4]
-constexpr unsigned long long kWaitNs = 2000000000ull;  // a tile that has not landed after 2 s is a fault
 constexpr int kSkip = -2147483647 - 1;         // "no page": the tile's rows past the segment
 
 // Shared memory: the ring (1024-byte aligned for the swizzle), then q [4][64],
@@ -66,6 +65,8 @@ struct DecodeArgs {
   float* parts;            // [B][8][splits][kPartFloats], or nullptr when splits == 1
   int B, max_blocks, num_pages, max_context, split_len, splits;
   unsigned* err;
+  unsigned long long timeout_ns;  // a tile that has not landed by then is a fault
+  int fault_skip_first;           // test hook: post the first tile's bytes, never load it
 };
 
 // mk, mv: the K and V page pools [num_pages * 16][8][64] as 2-D tensors
@@ -133,7 +134,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constan
     const unsigned npg = __popc(__ballot_sync(0xffffffffu, has));
     if (lane == 0) tc::mbar_arrive_expect_tx(&full[st], npg * 4u * kBoxBytes);
     __syncwarp();
-    if (has) {
+    if (has && !(a.fault_skip_first && n == 0)) {
       int y = pg;
       if (pg < 0 || pg >= a.num_pages) {
         record_error(a.err, kDevErrBounds);
@@ -174,7 +175,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constan
       issue(it + kStages - 1, pg_next);
       pg_next = page_of(it + kStages);  // its latency is spent on this tile's work
     }
-    const bool ok = tc::mbar_wait(&full[st], (it / kStages) & 1, kWaitNs);
+    const bool ok = tc::mbar_wait(&full[st], (it / kStages) & 1, a.timeout_ns);
     if (__syncthreads_or(!ok)) {
       failed = true;
       break;
@@ -253,12 +254,13 @@ decode_split_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constan
 
   if (failed) {
     // A tile did not land in time: record it and give the copies still in
-    // flight (tiles it .. it + kStages - 2) a bounded wait before the block's
-    // shared memory is released. The output is not written.
+    // flight (tiles it .. it + kStages - 1: the last was issued before the
+    // wait) a bounded wait before the block's shared memory is released. The
+    // output is not written.
     if (tid == 0) {
       record_error(a.err, kDevErrTimeout);
-      const int last = min(ntiles - 1, it + kStages - 2);
-      for (int n = it; n <= last; ++n) tc::mbar_wait(&full[n % kStages], (n / kStages) & 1, kWaitNs);
+      const int last = min(ntiles - 1, it + kStages - 1);
+      for (int n = it; n <= last; ++n) tc::mbar_wait(&full[n % kStages], (n / kStages) & 1, a.timeout_ns);
     }
     return;
   }
@@ -453,7 +455,7 @@ size_t decode_workspace_bytes(int B, int splits) {
 
 int launch_decode(const float* q, const float* k_pages, const float* v_pages, const int* table,
                   const int* ctx_lens, float* out, float* parts, int B, int max_blocks, int num_pages,
-                  int max_context, int split_len, int splits, unsigned* err, cudaStream_t stream) {
+                  int max_context, int split_len, int splits, unsigned* err, cudaStream_t stream, int fault) {
   DecodeDevice* d = nullptr;
   int rc = decode_device(&d);
   if (rc != ATTN_OK) return rc;
@@ -462,7 +464,8 @@ int launch_decode(const float* q, const float* k_pages, const float* v_pages, co
       (rc = encode_page_pool(v_pages, num_pages, &mv)) != ATTN_OK)
     return rc;
   DecodeArgs a{q, table, ctx_lens, out, splits > 1 ? parts : nullptr,
-               B, max_blocks, num_pages, max_context, split_len, splits, err};
+               B, max_blocks, num_pages, max_context, split_len, splits, err,
+               fault ? 20000000ull : 2000000000ull, fault};
   decode_split_kernel<<<dim3(splits, kHKV, B), kThreads, kSplitSmem, stream>>>(mk, mv, a);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ELAUNCH;
   if (splits > 1) {

@@ -343,6 +343,21 @@ int attn_selftest_timeout(const float *q, const float *kCache, const float *vCac
                           int C, int P, cudaStream_t stream);
 
 /*
+ * attn_selftest_decode_timeout -- the same test for the decode kernel: the
+ * arguments, checks and workspace of attn_decode_paged, but every split block
+ * posts the bytes of its first K/V tile without ever loading it and every
+ * bounded wait is limited to 20 ms, so each block's wait expires; the block
+ * records ATTN_ETIMEOUT, gives the copies it did issue a bounded wait and
+ * returns without writing. `out` is left unspecified and the context stays
+ * usable. Requires B >= 1 and maxContext >= 1 (ATTN_EINVAL otherwise); a
+ * sequence with context 0 has no tile and returns normally.
+ */
+int attn_selftest_decode_timeout(const float *q, const float *kPages, const float *vPages, const int *blockTable,
+                                 const int *contextLens, float *out, int B, int maxBlocks, int numPages,
+                                 int maxContext, int numSplits, void *workspace, size_t workspaceBytes,
+                                 cudaStream_t stream);
+
+/*
  * attn_get_device_error -- synchronises the current device, then returns and
  * clears the device-side error word: 0, ATTN_ETIMEOUT or ATTN_EBOUNDS (the
  * first fault recorded since the last call), or ATTN_ECUDA if the

@@ -43,3 +43,35 @@ def test_expired_wait_is_reported_and_context_survives(cp):
 def test_selftest_rejects_empty_chunk(cp):
     f = cp.raw("attn_selftest_timeout")
     assert f(None, None, None, None, 0, 0, None) == cp.ATTN_EINVAL
+
+
+@pytest.mark.parametrize("splits", [1, 3])
+def test_decode_expired_wait_is_reported_and_context_survives(cp, splits):
+    """The decode kernel's bounded wait: every block's first tile is withheld,
+    each block records ATTN_ETIMEOUT and returns; the next decode is correct."""
+    assert cp.attn_get_device_error() == 0
+    batch = W.decode_batch([300, 1000], seed=21)
+    q = torch.from_numpy(batch.q).cuda()
+    kp = torch.from_numpy(batch.k_pages).cuda()
+    vp = torch.from_numpy(batch.v_pages).cuda()
+    tb = torch.from_numpy(batch.table).cuda()
+    cl = torch.from_numpy(batch.ctx).cuda()
+    out = torch.empty_like(q)
+    nbytes = cp.attn_decode_workspace_bytes(2, batch.max_context, splits)
+    ws = torch.empty(max(nbytes, 16) // 4, dtype=torch.float32, device="cuda")
+    cp.attn_selftest_decode_timeout(q, kp, vp, tb, cl, out, batch.max_context, splits, ws)
+    assert cp.attn_get_device_error() == cp.ATTN_ETIMEOUT
+    assert cp.attn_get_device_error() == 0
+    cp.attn_decode_paged(q, kp, vp, tb, cl, out, batch.max_context, splits, ws)
+    got = out.cpu().numpy()
+    assert cp.attn_get_device_error() == 0
+    for b, T in enumerate(batch.ctx.tolist()):
+        k = oracle.gather_pages(batch.k_pages, batch.table[b], T)
+        v = oracle.gather_pages(batch.v_pages, batch.table[b], T)
+        rep = oracle.check(got[b], oracle.attention(batch.q[b:b + 1], k, v, T - 1)[0])
+        assert rep["n_bad"] == 0, rep
+
+
+def test_decode_selftest_rejects_empty_batch(cp):
+    f = cp.raw("attn_selftest_decode_timeout")
+    assert f(None, None, None, None, None, None, 0, 1, 1, 16, 0, None, 0, None) == cp.ATTN_EINVAL
