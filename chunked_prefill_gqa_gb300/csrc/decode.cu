@@ -148,9 +148,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constan
     }
   };
 
-  // Score layout: thread (key = tid % 64, head pair = tid / 64).
-  const int skey = tid & 63, hp = (tid >> 6) * 2;
-  // Softmax: warp = head (m and l live in warp `warp`'s registers for head `warp`).
+  // Scores and the online update: warp h is query head h and lane l scores
+  // keys l and l + 32 of the tile, so the scores stay in registers.
   // Weighted sum: warp w takes keys 16 w .. 16 w + 15 of every tile for all four
   // heads, lane = head dims 2 lane, 2 lane + 1; the four warps' sums share each
   // head's reference maximum and are added at the end.
@@ -176,36 +175,27 @@ decode_split_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constan
       pg_next = page_of(it + kStages);  // its latency is spent on this tile's work
     }
     const bool ok = tc::mbar_wait(&full[st], (it / kStages) & 1, a.timeout_ns);
-    if (__syncthreads_or(!ok)) {
-      failed = true;
-      break;
-    }
     const uint8_t* kt = dsm + st * kStageBytes;
     const uint8_t* vt = kt + 2 * kHalfBytes;
 
-    // Scores of this thread's key against two query heads, scale 1/8.
+    // Scores of keys `lane` and `lane + 32` against head `warp`, scale 1/8,
+    // then the head's tile maximum, alpha and probabilities. Keys past the
+    // segment read whatever the page slot holds (NaN included) and get score
+    // -inf. (After an expired wait the values are garbage; nothing is stored
+    // from them.)
     {
       float d0 = 0.f, d1 = 0.f;
 #pragma unroll
       for (int d4 = 0; d4 < kD / 4; ++d4) {
-        const float4 kv =
-            *reinterpret_cast<const float4*>(kt + (d4 >> 3) * kHalfBytes + swz(skey, (d4 & 7) * 4));
-        const float4 qa = *reinterpret_cast<const float4*>(&qs[hp][d4 * 4]);
-        const float4 qb = *reinterpret_cast<const float4*>(&qs[hp + 1][d4 * 4]);
-        d0 = fmaf(qa.x, kv.x, fmaf(qa.y, kv.y, fmaf(qa.z, kv.z, fmaf(qa.w, kv.w, d0))));
-        d1 = fmaf(qb.x, kv.x, fmaf(qb.y, kv.y, fmaf(qb.z, kv.z, fmaf(qb.w, kv.w, d1))));
+        const float4 qa = *reinterpret_cast<const float4*>(&qs[warp][d4 * 4]);
+        const uint8_t* kh = kt + (d4 >> 3) * kHalfBytes;
+        const float4 ka = *reinterpret_cast<const float4*>(kh + swz(lane, (d4 & 7) * 4));
+        const float4 kb = *reinterpret_cast<const float4*>(kh + swz(lane + 32, (d4 & 7) * 4));
+        d0 = fmaf(qa.x, ka.x, fmaf(qa.y, ka.y, fmaf(qa.z, ka.z, fmaf(qa.w, ka.w, d0))));
+        d1 = fmaf(qa.x, kb.x, fmaf(qa.y, kb.y, fmaf(qa.z, kb.z, fmaf(qa.w, kb.w, d1))));
       }
-      // Keys past the segment read whatever the page slot holds (NaN included).
-      const bool valid = t0 + skey < k1;
-      sc[hp][skey] = valid ? d0 * kScale : -INFINITY;
-      sc[hp + 1][skey] = valid ? d1 * kScale : -INFINITY;
-    }
-    __syncthreads();
-
-    // Online update for head `warp`: tile max, alpha, probabilities.
-    {
-      const int h = warp;
-      const float s0 = sc[h][lane], s1 = sc[h][lane + 32];
+      const float s0 = t0 + lane < k1 ? d0 * kScale : -INFINITY;
+      const float s1 = t0 + lane + 32 < k1 ? d1 * kScale : -INFINITY;
       float mx = fmaxf(s0, s1);
 #pragma unroll
       for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
@@ -217,11 +207,15 @@ decode_split_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constan
       for (int off = 16; off >= 1; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
       l = fmaf(l, alpha, ps);
       m = mnew;
-      pk[lane][h] = p0;
-      pk[lane + 32][h] = p1;
-      if (lane == 0) al[h] = alpha;
+      pk[lane][warp] = p0;
+      pk[lane + 32][warp] = p1;
+      if (lane == 0) al[warp] = alpha;
     }
-    __syncthreads();
+    // Every thread's wait either succeeded or it gives up with the others.
+    if (__syncthreads_or(!ok)) {
+      failed = true;
+      break;
+    }
 
     // O_w += P V over this warp's 16 keys, all four heads. A key past the
     // segment is skipped, not weighted by zero: its slot may hold NaN.
