@@ -291,11 +291,17 @@ decode_split_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constan
       }
     }
   }
+  // This block's partial is written: the merge grid may be scheduled (it
+  // still waits for this whole grid to finish before reading any partial).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // One block per (sequence, query head); thread d owns head dimension d.
 __global__ void __launch_bounds__(kD)
 decode_merge_kernel(DecodeArgs a) {
+  // Launched as a programmatic dependent of the split kernel: wait until that
+  // grid has completed and its partials are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int b = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
   const int g = h / kGroup, hl = h % kGroup;
   const float* base = a.parts + ((size_t)b * kHKV + g) * a.splits * kPartFloats;
@@ -463,8 +469,18 @@ int launch_decode(const float* q, const float* k_pages, const float* v_pages, co
   decode_split_kernel<<<dim3(splits, kHKV, B), kThreads, kSplitSmem, stream>>>(mk, mv, a);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ELAUNCH;
   if (splits > 1) {
-    decode_merge_kernel<<<dim3(B, kHQ), kD, 0, stream>>>(a);
-    if (cudaGetLastError() != cudaSuccess) return ATTN_ELAUNCH;
+    // The merge starts as soon as every split block has written its partial
+    // (programmatic dependent launch) instead of after the split grid drains.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(B, kHQ);
+    cfg.blockDim = dim3(kD);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, decode_merge_kernel, a) != cudaSuccess) return ATTN_ELAUNCH;
   }
   return ATTN_OK;
 }
