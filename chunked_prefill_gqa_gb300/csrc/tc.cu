@@ -214,6 +214,10 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&r)[64]) {
   tmem_ld32(taddr + 32, *reinterpret_cast<float(*)[32]>(&r[32]));
 }
 
+// kPagedOnly: the instantiation for page pools, which carries no contiguous-
+// cache code; the other one decides by prm.table at run time (it is the one
+// launched for contiguous caches; measured, dropping its paged branch slows it).
+template <bool kPagedOnly>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
           const Params prm) {
@@ -285,7 +289,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
           uint8_t* dst = is_k ? smem + kSmemK + st * kKStageBytes : smem + kSmemVRaw + st * kVRawBytes;
           const uint32_t half_stride = is_k ? kRegion : kHalf;  // d-half regions
           mbar_arrive_expect_tx(full, 2 * kHalf);
-          if (prm.table == nullptr) {
+          if (!kPagedOnly && prm.table == nullptr) {
             tma_load_2d(dst, map, full, w.g * kD, j * kBc);
             tma_load_2d(dst + half_stride, map, full, w.g * kD + 32, j * kBc);
           } else {
@@ -708,8 +712,10 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
     if (!st.ready) {
       if (cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return ATTN_ECUDA;
-      if (cudaFuncSetAttribute(tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc) !=
-          cudaSuccess)
+      if (cudaFuncSetAttribute(tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc) !=
+              cudaSuccess ||
+          cudaFuncSetAttribute(tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc) !=
+              cudaSuccess)
         return ATTN_ECUDA;
       st.ready = true;
     }
@@ -730,7 +736,10 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
   prm.table = table;
   prm.num_pages = num_pages;
   const int grid = prm.n_units < num_sms ? prm.n_units : num_sms;
-  tc_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(mk, mv, prm);
+  if (table)
+    tc_kernel<true><<<grid, kThreads, kSmemAlloc, stream>>>(mk, mv, prm);
+  else
+    tc_kernel<false><<<grid, kThreads, kSmemAlloc, stream>>>(mk, mv, prm);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ELAUNCH;
 }
 
