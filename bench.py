@@ -208,6 +208,20 @@ def kernel_source_hash(path_name: str) -> str:
     return hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
 
 
+def launches_per_call(path: str, C: int) -> int:
+    """Kernel launches in one call of `path` on C chunk rows. The split-TF32
+    path (contiguous or paged) adds a second grid for the last round's units
+    when that round would leave more than half of the SMs idle: the library's
+    own rule, on 32-row query tiles x 8 KV heads."""
+    if path != "attn_prefill":
+        return 1
+    units = -(-C // 32) * 8
+    grid = min(units, NUM_SMS)
+    full = units // grid * grid
+    rem = units - full
+    return 2 if full > 0 and rem > 0 and 2 * rem <= (NUM_SMS & ~1) else 1
+
+
 def profiled_traffic(path_name: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel source; otherwise None."""
@@ -613,13 +627,18 @@ def main():
             ee[i].record(stream)
         torch.cuda.synchronize()
         e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in zip(es, ee)), dev) / n_e2e
-        ok = np.array_equal(hout.numpy().view(np.uint32), out.cpu().numpy().view(np.uint32))
+        # The host path runs the chunk as sub-chunks; the device call may split
+        # its last round's units over CTA pairs (another summation order), so
+        # the two agree to rounding, far inside the oracle's tolerance.
+        dev_out = out.cpu().numpy()
+        diff = float(np.max(np.abs(hout.numpy() - dev_out)))
+        ok = bool(np.allclose(hout.numpy(), dev_out, rtol=1e-5, atol=1e-6))
         e2e = {"value": world * flops / (e_ms * 1e-3) / 1e12, "unit": UNIT,
                "ms_per_step": e_ms, "steps": n_e2e,
                "h2d_bytes_per_step": int(hq.numel() * 4 + (hk.numel() + hv.numel()) * hk.element_size()),
                "d2h_bytes_per_step": int(hout.numel()) * 4,
                "api": (args.path + "_host") if host_fn is not None else f"copies + {args.path}",
-               "matches_device_timed_output": bool(ok)}
+               "matches_device_timed_output": ok, "max_abs_diff_vs_device_timed_output": diff}
 
     compare = None
     if not args.no_compare and rank == 0 and args.kv == "fp32" and not args.paged:
@@ -675,7 +694,7 @@ def main():
                                  args.workload + ("-paged" if args.paged else "")),
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * launches_per_call(args.path, C),
             "clocks": sampler.summary(t_begin, t_end),
             "wall_s_timed_region": round(wall, 4),
         }

@@ -97,8 +97,9 @@ constexpr uint32_t kSmemK = kSmemQ + 2 * kQTermBytes;
 constexpr uint32_t kSmemVRaw = kSmemK + kKStages * kKStageBytes;
 constexpr uint32_t kSmemVT = kSmemVRaw + kVRawStages * kVRawBytes;
 constexpr uint32_t kSmemBar = kSmemVT + kVStages * kVStageBytes;
-constexpr uint32_t kNumBars = 3 * kKStages + 2 * kVRawStages + 2 * kVStages + 3 * kNumS + 1 + 2;
-constexpr uint32_t kSmemTotal = kSmemBar + kNumBars * 8 + 16;
+constexpr uint32_t kNumBars = 3 * kKStages + 2 * kVRawStages + 2 * kVStages + 3 * kNumS + 1 + 2 + 2;
+constexpr uint32_t kSmemSlot = kSmemBar + kNumBars * 8 + 16;  // tail kernel: rank 1's m and l per row
+constexpr uint32_t kSmemTotal = kSmemSlot + 2 * kM * 4;
 constexpr uint32_t kSmemAlloc = kSmemTotal + 1024;  // slack to align the base
 
 static_assert(kSmemAlloc <= 232448, "exceeds the 227 KB per-block shared memory limit");
@@ -122,6 +123,7 @@ struct Params {
   // contiguous [P + C][8][64] caches.
   const int* table;
   int num_pages;
+  int unit_base;  // tail kernel: pair p splits unit unit_base + p
 };
 
 constexpr int kPage = 16;  // tokens per page of a paged cache
@@ -139,6 +141,8 @@ struct Bars {
   uint64_t* odone;   // [kNumS] PV(n) done, barrier n % 3 (MMA commit)
   uint64_t* qready;  // Q hi/lo in shared memory (softmax warps)
   uint64_t* drain;   // [2] drain of each MMA issuer on abort (QK, PV)
+  uint64_t* partner;   // tail kernel, rank 0: rank 1's share of the unit is in place (128 remote arrivals)
+  uint64_t* slotfree;  // tail kernel, rank 1: rank 0 has taken it (128 remote arrivals)
 };
 
 __device__ __forceinline__ Bars carve_bars(uint8_t* base) {
@@ -156,6 +160,8 @@ __device__ __forceinline__ Bars carve_bars(uint8_t* base) {
   r.odone = b; b += kNumS;
   r.qready = b++;
   r.drain = b; b += 2;
+  r.partner = b++;
+  r.slotfree = b++;
   return r;
 }
 
@@ -203,10 +209,95 @@ __device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity, co
   return __all_sync(0xffffffffu, ok);
 }
 
+// As wait_bar_warp, for a barrier the partner CTA arrives on: the wait
+// acquires at cluster scope, so the partner's released writes are visible.
+__device__ __forceinline__ bool wait_bar_cluster_warp(uint64_t* bar, uint32_t parity, const Params& prm,
+                                                      volatile int* abort_flag) {
+  bool ok = mbar_try_wait_cluster(bar, parity);
+  if (!ok) {
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+      if (mbar_try_wait_cluster(bar, parity)) {
+        ok = true;
+        break;
+      }
+      if (*abort_flag) break;
+      if (globaltimer_ns() - t0 > prm.timeout_ns) {
+        record_error(prm.p.err, kDevErrTimeout);
+        *abort_flag = 1;
+        break;
+      }
+    }
+  }
+  return __all_sync(0xffffffffu, ok);
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Epilogue of a unit split over the CTA pair, for one softmax thread (row).
+// Each CTA holds O (the two stacked halves of O' added), m and l of its own
+// key tiles relative to its own reference maximum (none when it got no tile).
+// Rank 1 writes its normalised share to the output row and sends m and l to
+// rank 0's slot; rank 0 merges, m = max(m0, m1) with weights e^(m_s - m)
+// (in log2 units, (m_s - m) c), one division per element. `mu` counts the
+// CTA's earlier split units (the slot's phase). Kept out of line: it runs
+// once per CTA at most and stays out of the hot loop's code.
+__device__ __noinline__ bool split_epilogue(uint32_t lane_tmem, int n, bool has, const Bars& bars, const Params& prm,
+                                            volatile int* abort_flag, float* slot, uint32_t rank, int row,
+                                            float m_ref, float l, float c, bool store, float* dst, uint32_t mu) {
+  float o[64];
+  if (has) {
+    const int pb = (n - 1) % kNumS;
+    if (!wait_bar_warp(&bars.odone[pb], ((n - 1) / kNumS) & 1, prm, abort_flag)) return false;
+    tc_fence_after();
+#pragma unroll
+    for (int dh = 0; dh < 2; ++dh) {
+      float a[32], b[32];
+      tmem_ld32(lane_tmem + kColO + dh * 32, a);
+      tmem_ld32(lane_tmem + kColO + 64 + dh * 32, b);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) o[dh * 32 + i] = a[i] + b[i];
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 64; ++i) o[i] = 0.f;
+  }
+  const uint32_t peer = rank ^ 1u;
+  if (rank == 1) {
+    if (mu > 0 && !wait_bar_cluster_warp(bars.slotfree, (mu - 1) & 1, prm, abort_flag)) return false;
+    if (store) {
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+      for (int i = 0; i < 64; i += 4)
+        *reinterpret_cast<float4*>(dst + i) = make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
+    }
+    st_shared_cluster_f32(mapa_shared(smem_u32(slot + row), peer), m_ref);
+    st_shared_cluster_f32(mapa_shared(smem_u32(slot + kM + row), peer), l);
+    mbar_arrive_remote(mapa_shared(smem_u32(bars.partner), peer));
+  } else {
+    if (!wait_bar_cluster_warp(bars.partner, mu & 1, prm, abort_flag)) return false;
+    const float m1 = slot[row], l1 = slot[kM + row];
+    const float m = fmaxf(l > 0.f ? m_ref : -INFINITY, l1 > 0.f ? m1 : -INFINITY);
+    const float e0 = l > 0.f ? ex2((m_ref - m) * c) : 0.f;
+    const float w1 = l1 > 0.f ? ex2((m1 - m) * c) * l1 : 0.f;
+    const float inv = 1.f / fmaf(e0, l, w1);  // > 0: the unit sees at least key 0
+    if (store) {
+#pragma unroll
+      for (int i = 0; i < 64; i += 4) {
+        const float4 x1 = __ldcg(reinterpret_cast<const float4*>(dst + i));
+        *reinterpret_cast<float4*>(dst + i) =
+            make_float4(fmaf(e0, o[i], w1 * x1.x) * inv, fmaf(e0, o[i + 1], w1 * x1.y) * inv,
+                        fmaf(e0, o[i + 2], w1 * x1.z) * inv, fmaf(e0, o[i + 3], w1 * x1.w) * inv);
+      }
+    }
+    mbar_arrive_remote(mapa_shared(smem_u32(bars.slotfree), peer));
+  }
+  return true;
 }
 
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&r)[64]) {
@@ -214,10 +305,35 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&r)[64]) {
   tmem_ld32(taddr + 32, *reinterpret_cast<float(*)[32]>(&r[32]));
 }
 
-// kPagedOnly: the instantiation for page pools, which carries no contiguous-
-// cache code; the other one decides by prm.table at run time (it is the one
-// launched for contiguous caches; measured, dropping its paged branch slows it).
-template <bool kPagedOnly>
+// Instantiations. kMain: whole units in snake order; it decides by prm.table
+// at run time (it is the one launched for contiguous caches; measured,
+// dropping its paged branch slows it). kPaged: the same for page pools only.
+// kTail: launched after kMain as clusters of two CTAs; pair p splits unit
+// unit_base + p along its key tiles (rank 0 the first half, rank 1 the rest)
+// and merges the two online-softmax partials through distributed shared memory.
+constexpr int kMain = 0, kPaged = 1, kTail = 2;
+
+// Unit u's tiles for this CTA: all of them, or the tail kernel's half.
+template <int kMode>
+__device__ __forceinline__ void unit_range(const Unit& w, uint32_t rank, int* jb, int* je) {
+  if constexpr (kMode == kTail) {
+    *jb = rank == 0 ? 0 : w.ntiles / 2;
+    *je = rank == 0 ? w.ntiles / 2 : w.ntiles;
+  } else {
+    *jb = 0;
+    *je = w.ntiles;
+  }
+}
+
+// The CTA's k-th unit (kMain, kPaged: snake order; kTail: one per pair), or
+// n_units when it has none.
+template <int kMode>
+__device__ __forceinline__ int work_unit(int k, int cta, int grid, const Params& prm) {
+  if constexpr (kMode == kTail) return k == 0 ? prm.unit_base + (cta >> 1) : prm.n_units;
+  else return unit_index(k, cta, grid);
+}
+
+template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
           const Params prm) {
@@ -252,6 +368,10 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
     mbar_init(bars.qready, kSoftmaxWarps);
     mbar_init(&bars.drain[0], 1);
     mbar_init(&bars.drain[1], 1);
+    if constexpr (kMode == kTail) {
+      mbar_init(bars.partner, kSoftmaxWarps * 32);
+      mbar_init(bars.slotfree, kSoftmaxWarps * 32);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -265,6 +385,16 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  if constexpr (kMode == kTail) {
+    // Both CTAs of the pair are running and their barriers initialised before
+    // either can touch the other's shared memory.
+    cluster_sync_all();
+  } else {
+    // A tail launch after this one (a programmatic dependent) may start its
+    // blocks on SMs as soon as blocks of this grid leave them.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  }
+  const uint32_t rank = kMode == kTail ? cluster_ctarank() : 0u;
 
   const int cta = blockIdx.x, grid = gridDim.x;
   const Problem& p = prm.p;
@@ -276,10 +406,12 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
       const int stages = is_k ? kKStages : kVRawStages;
       int n = 0;
       for (int k = 0;; ++k) {
-        const int u = unit_index(k, cta, grid);
+        const int u = work_unit<kMode>(k, cta, grid, prm);
         if (u >= prm.n_units) break;
         const Unit w = decode_unit(u, prm);
-        for (int j = 0; j < w.ntiles; ++j, ++n) {
+        int jb, je;
+        unit_range<kMode>(w, rank, &jb, &je);
+        for (int j = jb; j < je; ++j, ++n) {
           const int st = n % stages;
           uint64_t* freed = is_k ? &bars.kempty[st] : &bars.vrfree[st];
           if (n >= stages && !wait_bar(freed, ((n / stages) - 1) & 1, prm, abort_flag)) goto producer_done;
@@ -289,7 +421,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
           uint8_t* dst = is_k ? smem + kSmemK + st * kKStageBytes : smem + kSmemVRaw + st * kVRawBytes;
           const uint32_t half_stride = is_k ? kRegion : kHalf;  // d-half regions
           mbar_arrive_expect_tx(full, 2 * kHalf);
-          if (!kPagedOnly && prm.table == nullptr) {
+          if (kMode != kPaged && prm.table == nullptr) {
             tma_load_2d(dst, map, full, w.g * kD, j * kBc);
             tma_load_2d(dst + half_stride, map, full, w.g * kD + 32, j * kBc);
           } else {
@@ -331,14 +463,19 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
     if (lane == 0) {
       int n = 0, lu = 0;
       for (int k = 0;; ++k) {
-        const int u = unit_index(k, cta, grid);
+        const int u = work_unit<kMode>(k, cta, grid, prm);
         if (u >= prm.n_units) break;
         const Unit w = decode_unit(u, prm);
+        int jb, je;
+        unit_range<kMode>(w, rank, &jb, &je);
+        if constexpr (kMode == kTail) {
+          if (jb == je) continue;  // no tiles here (its Q is not loaded either)
+        }
         if (is_qk) {
           if (!wait_bar(bars.qready, lu & 1, prm, abort_flag)) goto mma_done;
           tc_fence_after();
         }
-        for (int j = 0; j < w.ntiles; ++j, ++n) {
+        for (int j = jb; j < je; ++j, ++n) {
           if (is_qk) {
             // QK(n): K(n) converted; S buffer n % 3 free once PV(n-3) has read
             // P(n-3) from it (odone[n % 3] is at most one phase past PV(n-3):
@@ -371,7 +508,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
             const uint32_t vt = smem_u32(smem + kSmemVT + vs * kVStageBytes);
             const uint32_t phi = tmem + kColS + sb * 128;
             const uint32_t plo = phi + 64;
-            const bool first = j == 0;
+            const bool first = j == jb;
 #pragma unroll
             for (int s = 0; s < 8; ++s)  // [P_hi V_hi | P_hi V_lo]
               mma_tf32_ts(tmem + kColO, phi + s * 8, sdesc_sw128(vt + (s >> 2) * kRegion + (s & 3) * 32),
@@ -406,10 +543,12 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
     const int kc = warp - kFirstKConvWarp;
     int n = 0;
     for (int k = 0;; ++k) {
-      const int u = unit_index(k, cta, grid);
+      const int u = work_unit<kMode>(k, cta, grid, prm);
       if (u >= prm.n_units) break;
       const Unit w = decode_unit(u, prm);
-      for (int j = 0; j < w.ntiles; ++j, ++n) {
+      int jb, je;
+      unit_range<kMode>(w, rank, &jb, &je);
+      for (int j = jb; j < je; ++j, ++n) {
         const int ks = n % kKStages;
         if (!wait_bar_warp(&bars.kfull[ks], (n / kKStages) & 1, prm, abort_flag)) goto kconv_done;
         uint8_t* kb = smem + kSmemK + ks * kKStageBytes + kc * kRegion;
@@ -443,10 +582,12 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
     const int quarter = lane >> 3;
     int n = 0;
     for (int k = 0;; ++k) {
-      const int u = unit_index(k, cta, grid);
+      const int u = work_unit<kMode>(k, cta, grid, prm);
       if (u >= prm.n_units) break;
       const Unit w = decode_unit(u, prm);
-      for (int j = 0; j < w.ntiles; ++j, ++n) {
+      int jb, je;
+      unit_range<kMode>(w, rank, &jb, &je);
+      for (int j = jb; j < je; ++j, ++n) {
         const int vr = n % kVRawStages;
         const int vs = n % kVStages;
         if (!wait_bar_warp(&bars.vfull[vr], (n / kVRawStages) & 1, prm, abort_flag)) goto vconv_done;
@@ -529,15 +670,18 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
 
     bool q_loaded = false;
     for (int k = 0;; ++k) {
-      const int u = unit_index(k, cta, grid);
+      const int u = work_unit<kMode>(k, cta, grid, prm);
       if (u >= prm.n_units) break;
       const Unit w = decode_unit(u, prm);
-      if (!q_loaded) load_q(w);
+      int jb, je;
+      unit_range<kMode>(w, rank, &jb, &je);
+      const bool has = jb < je;
+      if (has && !q_loaded) load_q(w);
       q_loaded = false;
       float m_ref = -INFINITY, l = 0.f;
       const int pos = w.t0 + (row >> 2);
       const int limit = p.P + pos;  // last visible key of this row
-      for (int j = 0; j < w.ntiles; ++j, ++n) {
+      for (int j = jb; j < je; ++j, ++n) {
         const int j0 = j * kBc;
         const int sb = n % kNumS;
         const uint32_t sbuf = lane_tmem + kColS + sb * 128;
@@ -596,7 +740,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
         // complete first. Skipping this wait otherwise is safe for the parity
         // bookkeeping: PV(n+2) cannot run before these warps release P(n+2), so
         // odone[(n-1) % 3] is at most one phase past the one waited for here.
-        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        if (j > jb && __any_sync(0xffffffffu, alpha != 1.f)) {
           const int pb = (n - 1) % kNumS;
           if (!wait_bar_warp(&bars.odone[pb], ((n - 1) / kNumS) & 1, prm, abort_flag)) goto softmax_done;
           tc_fence_after();
@@ -618,11 +762,19 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
       // The next unit's Q can go into shared memory now: its last QK has
       // completed (its S was just consumed).
       {
-        const int u_next = unit_index(k + 1, cta, grid);
+        const int u_next = work_unit<kMode>(k + 1, cta, grid, prm);
         if (u_next < prm.n_units) {
           load_q(decode_unit(u_next, prm));
           q_loaded = true;
         }
+      }
+      if constexpr (kMode == kTail) {
+        float* dst = p.out + ((size_t)pos * kHQ + w.g * kGroup + (row & 3)) * kD;
+        if (!split_epilogue(lane_tmem, n, has, bars, prm, abort_flag, reinterpret_cast<float*>(smem + kSmemSlot),
+                            rank, row, m_ref, l, c, pos < p.C, dst, 0))
+          goto softmax_done;
+        tc_fence_before();
+        continue;
       }
       // Epilogue: wait for the last PV, add the two stacked halves of O', one
       // division per element.
@@ -655,7 +807,17 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if constexpr (kMode == kTail) {
+    // Neither CTA of the pair leaves while the other may still write its
+    // shared memory or arrive on its barriers.
+    cluster_sync_all();
+  }
   if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+  if constexpr (kMode == kTail) {
+    // This grid ends only after the grid of whole units it overlaps: work
+    // ordered after it on the stream sees both complete.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -712,9 +874,11 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
     if (!st.ready) {
       if (cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return ATTN_ECUDA;
-      if (cudaFuncSetAttribute(tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc) !=
+      if (cudaFuncSetAttribute(tc_kernel<kMain>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc) !=
               cudaSuccess ||
-          cudaFuncSetAttribute(tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc) !=
+          cudaFuncSetAttribute(tc_kernel<kPaged>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc) !=
+              cudaSuccess ||
+          cudaFuncSetAttribute(tc_kernel<kTail>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc) !=
               cudaSuccess)
         return ATTN_ECUDA;
       st.ready = true;
@@ -735,11 +899,40 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
   prm.fault_skip_first_k = fault;
   prm.table = table;
   prm.num_pages = num_pages;
+  prm.unit_base = 0;
   const int grid = prm.n_units < num_sms ? prm.n_units : num_sms;
+  // When the last round of whole units would leave more than half of the SMs
+  // idle, the full rounds run as one grid and the remaining units as a second
+  // grid of CTA pairs that each split one unit; launched as a programmatic
+  // dependent, its pairs take SMs as the first grid's blocks leave them.
+  const int full = prm.n_units / grid * grid;
+  const int rem = prm.n_units - full;
+  const bool tail = full > 0 && rem > 0 && 2 * rem <= (num_sms & ~1);
+  Params main_prm = prm;
+  if (tail) main_prm.n_units = full;
   if (table)
-    tc_kernel<true><<<grid, kThreads, kSmemAlloc, stream>>>(mk, mv, prm);
+    tc_kernel<kPaged><<<grid, kThreads, kSmemAlloc, stream>>>(mk, mv, main_prm);
   else
-    tc_kernel<false><<<grid, kThreads, kSmemAlloc, stream>>>(mk, mv, prm);
+    tc_kernel<kMain><<<grid, kThreads, kSmemAlloc, stream>>>(mk, mv, main_prm);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ELAUNCH;
+  if (!tail) return ATTN_OK;
+  Params tail_prm = prm;
+  tail_prm.unit_base = full;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * rem);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  if (cudaLaunchKernelEx(&cfg, tc_kernel<kTail>, mk, mv, tail_prm) != cudaSuccess) return ATTN_ELAUNCH;
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ELAUNCH;
 }
 

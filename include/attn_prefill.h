@@ -139,8 +139,10 @@ int attn_prefill_bf16kv(const float *q, const uint16_t *kCache, const uint16_t *
  * whole 32-row query tiles, and each copies in only its own query rows and the
  * K/V rows the sub-chunk before it did not need. Copy-in of sub-chunk s+1 and
  * copy-out of sub-chunk s-1 run under the compute of sub-chunk s, on two
- * streams the library keeps per device. The result is bit-identical to the
- * device-pointer entry point on the same inputs.
+ * streams the library keeps per device. Each sub-chunk's rows are exactly
+ * those of the device-pointer entry point called on that sub-chunk; against one
+ * call on the whole chunk they agree to rounding (that call may split its last
+ * round's units over CTA pairs, another summation order).
  *
  *   q_host, kCache_host, vCache_host   read; the layouts of attn_prefill
  *                                      (uint16_t bf16 patterns for the
