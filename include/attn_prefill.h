@@ -82,7 +82,7 @@ extern "C" {
 #define ATTN_DECODE_SCRATCH_BYTES (4u << 20)
 
 /*
- * attn_prefill -- the main path: one persistent, warp-specialised tcgen05
+ * attn_prefill -- the main path: a persistent, warp-specialised tcgen05
  * kernel. A CTA owns a work unit of 32 chunk positions x the 4 query heads of
  * one KV head (GQA packing, "FlashAttention and inference kernels", GQA read
  * amplification exercise), so each K/V tile is staged in shared memory once
@@ -95,6 +95,10 @@ extern "C" {
  * error-compensated split-TF32: each fp32 operand x = hi + lo with hi exactly
  * representable in tf32, and each product accumulates hi*hi + hi*lo + lo*hi in
  * fp32, so the result matches exact fp32 products to about 2^-20 relative.
+ * When the last round of units would leave more than half of the SMs idle, a
+ * second grid of two-CTA clusters takes those units, each pair splitting one
+ * along its keys and merging the two partials with the split-K rule (same
+ * page, Flash-Decoding and the split-K merge); it needs no device memory.
  */
 int attn_prefill(const float *q, const float *kCache, const float *vCache, float *out,
                  int C, int P, cudaStream_t stream);
