@@ -92,10 +92,11 @@ struct Layout {
   static constexpr uint32_t kSmemK = 0;
   static constexpr uint32_t kSmemV = kSmemK + kStages * kStageBytes;
   static constexpr uint32_t kSmemBar = kSmemV + kStages * kStageBytes;
-  static constexpr uint32_t kNumBars = 9 * kStages + 1 + 2 + 4;
+  static constexpr uint32_t kNumBars = 9 * kStages + 1 + 2 + 4 + 2;
   static constexpr uint32_t kSmemRed = kSmemBar + kNumBars * 8 + 16;  // [2 tile parities][2 key halves][128 rows]
   static constexpr uint32_t kSmemLsum = kSmemRed + 2 * 2 * 128 * 4;   // [2 key halves][128 rows]
-  static constexpr uint32_t kSmemTotal = kSmemLsum + 2 * 128 * 4;
+  static constexpr uint32_t kSmemSlot = kSmemLsum + 2 * 128 * 4;    // tail kernel: rank 1's m and l per row
+  static constexpr uint32_t kSmemTotal = kSmemSlot + 2 * 128 * 4;
   static constexpr uint32_t kSmemAlloc = kSmemTotal + 1024;
   static_assert(kSmemAlloc <= 232448, "exceeds the 227 KB per-block shared memory limit");
 };
@@ -112,6 +113,7 @@ struct Params {
   int n_units;
   int n_qtiles;
   unsigned long long timeout_ns;
+  int unit_base;  // tail kernel: pair p splits unit unit_base + p
 };
 
 struct Bars {
@@ -127,6 +129,8 @@ struct Bars {
   uint64_t* qready;  // Q hi/lo in TMEM
   uint64_t* drain;   // [2] MMA issuers' drain on abort
   uint64_t* pair;    // [4] row-set exchanges of the softmax warps
+  uint64_t* partner;   // tail kernel, rank 0: rank 1's share of the unit is in place (256 remote arrivals)
+  uint64_t* slotfree;  // tail kernel, rank 1: rank 0 has taken it (256 remote arrivals)
 };
 
 template <bool kF32>
@@ -146,6 +150,8 @@ __device__ __forceinline__ Bars carve_bars(uint8_t* base) {
   r.qready = b++;
   r.drain = b; b += 2;
   r.pair = b; b += 4;
+  r.partner = b++;
+  r.slotfree = b++;
   return r;
 }
 
@@ -164,6 +170,26 @@ __device__ __forceinline__ Unit decode_unit(int u, const Params& prm) {
   const int nkeys = unit_keys(prm.p.P, prm.p.C, w.t0, kBq);
   w.ntiles = (nkeys + kBc - 1) / kBc;
   return w;
+}
+
+// kTail == false: whole units in snake order. kTail: launched after that grid
+// as clusters of two CTAs; pair p splits unit unit_base + p along its key tiles
+// (rank 0 the first half, rank 1 the rest) and merges the two online-softmax
+// partials through distributed shared memory.
+template <bool kTail>
+__device__ __forceinline__ int work_unit(int k, int cta, int grid, const Params& prm) {
+  if constexpr (kTail) return k == 0 ? prm.unit_base + (cta >> 1) : prm.n_units;
+  else return unit_index(k, cta, grid);
+}
+template <bool kTail>
+__device__ __forceinline__ void unit_range(const Unit& w, uint32_t rank, int* jb, int* je) {
+  if constexpr (kTail) {
+    *jb = rank == 0 ? 0 : w.ntiles / 2;
+    *je = rank == 0 ? w.ntiles / 2 : w.ntiles;
+  } else {
+    *jb = 0;
+    *je = w.ntiles;
+  }
 }
 
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const Params& prm,
@@ -186,6 +212,29 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const P
 __device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity, const Params& prm,
                                               volatile int* abort_flag) {
   const bool ok = wait_bar(bar, parity, prm, abort_flag);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// As wait_bar_warp, for a barrier the partner CTA arrives on: the wait
+// acquires at cluster scope, so the partner's released writes are visible.
+__device__ __forceinline__ bool wait_bar_cluster_warp(uint64_t* bar, uint32_t parity, const Params& prm,
+                                                      volatile int* abort_flag) {
+  bool ok = mbar_try_wait_cluster(bar, parity);
+  if (!ok) {
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+      if (mbar_try_wait_cluster(bar, parity)) {
+        ok = true;
+        break;
+      }
+      if (*abort_flag) break;
+      if (globaltimer_ns() - t0 > prm.timeout_ns) {
+        record_error(prm.p.err, kDevErrTimeout);
+        *abort_flag = 1;
+        break;
+      }
+    }
+  }
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -218,7 +267,7 @@ __device__ __forceinline__ void split_pack_rn(const float* x, uint32_t* hi, uint
   }
 }
 
-template <bool kF32>
+template <bool kF32, bool kTail>
 __global__ void __launch_bounds__(threads_of<kF32>(), 1)
 tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                const Params prm) {
@@ -253,6 +302,10 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
     mbar_init(&bars.drain[0], 1);
     mbar_init(&bars.drain[1], 1);
     for (int q = 0; q < 4; ++q) mbar_init(&bars.pair[q], 2);
+    if constexpr (kTail) {
+      mbar_init(bars.partner, kSoftmaxWarps * 32);
+      mbar_init(bars.slotfree, kSoftmaxWarps * 32);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -266,6 +319,16 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  if constexpr (kTail) {
+    // Both CTAs of the pair are running and their barriers initialised before
+    // either can touch the other's shared memory.
+    cluster_sync_all();
+  } else {
+    // A tail launch after this one (a programmatic dependent) may start its
+    // blocks on SMs as soon as blocks of this grid leave them.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  }
+  const uint32_t rank = kTail ? cluster_ctarank() : 0u;
 
   const int cta = blockIdx.x, grid = gridDim.x;
   const Problem& p = prm.p;
@@ -276,10 +339,12 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
     if (lane == 0) {
       int n = 0;
       for (int k = 0;; ++k) {
-        const int u = unit_index(k, cta, grid);
+        const int u = work_unit<kTail>(k, cta, grid, prm);
         if (u >= prm.n_units) break;
         const Unit w = decode_unit(u, prm);
-        for (int j = 0; j < w.ntiles; ++j, ++n) {
+        int jb, je;
+        unit_range<kTail>(w, rank, &jb, &je);
+        for (int j = jb; j < je; ++j, ++n) {
           const int st = n % kStages;
           uint64_t* freed = is_k ? &bars.kempty[st] : &bars.vempty[st];
           if (n >= kStages && !wait_bar(freed, ((n / kStages) - 1) & 1, prm, abort_flag)) goto producer_done;
@@ -307,14 +372,19 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
     if (lane == 0) {
       int n = 0, lu = 0;
       for (int k = 0;; ++k) {
-        const int u = unit_index(k, cta, grid);
+        const int u = work_unit<kTail>(k, cta, grid, prm);
         if (u >= prm.n_units) break;
         const Unit w = decode_unit(u, prm);
+        int jb, je;
+        unit_range<kTail>(w, rank, &jb, &je);
+        if constexpr (kTail) {
+          if (jb == je) continue;  // no tiles here (its Q is not loaded either)
+        }
         if (is_qk) {
           if (!wait_bar(bars.qready, lu & 1, prm, abort_flag)) goto mma_done;
           tc_fence_after();
         }
-        for (int j = 0; j < w.ntiles; ++j, ++n) {
+        for (int j = jb; j < je; ++j, ++n) {
           const int b = n % kNumS;
           const int st = n % kStages;
           if (is_qk) {
@@ -346,7 +416,7 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
             tc_fence_after();
             const uint32_t vb = smem_u32(smem + kSmemV + st * kStageBytes);
             const uint32_t phi = tmem + kColS + b * 128;
-            const bool first = j == 0;
+            const bool first = j == jb;
 #pragma unroll
             for (int s = 0; s < 8; ++s)  // 16 keys per step: 2048 bytes of V rows
               mma_f16_ts(tmem + kColO, phi + s * 8, sdesc_sw128_mn(vb + s * 2048), kIdescPV,
@@ -388,10 +458,12 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
       const int cw = (warp - kFirstConvWarp) % kConvWarpsPerOperand;
       int n = 0;
       for (int k = 0;; ++k) {
-        const int u = unit_index(k, cta, grid);
+        const int u = work_unit<kTail>(k, cta, grid, prm);
         if (u >= prm.n_units) break;
         const Unit w = decode_unit(u, prm);
-        for (int j = 0; j < w.ntiles; ++j, ++n) {
+        int jb, je;
+        unit_range<kTail>(w, rank, &jb, &je);
+        for (int j = jb; j < je; ++j, ++n) {
           const int st = n % kStages;
           if (!wait_bar_warp(is_k ? &bars.kfull[st] : &bars.vfull[st], (n / kStages) & 1, prm, abort_flag))
             goto conv_done;
@@ -474,15 +546,18 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
 
     bool q_loaded = false;
     for (int k = 0;; ++k) {
-      const int u = unit_index(k, cta, grid);
+      const int u = work_unit<kTail>(k, cta, grid, prm);
       if (u >= prm.n_units) break;
       const Unit w = decode_unit(u, prm);
-      if (!q_loaded) load_q(w);
+      int jb, je;
+      unit_range<kTail>(w, rank, &jb, &je);
+      const bool has = jb < je;
+      if (has && !q_loaded) load_q(w);
       q_loaded = false;
       float m_ref = -INFINITY, l = 0.f;
       const int pos = w.t0 + (row >> 2);
       const int limit = p.P + pos;
-      for (int j = 0; j < w.ntiles; ++j, ++n) {
+      for (int j = jb; j < je; ++j, ++n) {
         const int b = n % kNumS;
         const int j0 = j * kBc + kh * 64;
         const uint32_t sbuf = lane_tmem + kColS + b * 128;
@@ -537,7 +612,7 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
         // O is rescaled only when the reference maximum moved, after PV(n-1)
         // completes (odone[(n-1) % 3] cannot be a phase further: PV(n+2) needs
         // P(n+2) from these warps).
-        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        if (j > jb && __any_sync(0xffffffffu, alpha != 1.f)) {
           const int pb = (n - 1) % kNumS;
           if (!wait_bar_warp(&bars.odone[pb], ((n - 1) / kNumS) & 1, prm, abort_flag)) goto softmax_done;
           tc_fence_after();
@@ -554,7 +629,7 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
         if (lane == 0) mbar_arrive(&bars.pfull[b]);
       }
       {
-        const int u_next = unit_index(k + 1, cta, grid);
+        const int u_next = work_unit<kTail>(k + 1, cta, grid, prm);
         if (u_next < prm.n_units) {
           load_q(decode_unit(u_next, prm));
           q_loaded = true;
@@ -563,6 +638,60 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
       lred[kh * 128 + row] = l;
       if (!pair_sync()) goto softmax_done;
       l += lred[(kh ^ 1) * 128 + row];
+      if constexpr (kTail) {
+        // A unit split over the CTA pair; this thread holds 32 of its row's 64
+        // output dims (head dims 32 kh ..), and l and the reference maximum of
+        // this CTA's key tiles (none when it got no tile). Rank 1 writes its
+        // normalised share and sends m and l (one warp of the row set) to rank
+        // 0's slot; rank 0 merges, m = max(m0, m1) with weights e^(m_s - m)
+        // (in log2 units, (m_s - m) c), one division per element.
+        float o[32];
+        if (has) {
+          const int pb = (n - 1) % kNumS;
+          if (!wait_bar_warp(&bars.odone[pb], ((n - 1) / kNumS) & 1, prm, abort_flag)) goto softmax_done;
+          tc_fence_after();
+          tmem_ld32(lane_tmem + kColO + kh * 32, o);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = 0.f;
+        }
+        float* slot = reinterpret_cast<float*>(smem + L::kSmemSlot);  // [m of rank 1][l of rank 1], per row
+        float* dst = p.out + ((size_t)pos * kHQ + w.g * kGroup + (row & 3)) * kD + kh * 32;
+        const uint32_t peer = rank ^ 1u;
+        if (rank == 1) {
+          if (pos < p.C) {
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+              *reinterpret_cast<float4*>(dst + i) =
+                  make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
+          }
+          if (kh == 0) {
+            st_shared_cluster_f32(mapa_shared(smem_u32(slot + row), peer), m_ref);
+            st_shared_cluster_f32(mapa_shared(smem_u32(slot + 128 + row), peer), l);
+          }
+          mbar_arrive_remote(mapa_shared(smem_u32(bars.partner), peer));
+        } else {
+          if (!wait_bar_cluster_warp(bars.partner, 0, prm, abort_flag)) goto softmax_done;
+          const float m1 = slot[row], l1 = slot[128 + row];
+          const float m = fmaxf(l > 0.f ? m_ref : -INFINITY, l1 > 0.f ? m1 : -INFINITY);
+          const float e0 = l > 0.f ? ex2((m_ref - m) * c) : 0.f;
+          const float w1 = l1 > 0.f ? ex2((m1 - m) * c) * l1 : 0.f;
+          const float inv = 1.f / fmaf(e0, l, w1);  // > 0: the unit sees at least key 0
+          if (pos < p.C) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+              const float4 x1 = __ldcg(reinterpret_cast<const float4*>(dst + i));
+              *reinterpret_cast<float4*>(dst + i) =
+                  make_float4(fmaf(e0, o[i], w1 * x1.x) * inv, fmaf(e0, o[i + 1], w1 * x1.y) * inv,
+                              fmaf(e0, o[i + 2], w1 * x1.z) * inv, fmaf(e0, o[i + 3], w1 * x1.w) * inv);
+            }
+          }
+        }
+        tc_fence_before();
+        continue;
+      }
       {
         const int pb = (n - 1) % kNumS;
         if (!wait_bar_warp(&bars.odone[pb], ((n - 1) / kNumS) & 1, prm, abort_flag)) goto softmax_done;
@@ -590,7 +719,17 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if constexpr (kTail) {
+    // Neither CTA of the pair leaves while the other may still write its
+    // shared memory or arrive on its barriers.
+    cluster_sync_all();
+  }
   if (warp == kQkWarp) tmem_dealloc(tmem, kTmemCols);
+  if constexpr (kTail) {
+    // This grid ends only after the grid of whole units it overlaps: work
+    // ordered after it on the stream sees both complete.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -629,7 +768,7 @@ int encode_kv_tile_map(const void* base, int rows, bool f32, CUtensorMap* map) {
 }
 
 struct DevState {
-  bool ready[2] = {false, false};
+  bool ready[2] = {false, false};  // per cache type, both instantiations set up
   int num_sms = 0;
 };
 DevState g_state[64];
@@ -646,7 +785,9 @@ int launch_impl(const Problem& p, cudaStream_t stream) {
     if (!st.ready[kF32]) {
       if (cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return ATTN_ECUDA;
-      if (cudaFuncSetAttribute(tc_bf16_kernel<kF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      if (cudaFuncSetAttribute(tc_bf16_kernel<kF32, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)Layout<kF32>::kSmemAlloc) != cudaSuccess ||
+          cudaFuncSetAttribute(tc_bf16_kernel<kF32, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)Layout<kF32>::kSmemAlloc) != cudaSuccess)
         return ATTN_ECUDA;
       st.ready[kF32] = true;
@@ -662,8 +803,40 @@ int launch_impl(const Problem& p, cudaStream_t stream) {
   prm.n_qtiles = (p.C + kBq - 1) / kBq;
   prm.n_units = prm.n_qtiles * kHKV;
   prm.timeout_ns = 2000000000ull;
+  prm.unit_base = 0;
   const int grid = prm.n_units < num_sms ? prm.n_units : num_sms;
-  tc_bf16_kernel<kF32><<<grid, threads_of<kF32>(), Layout<kF32>::kSmemAlloc, stream>>>(mk, mv, prm);
+  // When the last round of whole units would leave more than half of the SMs
+  // idle, the full rounds run as one grid and the remaining units as a second
+  // grid of CTA pairs that each split one unit; launched as a programmatic
+  // dependent, its pairs take SMs as the first grid's blocks leave them. This
+  // kernel only does so when even the shortest unit sees 8192 keys or more:
+  // measured, with shorter units (the serving chunk's 2080 to 4096) the split
+  // costs more than the imbalance it removes.
+  const int full = prm.n_units / grid * grid;
+  const int rem = prm.n_units - full;
+  const bool tail = full > 0 && rem > 0 && 2 * rem <= (num_sms & ~1) && unit_keys(p.P, p.C, 0, kBq) >= 8192;
+  Params main_prm = prm;
+  if (tail) main_prm.n_units = full;
+  tc_bf16_kernel<kF32, false><<<grid, threads_of<kF32>(), Layout<kF32>::kSmemAlloc, stream>>>(mk, mv, main_prm);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ELAUNCH;
+  if (!tail) return ATTN_OK;
+  Params tail_prm = prm;
+  tail_prm.unit_base = full;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * rem);
+  cfg.blockDim = dim3(threads_of<kF32>());
+  cfg.dynamicSmemBytes = Layout<kF32>::kSmemAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  if (cudaLaunchKernelEx(&cfg, tc_bf16_kernel<kF32, true>, mk, mv, tail_prm) != cudaSuccess) return ATTN_ELAUNCH;
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ELAUNCH;
 }
 
