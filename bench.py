@@ -208,18 +208,22 @@ def kernel_source_hash(path_name: str) -> str:
     return hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
 
 
-def launches_per_call(path: str, C: int) -> int:
-    """Kernel launches in one call of `path` on C chunk rows. The split-TF32
-    path (contiguous or paged) adds a second grid for the last round's units
-    when that round would leave more than half of the SMs idle: the library's
-    own rule, on 32-row query tiles x 8 KV heads."""
-    if path != "attn_prefill":
+def launches_per_call(path: str, C: int, P: int) -> int:
+    """Kernel launches in one call of `path` on a chunk of C rows at offset P:
+    the library's own rule for its split-unit grid, on 32-row query tiles x 8
+    KV heads and the device's SMs. A second grid of CTA pairs takes the last
+    round's units when that round would leave more than half of the SMs idle
+    (the bf16 paths only when every unit sees 8192 keys or more). With at most
+    half as many units as SMs, long units are all split in a single grid of
+    pairs instead of the whole-unit grid: still one launch."""
+    if path not in ("attn_prefill", "attn_prefill_bf16x3", "attn_prefill_bf16kv"):
         return 1
     units = -(-C // 32) * 8
-    grid = min(units, NUM_SMS)
-    full = units // grid * grid
-    rem = units - full
-    return 2 if full > 0 and rem > 0 and 2 * rem <= (NUM_SMS & ~1) else 1
+    if units > NUM_SMS:
+        rem = units % NUM_SMS
+        ok = P + min(32, C) >= 8192 if path != "attn_prefill" else True  # the shortest unit's keys
+        return 2 if rem > 0 and 2 * rem <= (NUM_SMS & ~1) and ok else 1
+    return 1  # one grid: whole units, or (at most half as many units as SMs) all split
 
 
 def profiled_traffic(path_name: str, workload: str):
@@ -694,7 +698,7 @@ def main():
                                  args.workload + ("-paged" if args.paged else "")),
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": args.steps * launches_per_call(args.path, C),
+            "gpu_launches": args.steps * launches_per_call(args.path, C, P),
             "clocks": sampler.summary(t_begin, t_end),
             "wall_s_timed_region": round(wall, 4),
         }

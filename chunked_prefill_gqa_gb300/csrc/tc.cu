@@ -901,25 +901,47 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
   prm.num_pages = num_pages;
   prm.unit_base = 0;
   const int grid = prm.n_units < num_sms ? prm.n_units : num_sms;
-  // When the last round of whole units would leave more than half of the SMs
-  // idle, the full rounds run as one grid and the remaining units as a second
-  // grid of CTA pairs that each split one unit; launched as a programmatic
-  // dependent, its pairs take SMs as the first grid's blocks leave them.
-  const int full = prm.n_units / grid * grid;
-  const int rem = prm.n_units - full;
-  const bool tail = full > 0 && rem > 0 && 2 * rem <= (num_sms & ~1);
-  Params main_prm = prm;
-  if (tail) main_prm.n_units = full;
-  if (table)
-    tc_kernel<kPaged><<<grid, kThreads, kSmemAlloc, stream>>>(mk, mv, main_prm);
-  else
-    tc_kernel<kMain><<<grid, kThreads, kSmemAlloc, stream>>>(mk, mv, main_prm);
-  if (cudaGetLastError() != cudaSuccess) return ATTN_ELAUNCH;
-  if (!tail) return ATTN_OK;
-  Params tail_prm = prm;
-  tail_prm.unit_base = full;
+  // Split units. With several rounds, when the last round of whole units would
+  // leave more than half of the SMs idle, the full rounds run as one grid and
+  // the remaining units as a second grid of CTA pairs that each split one unit.
+  // With at most half as many units as SMs and long units, every unit is
+  // split over a pair. (The two grids can also split only the longest s units,
+  // the whole-unit grid starting s / 8 q-tiles down.) The pair grid
+  // is a programmatic dependent of the whole-unit grid: its pairs take SMs as
+  // soon as they are free.
+  Params main_prm = prm, tail_prm = prm;
+  int main_grid = grid, tail_units = 0;
+  if (prm.n_units > grid) {
+    const int full = prm.n_units / grid * grid;
+    const int rem = prm.n_units - full;
+    if (rem > 0 && 2 * rem <= (num_sms & ~1)) {
+      main_prm.n_units = full;
+      tail_prm.unit_base = full;
+      tail_units = rem;
+    }
+  } else if (2 * prm.n_units <= num_sms && unit_keys(p.P, p.C, (prm.n_qtiles - 1) * kBq, kBq) >= 2048) {
+    // Measured: splitting only some of the units (more than half as many
+    // units as SMs) costs more than it gains.
+    const int split = prm.n_units;
+    {
+      main_prm.n_qtiles -= split / kHKV;
+      main_prm.n_units -= split;
+      main_grid = main_prm.n_units;
+      tail_prm.unit_base = 0;
+      tail_prm.n_units = split;
+      tail_units = split;
+    }
+  }
+  if (main_prm.n_units > 0) {
+    if (table)
+      tc_kernel<kPaged><<<main_grid, kThreads, kSmemAlloc, stream>>>(mk, mv, main_prm);
+    else
+      tc_kernel<kMain><<<main_grid, kThreads, kSmemAlloc, stream>>>(mk, mv, main_prm);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ELAUNCH;
+  }
+  if (tail_units == 0) return ATTN_OK;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * rem);
+  cfg.gridDim = dim3(2 * tail_units);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemAlloc;
   cfg.stream = stream;
@@ -931,7 +953,7 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = main_prm.n_units > 0 ? 2 : 1;  // a dependent only of a whole-unit grid
   if (cudaLaunchKernelEx(&cfg, tc_kernel<kTail>, mk, mv, tail_prm) != cudaSuccess) return ATTN_ELAUNCH;
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ELAUNCH;
 }

@@ -805,25 +805,43 @@ int launch_impl(const Problem& p, cudaStream_t stream) {
   prm.timeout_ns = 2000000000ull;
   prm.unit_base = 0;
   const int grid = prm.n_units < num_sms ? prm.n_units : num_sms;
-  // When the last round of whole units would leave more than half of the SMs
-  // idle, the full rounds run as one grid and the remaining units as a second
-  // grid of CTA pairs that each split one unit; launched as a programmatic
-  // dependent, its pairs take SMs as the first grid's blocks leave them. This
-  // kernel only does so when even the shortest unit sees 8192 keys or more:
-  // measured, with shorter units (the serving chunk's 2080 to 4096) the split
-  // costs more than the imbalance it removes.
-  const int full = prm.n_units / grid * grid;
-  const int rem = prm.n_units - full;
-  const bool tail = full > 0 && rem > 0 && 2 * rem <= (num_sms & ~1) && unit_keys(p.P, p.C, 0, kBq) >= 8192;
-  Params main_prm = prm;
-  if (tail) main_prm.n_units = full;
-  tc_bf16_kernel<kF32, false><<<grid, threads_of<kF32>(), Layout<kF32>::kSmemAlloc, stream>>>(mk, mv, main_prm);
-  if (cudaGetLastError() != cudaSuccess) return ATTN_ELAUNCH;
-  if (!tail) return ATTN_OK;
-  Params tail_prm = prm;
-  tail_prm.unit_base = full;
+  // Split units, as for the split-TF32 kernel: with several rounds, a short
+  // last round's units go to a second grid of CTA pairs that each split one;
+  // with at most half as many units as SMs, every unit is split over a pair.
+  // This kernel only splits units of 8192 keys or more:
+  // measured, with the serving chunk's 2080 to 4096 the split costs about 1 %
+  // more than the imbalance it removes.
+  Params main_prm = prm, tail_prm = prm;
+  int main_grid = grid, tail_units = 0;
+  if (prm.n_units > grid) {
+    const int full = prm.n_units / grid * grid;
+    const int rem = prm.n_units - full;
+    if (rem > 0 && 2 * rem <= (num_sms & ~1) && unit_keys(p.P, p.C, 0, kBq) >= 8192) {
+      main_prm.n_units = full;
+      tail_prm.unit_base = full;
+      tail_units = rem;
+    }
+  } else if (2 * prm.n_units <= num_sms && unit_keys(p.P, p.C, 0, kBq) >= 8192) {
+    // Measured: splitting only some of the units (more than half as many
+    // units as SMs) costs more than it gains.
+    const int split = prm.n_units;
+    {
+      main_prm.n_qtiles -= split / kHKV;
+      main_prm.n_units -= split;
+      main_grid = main_prm.n_units;
+      tail_prm.unit_base = 0;
+      tail_prm.n_units = split;
+      tail_units = split;
+    }
+  }
+  if (main_prm.n_units > 0) {
+    tc_bf16_kernel<kF32, false><<<main_grid, threads_of<kF32>(), Layout<kF32>::kSmemAlloc, stream>>>(mk, mv,
+                                                                                                   main_prm);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ELAUNCH;
+  }
+  if (tail_units == 0) return ATTN_OK;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * rem);
+  cfg.gridDim = dim3(2 * tail_units);
   cfg.blockDim = dim3(threads_of<kF32>());
   cfg.dynamicSmemBytes = Layout<kF32>::kSmemAlloc;
   cfg.stream = stream;
@@ -835,7 +853,7 @@ int launch_impl(const Problem& p, cudaStream_t stream) {
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = main_prm.n_units > 0 ? 2 : 1;  // a dependent only of a whole-unit grid
   if (cudaLaunchKernelEx(&cfg, tc_bf16_kernel<kF32, true>, mk, mv, tail_prm) != cudaSuccess) return ATTN_ELAUNCH;
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ELAUNCH;
 }
