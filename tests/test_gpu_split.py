@@ -1,0 +1,75 @@
+"""The split-unit grids against the oracle, every element checked on a poisoned,
+guarded output: chunks small enough that every unit is split over a CTA pair
+(with P + C past the split thresholds: 2048 keys for the split-TF32 kernel,
+8192 for the bf16 kernels), and chunks whose last round of units goes to the
+pair grid (the tail), including a ragged last query tile and a paged cache."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+from gpu_util import GuardedOut  # noqa: E402
+
+
+@pytest.fixture(scope="module")
+def cp():
+    from chunked_prefill_gqa_gb300 import build
+    build.build()
+    import chunked_prefill_gqa_gb300 as m
+    return m
+
+
+def run(cp, path, inp):
+    g = GuardedOut(inp.C)
+    q = torch.from_numpy(inp.q).cuda()
+    if path == "attn_prefill_bf16kv":
+        kv = W.to_bf16(inp)
+        k = torch.from_numpy(kv.k.view(np.int16)).cuda()
+        v = torch.from_numpy(kv.v.view(np.int16)).cuda()
+        ref = oracle.prefill_bf16kv(inp.q, kv.k, kv.v, inp.P)
+    else:
+        k, v = torch.from_numpy(inp.k).cuda(), torch.from_numpy(inp.v).cuda()
+        ref = oracle.prefill(inp)
+    if path == "attn_prefill_paged":
+        pg = W.to_pages(inp, seed=inp.C)
+        cp.attn_prefill_paged(q, torch.from_numpy(pg.k_pages).cuda(), torch.from_numpy(pg.v_pages).cuda(),
+                              torch.from_numpy(pg.table).cuda(), g.out, inp.P)
+    else:
+        getattr(cp, path)(q, k, v, g.out, inp.P)
+    torch.cuda.synchronize()
+    got = g.numpy()
+    assert g.guards_intact(), "a value outside out was written"
+    assert np.isfinite(got).all()
+    rep = oracle.check(got, ref)
+    assert rep["n_bad"] == 0, f"{path} C={inp.C} P={inp.P}: {rep}"
+    assert cp.attn_get_device_error() == 0
+
+
+# Every unit split (at most 76 units, i.e. C <= 304 rows, on 152 SMs).
+@pytest.mark.parametrize("path,C,P", [
+    ("attn_prefill", 1, 2048), ("attn_prefill", 33, 2048), ("attn_prefill", 100, 3000),
+    ("attn_prefill", 288, 2500), ("attn_prefill_paged", 100, 3000), ("attn_prefill_paged", 17, 4100),
+    ("attn_prefill_bf16kv", 64, 8200), ("attn_prefill_bf16kv", 288, 8192), ("attn_prefill_bf16x3", 100, 8300),
+])
+def test_every_unit_split(cp, path, C, P):
+    run(cp, path, W.edge(C, P, seed=C + P))
+
+
+@pytest.mark.parametrize("variant", ["lastkey", "ramp"])
+def test_every_unit_split_max_in_last_tile(cp, variant):
+    """A row's maximum in its final key tile: with the unit split, that tile
+    belongs to rank 1 and the merge must carry it."""
+    run(cp, "attn_prefill", W.edge(64, 3000, variant=variant))
+
+
+# The tail: 512 units of which 56 go to the pair grid; C = 2040 leaves the last
+# query tile 24 rows short.
+@pytest.mark.parametrize("path,C,P", [
+    ("attn_prefill", 2040, 100), ("attn_prefill_paged", 2040, 100), ("attn_prefill_bf16kv", 2040, 8200),
+])
+def test_tail_grid_ragged(cp, path, C, P):
+    run(cp, path, W.edge(C, P, seed=7))
