@@ -402,7 +402,10 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
   if (warp == kKProducerWarp || warp == kVProducerWarp) {
     // ------------------------------------------------------------ producers
     const bool is_k = warp == kKProducerWarp;
-    if (lane == 0) {
+    // Page pools: lanes 0-3 each issue one page of a tile (its table entry and
+    // its two boxes); otherwise lane 0 issues the whole tile.
+    constexpr int kLanes = kMode == kPaged ? kBc / kPage : 1;
+    if (lane < kLanes) {
       const int stages = is_k ? kKStages : kVRawStages;
       int n = 0;
       for (int k = 0;; ++k) {
@@ -414,14 +417,37 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
         for (int j = jb; j < je; ++j, ++n) {
           const int st = n % stages;
           uint64_t* freed = is_k ? &bars.kempty[st] : &bars.vrfree[st];
-          if (n >= stages && !wait_bar(freed, ((n / stages) - 1) & 1, prm, abort_flag)) goto producer_done;
+          if constexpr (kMode == kPaged) {
+            // The four lanes leave together or not at all.
+            const bool ok = n < stages || wait_bar(freed, ((n / stages) - 1) & 1, prm, abort_flag);
+            if (!__all_sync((1u << kLanes) - 1, ok)) goto producer_done;
+          } else {
+            if (n >= stages && !wait_bar(freed, ((n / stages) - 1) & 1, prm, abort_flag)) goto producer_done;
+          }
           if (is_k && prm.fault_skip_first_k && n == 0) continue;
           const CUtensorMap* map = is_k ? &tmk : &tmv;
           uint64_t* full = is_k ? &bars.kfull[st] : &bars.vfull[st];
           uint8_t* dst = is_k ? smem + kSmemK + st * kKStageBytes : smem + kSmemVRaw + st * kVRawBytes;
           const uint32_t half_stride = is_k ? kRegion : kHalf;  // d-half regions
+          if constexpr (kMode == kPaged) {
+            // Lane 0 posts the tile's bytes before any of its boxes is issued.
+            if (lane == 0) mbar_arrive_expect_tx(full, 2 * kHalf);
+            __syncwarp((1u << kLanes) - 1);
+            const int lp = j * (kBc / kPage) + lane;
+            int y = prm.num_pages * kPage;
+            if (lp * kPage < p.P + p.C) {
+              const int phys = __ldg(prm.table + lp);
+              if (phys >= 0 && phys < prm.num_pages)
+                y = phys * kPage;
+              else
+                record_error(p.err, kDevErrBounds);
+            }
+            tma_load_2d(dst + lane * kPage * 128, map, full, w.g * kD, y);
+            tma_load_2d(dst + half_stride + lane * kPage * 128, map, full, w.g * kD + 32, y);
+            continue;
+          }
           mbar_arrive_expect_tx(full, 2 * kHalf);
-          if (kMode != kPaged && prm.table == nullptr) {
+          if (prm.table == nullptr) {
             tma_load_2d(dst, map, full, w.g * kD, j * kBc);
             tma_load_2d(dst + half_stride, map, full, w.g * kD + 32, j * kBc);
           } else {
