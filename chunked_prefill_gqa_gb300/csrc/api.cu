@@ -95,33 +95,38 @@ int naive_prepare(int C, int P, DeviceState** st) {
 
 // ---------------------------------------------------------------------------
 // Host-buffer calls: the chunk is run as up to kMaxSlices consecutive
-// sub-chunks of whole 32-row query tiles. Sub-chunk s (rows r0 .. r1-1) is the
+// sub-chunks of whole 32-row query tiles, each one full round of units. Sub-chunk s (rows r0 .. r1-1) is the
 // prefill of those rows against positions 0 .. P+r1-1, the same rows of the
 // whole call's result. Its copy-in adds only its query rows and the K/V rows
 // past the previous sub-chunk's end, so copy-in of s+1 and copy-out of s-1
 // overlap the compute of s.
 constexpr int kMaxSlices = 4;
-constexpr int kSliceRows = 512;  // 128 units, under one wave of 152 SMs
 
 struct HostPipe {
   std::mutex mu;  // held for a whole enqueue: every call re-records the events
   bool made = false;
+  int sms = 0;
   cudaStream_t in = nullptr, out = nullptr;
   cudaEvent_t start = nullptr, done = nullptr;
   cudaEvent_t loaded[kMaxSlices] = {}, computed[kMaxSlices] = {};
 };
 HostPipe g_pipes[kMaxDevices];
 
-// Slice boundaries: n = clamp(C / 512, 1, 4) slices, slice s ending after
-// floor((s + 1) tiles / n) query tiles, so later slices take the spare tiles.
-int plan_slices(int C, int bounds[kMaxSlices + 1]) {
+// Slice boundaries: each slice is one full round of units, sms / 8 query
+// tiles (8 KV heads per tile: one unit per SM), the last one the remainder; with
+// more than kMaxSlices such rounds, kMaxSlices equal slices instead.
+int plan_slices(int C, int sms, int bounds[kMaxSlices + 1]) {
   const int tiles = (C + 31) / 32;
-  int n = C / kSliceRows;
-  n = n < 1 ? 1 : (n > kMaxSlices ? kMaxSlices : n);
-  if (n > tiles) n = tiles;
+  int per = sms / ATTN_HKV;
+  if (per < 1) per = 1;
+  int n = (tiles + per - 1) / per;
+  if (n > kMaxSlices) {
+    n = kMaxSlices;
+    per = (tiles + n - 1) / n;
+  }
   bounds[0] = 0;
   for (int s = 0; s < n; ++s) {
-    const long long end = (long long)(s + 1) * tiles / n * 32;
+    const long long end = (long long)((s + 1) * per < tiles ? (s + 1) * per : tiles) * 32;
     bounds[s + 1] = end < C ? (int)end : C;
   }
   return n;
@@ -140,6 +145,7 @@ int make_pipe(HostPipe* hp) {
     if (cudaEventCreateWithFlags(&hp->loaded[s], cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&hp->computed[s], cudaEventDisableTiming) != cudaSuccess)
       return ATTN_ECUDA;
+  if (sm_count(&hp->sms) != ATTN_OK) return ATTN_ECUDA;
   hp->made = true;
   return ATTN_OK;
 }
@@ -168,7 +174,7 @@ int run_from_host(const float* q_h, const void* k_h, const void* v_h, float* out
   const auto* kh = static_cast<const char*>(k_h);
   const auto* vh = static_cast<const char*>(v_h);
   int bounds[kMaxSlices + 1];
-  const int n = plan_slices(C, bounds);
+  const int n = plan_slices(C, hp->sms, bounds);
   size_t kv0 = 0;
   for (int s = 0; s < n && rc == ATTN_OK; ++s) {
     const int r0 = bounds[s], r1 = bounds[s + 1];

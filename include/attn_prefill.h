@@ -141,9 +141,10 @@ int attn_prefill_bf16kv(const float *q, const uint16_t *kCache, const uint16_t *
  * Attention 2: Flash Prefill Against a Cached Prefix", Lesson: a chunk at
  * positions P .. P+C-1 attends to every position up to its own): rows r0 ..
  * r1-1 of the result are the prefill of those query rows against positions
- * 0 .. P+r1-1. So the chunk runs as n = clamp(C / 512, 1, 4) sub-chunks of
- * whole 32-row query tiles, and each copies in only its own query rows and the
- * K/V rows the sub-chunk before it did not need. Copy-in of sub-chunk s+1 and
+ * 0 .. P+r1-1. So the chunk runs as sub-chunks of whole 32-row query tiles,
+ * each one full round of units (SMs / 8 tiles: 608 rows on 152 SMs, the last
+ * the remainder; at most four, equal ones beyond that), and each copies in
+ * only its own query rows and the K/V rows the sub-chunk before it did not need. Copy-in of sub-chunk s+1 and
  * copy-out of sub-chunk s-1 run under the compute of sub-chunk s, on two
  * streams the library keeps per device. Each sub-chunk's rows are exactly
  * those of the device-pointer entry point called on that sub-chunk; against one

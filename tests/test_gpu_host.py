@@ -1,11 +1,12 @@
 """The host-buffer entry points (attn_prefill_host and its bf16x3 and bf16-cache
 twins): the chunk runs as up to four sub-chunks of whole query tiles with the
-copies overlapped. Each case is checked against the oracle, and against the
+copies overlapped; each sub-chunk is one full round of units (19 query tiles
+on 152 SMs). Each case is checked against the oracle, and against the
 device-pointer entry point: bit for bit where the whole call and its sub-chunks
-take the same units in the same order, to a tight tolerance where the whole
-call splits its last round's units over CTA pairs (the serving chunk), whose
+take the same units in the same order, to a tight tolerance where one of them
+splits units over CTA pairs and the other does not (the serving chunk, whose
 sub-chunks are then each checked bit for bit against a device call of their
-own. Rows before and after out_host must stay untouched,
+own). Rows before and after out_host must stay untouched,
 pageable memory must work, and back-to-back calls that reuse the same device
 buffers must not race."""
 import threading
@@ -97,8 +98,8 @@ def check(got, ref, what):
     assert rep["n_bad"] == 0, f"{what}: {rep}"
 
 
-# (C, P) spanning one sub-chunk (C < 1024), two (1057 = 17 + 17 tiles, the
-# second one ragged), and four (2118 rows: 67 tiles as 16, 17, 17, 17).
+# (C, P) spanning one sub-chunk (C <= 608), two (1057 = 19 + 15 tiles, the
+# second one ragged), and four (2118 rows: 67 tiles as 19, 19, 19, 10).
 @pytest.mark.parametrize("name", list(PATHS))
 @pytest.mark.parametrize("C,P", [(1, 0), (17, 31), (100, 77), (1057, 300), (2118, 5)])
 def test_matches_oracle_and_the_device_entry(cp, name, C, P):
@@ -117,20 +118,21 @@ def test_matches_oracle_and_the_device_entry(cp, name, C, P):
     assert np.array_equal(dk.cpu().numpy(), want_k)
 
 
-def test_serving_chunk_four_sub_chunks(cp):
-    """Four sub-chunks of 512 rows. Each one's rows are exactly the device call
-    on that sub-chunk; the device call on the whole chunk may split its last
-    round's units over CTA pairs (another summation order), so against it the
-    comparison is to a tolerance far inside the oracle's."""
+def test_serving_chunk_sub_chunks(cp):
+    """Sub-chunks of 608, 608, 608 and 224 rows. Each one's rows are exactly
+    the device call on that sub-chunk (the last one's 56 units split over CTA
+    pairs); the device call on the whole chunk splits its last round's units
+    instead (another summation order), so against it the comparison is to a
+    tolerance far inside the oracle's."""
     inp = W.serve()
     got, guards, _, kv = run_host(cp, "attn_prefill_host", inp)
     assert guards and np.isfinite(got).all()
     np.testing.assert_allclose(got, run_device(cp, "attn_prefill_host", inp, kv), rtol=1e-5, atol=1e-6)
-    for r0 in (0, 512, 1536):
-        sub = W.Inputs(q=inp.q[r0:r0 + 512], k=inp.k[:inp.P + r0 + 512], v=inp.v[:inp.P + r0 + 512],
-                       C=512, P=inp.P + r0, name=f"rows {r0}..{r0 + 511}")
-        assert np.array_equal(got[r0:r0 + 512], run_device(cp, "attn_prefill_host", sub, None)), r0
-    rows = sample_rows(inp.C, extra=(511, 512, 1023, 1024, 1535, 1536), n_random=6, seed=11)
+    for r0, r1 in ((0, 608), (608, 1216), (1824, 2048)):
+        sub = W.Inputs(q=inp.q[r0:r1], k=inp.k[:inp.P + r1], v=inp.v[:inp.P + r1],
+                       C=r1 - r0, P=inp.P + r0, name=f"rows {r0}..{r1 - 1}")
+        assert np.array_equal(got[r0:r1], run_device(cp, "attn_prefill_host", sub, None)), r0
+    rows = sample_rows(inp.C, extra=(607, 608, 1215, 1216, 1823, 1824), n_random=6, seed=11)
     check(got[rows], expected(inp, kv, rows=rows), "serve via host buffers")
 
 
@@ -185,7 +187,10 @@ def test_concurrent_host_threads(cp):
     [t.join() for t in ts]
     assert not errors, errors
     for i, inp in enumerate(inps):
-        assert np.array_equal(results[i], run_device(cp, "attn_prefill_host", inp, None)), i
+        # 700 and 800 rows: the whole call splits its tail, the sub-chunks do not.
+        np.testing.assert_allclose(results[i], run_device(cp, "attn_prefill_host", inp, None), rtol=1e-5, atol=1e-6)
+        rep = oracle.check(results[i], oracle.prefill(inp))
+        assert rep["n_bad"] == 0, (i, rep)
     assert cp.attn_get_device_error() == 0
 
 
