@@ -938,9 +938,11 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
   Params main_prm = prm, tail_prm = prm;
   int main_grid = grid, tail_units = 0;
   if (prm.n_units > grid) {
+    // (Only when even the shortest unit sees 1024 keys: measured, a full
+    // prompt's last round of 32-224 keys runs slower split.)
     const int full = prm.n_units / grid * grid;
     const int rem = prm.n_units - full;
-    if (rem > 0 && 2 * rem <= (num_sms & ~1)) {
+    if (rem > 0 && 2 * rem <= (num_sms & ~1) && unit_keys(p.P, p.C, 0, kBq) >= 1024) {
       main_prm.n_units = full;
       tail_prm.unit_base = full;
       tail_units = rem;
