@@ -300,11 +300,6 @@ __device__ __noinline__ bool split_epilogue(uint32_t lane_tmem, int n, bool has,
   return true;
 }
 
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&r)[64]) {
-  tmem_ld32(taddr, *reinterpret_cast<float(*)[32]>(&r[0]));
-  tmem_ld32(taddr + 32, *reinterpret_cast<float(*)[32]>(&r[32]));
-}
-
 // Instantiations. kMain: whole units in snake order; it decides by prm.table
 // at run time (it is the one launched for contiguous caches; measured,
 // dropping its paged branch slows it). kPaged: the same for page pools only.
