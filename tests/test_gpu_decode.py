@@ -83,6 +83,31 @@ def test_many_sequences_mixed_lengths(cp):
     assert np.all(got[0] == 0.0)   # an empty context gives zeros
 
 
+@pytest.mark.parametrize("splits", [2, 16])
+def test_workspace_starts_as_garbage_and_is_reused(cp, splits):
+    """Nothing in the workspace needs to start at zero: it is filled with 0xFF
+    bytes (every m_s, l_s and O_s reads NaN), then three calls in a row on one
+    stream reuse it unchanged. Their short second sequences leave most of 16
+    segments empty, whose records carry l_s = 0 and a stale O_s that the merge
+    must skip."""
+    mc = 3000
+    nbytes = cp.attn_decode_workspace_bytes(2, mc, splits)
+    assert nbytes > 0
+    ws = torch.empty(nbytes // 4 + 4, dtype=torch.float32, device="cuda")
+    ws.view(torch.int32).fill_(-1)
+    calls = []
+    for i, lens in enumerate(([3000, 5], [3000, 1], [3000, 2048])):
+        batch = W.decode_batch(lens, seed=30 + i)
+        t = [torch.from_numpy(x).cuda() for x in (batch.q, batch.k_pages, batch.v_pages, batch.table, batch.ctx)]
+        out = torch.full_like(t[0], float("nan"))
+        cp.attn_decode_paged(t[0], t[1], t[2], t[3], t[4], out, mc, splits, ws)
+        calls.append((batch, out, t))
+    torch.cuda.synchronize()
+    for batch, out, _ in calls:
+        check(out.cpu().numpy(), reference(batch), f"splits={splits} ctx={batch.ctx.tolist()}")
+    assert cp.attn_get_device_error() == 0
+
+
 def test_long_context_split(cp):
     batch = W.decode_batch([32768, 5000], seed=6)
     got, nbytes = run_decode(cp, batch, 0)
