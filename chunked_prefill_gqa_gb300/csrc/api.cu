@@ -449,9 +449,11 @@ extern "C" int attn_get_device_error(void) {
 extern "C" const char* attn_strerror(int code) {
   switch (code) {
     case ATTN_OK: return "success";
-    case ATTN_EINVAL: return "invalid argument (NULL pointer, C < 0 or P < 0)";
+    case ATTN_EINVAL: return "invalid argument (a NULL pointer, or a size below what the call accepts)";
     case ATTN_EALIGN: return "a tensor pointer is not 16-byte aligned";
-    case ATTN_ERANGE: return "C or P + C exceeds ATTN_MAX_TOKENS";
+    case ATTN_ERANGE:
+      return "a size is out of range (C or P + C above ATTN_MAX_TOKENS, numPages above ATTN_MAX_TOKENS / 16, "
+             "B above 65535, or maxContext above 16 * maxBlocks)";
     case ATTN_ELAUNCH: return "kernel launch failed";
     case ATTN_ETIMEOUT: return "a device-side bounded wait expired";
     case ATTN_EBOUNDS: return "a device-side bounds check failed";

@@ -68,7 +68,7 @@ extern "C" {
 #define ATTN_OK 0
 #define ATTN_EINVAL -1      /* NULL pointer with C > 0, C < 0, P < 0 */
 #define ATTN_EALIGN -2      /* a pointer is not 16-byte aligned */
-#define ATTN_ERANGE -3      /* C or P + C above ATTN_MAX_TOKENS */
+#define ATTN_ERANGE -3      /* a size out of range: C or P + C above ATTN_MAX_TOKENS, or as a call states */
 #define ATTN_ELAUNCH -4     /* the kernel launch failed (cudaGetLastError) */
 #define ATTN_ETIMEOUT -5    /* device word: a bounded wait expired */
 #define ATTN_EBOUNDS -6     /* device word: a device-side bounds check failed */
