@@ -22,10 +22,13 @@
 // an A operand run as one MMA of N = 128 by stacking the B operands:
 //   S' = Q_hi [K_hi; K_lo]^T  (N = 128)   then  S'[:, :64] += Q_lo K_hi^T
 //   S  = S'[:, :64] + S'[:, 64:]            (summed by the softmax warps)
-//   O' += P_hi [V_hi^T; V_lo^T]^T (N = 128) then O'[:, :64] += P_lo V_hi^T
+//   O' += P_hi [V_hi V_lo]  (N = 128)     then  O'[:, :64] += P_lo V_hi
 //   O  = O'[:, :64] + O'[:, 64:]            (summed in the epilogue)
-// Q hi/lo and K, V^T are 128-byte-swizzled K-major shared-memory operands; P
-// is a TMEM operand (P hi and P lo overwrite the S columns they came from).
+// Q hi/lo and K are 128-byte-swizzled K-major shared-memory operands, V an
+// MN-major one (rows are keys, as TMA lands them, swizzled in 32-byte chunks
+// as MN-major 32-bit operands must be), and the tensor core reads
+// raw K and V as their tf32 hi parts by itself; P is a TMEM operand (P hi and
+// P lo overwrite the S columns they came from).
 // TMEM holds three S buffers (QK runs up to two tiles ahead of the softmax)
 // and O'.
 //
@@ -37,10 +40,10 @@
 //   4     K producer: TMA loads of K tiles into the K ring.
 //   5     QK issuer: allocates TMEM; one lane issues QK(n) as soon as K(n) is
 //         converted and S buffer n % 3 is free (PV(n-3) complete).
-//   6     V producer: TMA loads of V tiles into the raw V ring.
+//   6     V producer: TMA loads of V tiles into the V ring.
 //   7-8   K converters: K lo next to each K tile (one d-half each).
-//   9-10  V converters: raw V -> V^T hi / V^T lo (one d-half each).
-//   11    PV issuer: one lane issues PV(n) as soon as P(n) and V^T(n) are ready.
+//   9-10  V converters: V lo next to each V tile (one d-half each).
+//   11    PV issuer: one lane issues PV(n) as soon as P(n) and V lo(n) are ready.
 // The two issuers are separate threads so that neither stream of MMAs waits
 // behind the other's inputs: the tensor core's issue queue is shallow, and a
 // single issuer that blocks on one condition leaves the pipe idle.
@@ -63,8 +66,7 @@ constexpr int kBq = 32;           // chunk positions per unit
 constexpr int kM = kBq * kGroup;  // 128 rows = TMEM lanes
 constexpr int kBc = 64;           // keys per tile
 constexpr int kKStages = 2;       // K ring: [K | K lo] per d-half region
-constexpr int kVRawStages = 2;    // raw V landing ring
-constexpr int kVStages = 2;       // V^T ring: [V^T hi | V^T lo] per key-half region
+constexpr int kVStages = 3;       // V ring: [V | V lo], each as two d-half regions
 constexpr int kNumS = 3;          // S / P buffers in TMEM
 
 constexpr int kSoftmaxWarps = 4;
@@ -89,15 +91,13 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kRegion = 128 * 128;                  // 16 KB: 128 rows
 constexpr uint32_t kHalf = 64 * 128;                     // 8 KB: 64 rows
 constexpr uint32_t kKStageBytes = 2 * kRegion;           // 2 d-half regions
-constexpr uint32_t kVRawBytes = 2 * kHalf;               // 2 d-half regions of 64 keys
-constexpr uint32_t kVStageBytes = 2 * kRegion;           // 2 key-half regions
+constexpr uint32_t kVStageBytes = 4 * kHalf;            // V d-halves 0, 1, then V lo d-halves 0, 1
 constexpr uint32_t kSmemQ = 0;                           // Q hi (two d-half regions), then Q lo
 constexpr uint32_t kQTermBytes = 2 * kRegion;             // 32 KB per term
 constexpr uint32_t kSmemK = kSmemQ + 2 * kQTermBytes;
-constexpr uint32_t kSmemVRaw = kSmemK + kKStages * kKStageBytes;
-constexpr uint32_t kSmemVT = kSmemVRaw + kVRawStages * kVRawBytes;
-constexpr uint32_t kSmemBar = kSmemVT + kVStages * kVStageBytes;
-constexpr uint32_t kNumBars = 3 * kKStages + 2 * kVRawStages + 2 * kVStages + 3 * kNumS + 1 + 2 + 2;
+constexpr uint32_t kSmemV = kSmemK + kKStages * kKStageBytes;
+constexpr uint32_t kSmemBar = kSmemV + kVStages * kVStageBytes;
+constexpr uint32_t kNumBars = 3 * kKStages + 3 * kVStages + 3 * kNumS + 1 + 2 + 2;
 constexpr uint32_t kSmemSlot = kSmemBar + kNumBars * 8 + 16;  // tail kernel: rank 1's m and l per row
 constexpr uint32_t kSmemTotal = kSmemSlot + 2 * kM * 4;
 constexpr uint32_t kSmemAlloc = kSmemTotal + 1024;  // slack to align the base
@@ -107,6 +107,8 @@ static_assert(kM == 128 && kD == 64 && kBc == 64, "the MMA shapes below assume 1
 
 constexpr uint32_t kIdescN128 = idesc_tf32(128, 128);
 constexpr uint32_t kIdescN64 = idesc_tf32(128, 64);
+constexpr uint32_t kIdescPvN128 = idesc_tf32(128, 128, true);  // B (V) MN-major
+constexpr uint32_t kIdescPvN64 = idesc_tf32(128, 64, true);
 // Keep a stale reference maximum while the new maximum exceeds it by at most
 // this much in log2 units (p stays <= 2^8): l and O share the reference, so
 // O / l is exact either way, and O needs no rescale.
@@ -132,9 +134,8 @@ struct Bars {
   uint64_t* kfull;   // [kKStages] TMA K landed
   uint64_t* kconv;   // [kKStages] K lo written
   uint64_t* kempty;  // [kKStages] QK done with the stage (MMA commit)
-  uint64_t* vfull;   // [kVRawStages] TMA V landed
-  uint64_t* vrfree;  // [kVRawStages] V converters done reading raw V
-  uint64_t* vconv;   // [kVStages] V^T hi/lo written
+  uint64_t* vfull;   // [kVStages] TMA V landed
+  uint64_t* vconv;   // [kVStages] V lo written (and V rows past the sequence zeroed)
   uint64_t* vempty;  // [kVStages] PV done with the stage (MMA commit)
   uint64_t* sfull;   // [kNumS] S buffer written (MMA commit)
   uint64_t* pfull;   // [kNumS] P hi/lo written and O rescaled (softmax warps)
@@ -151,8 +152,7 @@ __device__ __forceinline__ Bars carve_bars(uint8_t* base) {
   r.kfull = b; b += kKStages;
   r.kconv = b; b += kKStages;
   r.kempty = b; b += kKStages;
-  r.vfull = b; b += kVRawStages;
-  r.vrfree = b; b += kVRawStages;
+  r.vfull = b; b += kVStages;
   r.vconv = b; b += kVStages;
   r.vempty = b; b += kVStages;
   r.sfull = b; b += kNumS;
@@ -347,11 +347,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
       mbar_init(&bars.kconv[s], kKConvWarps);
       mbar_init(&bars.kempty[s], 1);
     }
-    for (int s = 0; s < kVRawStages; ++s) {
-      mbar_init(&bars.vfull[s], 1);
-      mbar_init(&bars.vrfree[s], kVConvWarps);
-    }
     for (int s = 0; s < kVStages; ++s) {
+      mbar_init(&bars.vfull[s], 1);
       mbar_init(&bars.vconv[s], kVConvWarps);
       mbar_init(&bars.vempty[s], 1);
     }
@@ -401,7 +398,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
     // its two boxes); otherwise lane 0 issues the whole tile.
     constexpr int kLanes = kMode == kPaged ? kBc / kPage : 1;
     if (lane < kLanes) {
-      const int stages = is_k ? kKStages : kVRawStages;
+      const int stages = is_k ? kKStages : kVStages;
       int n = 0;
       for (int k = 0;; ++k) {
         const int u = work_unit<kMode>(k, cta, grid, prm);
@@ -411,7 +408,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
         unit_range<kMode>(w, rank, &jb, &je);
         for (int j = jb; j < je; ++j, ++n) {
           const int st = n % stages;
-          uint64_t* freed = is_k ? &bars.kempty[st] : &bars.vrfree[st];
+          uint64_t* freed = is_k ? &bars.kempty[st] : &bars.vempty[st];
           if constexpr (kMode == kPaged) {
             // The four lanes leave together or not at all.
             const bool ok = n < stages || wait_bar(freed, ((n / stages) - 1) & 1, prm, abort_flag);
@@ -422,7 +419,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
           if (is_k && prm.fault_skip_first_k && n == 0) continue;
           const CUtensorMap* map = is_k ? &tmk : &tmv;
           uint64_t* full = is_k ? &bars.kfull[st] : &bars.vfull[st];
-          uint8_t* dst = is_k ? smem + kSmemK + st * kKStageBytes : smem + kSmemVRaw + st * kVRawBytes;
+          uint8_t* dst = is_k ? smem + kSmemK + st * kKStageBytes : smem + kSmemV + st * kVStageBytes;
           const uint32_t half_stride = is_k ? kRegion : kHalf;  // d-half regions
           if constexpr (kMode == kPaged) {
             // Lane 0 posts the tile's bytes before any of its boxes is issued.
@@ -520,24 +517,26 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
             mma_commit(&bars.sfull[sb]);
             mma_commit(&bars.kempty[ks]);
           } else {
-            // PV(n): P(n) written by the softmax warps, V^T(n) converted.
+            // PV(n): P(n) written by the softmax warps, V lo(n) written.
+            // Keys 8s .. 8s + 7 are rows 8s .. 8s + 7 (one 1024-byte atom)
+            // of each 8 KB d-half region; the regions in stage order (V 0-31,
+            // V 32-63, V lo 0-31, V lo 32-63) are the B operand's N blocks.
             const int vs = n % kVStages;
             const int sb = n % kNumS;
             if (!wait_bar(&bars.pfull[sb], (n / kNumS) & 1, prm, abort_flag)) goto mma_done;
             if (!wait_bar(&bars.vconv[vs], (n / kVStages) & 1, prm, abort_flag)) goto mma_done;
             tc_fence_after();
-            const uint32_t vt = smem_u32(smem + kSmemVT + vs * kVStageBytes);
+            const uint32_t vb = smem_u32(smem + kSmemV + vs * kVStageBytes);
             const uint32_t phi = tmem + kColS + sb * 128;
             const uint32_t plo = phi + 64;
             const bool first = j == jb;
 #pragma unroll
             for (int s = 0; s < 8; ++s)  // [P_hi V_hi | P_hi V_lo]
-              mma_tf32_ts(tmem + kColO, phi + s * 8, sdesc_sw128(vt + (s >> 2) * kRegion + (s & 3) * 32),
-                          kIdescN128, (first && s == 0) ? 0u : 1u);
+              mma_tf32_ts(tmem + kColO, phi + s * 8, sdesc_sw128a32_mn(vb + s * 1024, kHalf), kIdescPvN128,
+                          (first && s == 0) ? 0u : 1u);
 #pragma unroll
             for (int s = 0; s < 8; ++s)  // += P_lo V_hi into the first half
-              mma_tf32_ts(tmem + kColO, plo + s * 8, sdesc_sw128(vt + (s >> 2) * kRegion + (s & 3) * 32),
-                          kIdescN64, 1);
+              mma_tf32_ts(tmem + kColO, plo + s * 8, sdesc_sw128a32_mn(vb + s * 1024, kHalf), kIdescPvN64, 1);
             mma_commit(&bars.odone[sb]);
             mma_commit(&bars.vempty[vs]);
           }
@@ -589,18 +588,13 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
   kconv_done:;
   } else if (warp >= kFirstVConvWarp) {
     // ---------------------------------------------------------- V converters
-    // Raw V [key][d] (two d-half regions of 64 keys) -> V^T [d][key] in two
-    // key-half regions, hi rows 0-63 and lo rows 64-127. This warp takes the
-    // d-half cw; a lane owns a block of 4 keys x 4 head dimensions per round
-    // and turns four 16-byte row loads into four 16-byte transposed stores
-    // (hi and lo). 16-byte accesses are served per quarter-warp, so lane x of
-    // a quarter takes key quad x and d-quad (x + t) mod 8: under the 128-byte
-    // swizzle both its loads and its stores then fall in 8 distinct 16-byte
-    // bank groups. Quarter q in round rd covers key half kh = (q + 4 rd) / 8
-    // and diagonal t = (q + 4 rd) mod 8: all 2 x 8 x 8 blocks, once each.
+    // V lo = V - tf32_hi(V) into the stage's second half; warp cw takes d-half
+    // cw. In a tile that reaches past the sequence, the rows of keys at or
+    // past P + C are zeroed first, in V and V lo: they carry zero weight, but
+    // 0 * NaN is NaN and the unused slots of a cache page need not hold finite
+    // values. (A row of the swizzled region is one key: the swizzle only
+    // permutes the 16-byte chunks within it.)
     const int cw = warp - kFirstVConvWarp;
-    const uint32_t x = (uint32_t)(lane & 7);
-    const int quarter = lane >> 3;
     int n = 0;
     for (int k = 0;; ++k) {
       const int u = work_unit<kMode>(k, cta, grid, prm);
@@ -609,50 +603,29 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
       int jb, je;
       unit_range<kMode>(w, rank, &jb, &je);
       for (int j = jb; j < je; ++j, ++n) {
-        const int vr = n % kVRawStages;
         const int vs = n % kVStages;
-        if (!wait_bar_warp(&bars.vfull[vr], (n / kVRawStages) & 1, prm, abort_flag)) goto vconv_done;
-        if (n >= kVStages && !wait_bar_warp(&bars.vempty[vs], ((n / kVStages) - 1) & 1, prm, abort_flag))
-          goto vconv_done;
-        const uint8_t* vraw = smem + kSmemVRaw + vr * kVRawBytes + cw * kHalf;  // this warp's d-half
-        uint8_t* vt = smem + kSmemVT + vs * kVStageBytes;
-        float4 xv[4][4];  // [round][key within the quad]
+        if (!wait_bar_warp(&bars.vfull[vs], (n / kVStages) & 1, prm, abort_flag)) goto vconv_done;
+        uint8_t* vb = smem + kSmemV + vs * kVStageBytes + cw * kHalf;
+        float4 x[16];
 #pragma unroll
-        for (int rd = 0; rd < 4; ++rd) {
-          const uint32_t combo = (uint32_t)(quarter + 4 * rd);
-          const uint32_t key0 = (combo >> 3) * 32u + 4u * x;
-          const uint32_t d4 = (x + combo) & 7u;
+        for (int i = 0; i < 16; ++i) x[i] = *reinterpret_cast<const float4*>(vb + (uint32_t)(lane + 32 * i) * 16u);
+        if ((j + 1) * kBc > p.P + p.C) {
 #pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            xv[rd][r] = *reinterpret_cast<const float4*>(vraw + sw128((key0 + r) * 128u + d4 * 16u));
-            // Keys at or past P + C carry zero weight, but 0 * NaN is NaN: the
-            // unused slots of a cache page need not hold finite values.
-            if (j * kBc + (int)(key0 + r) >= p.P + p.C) xv[rd][r] = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int i = 0; i < 16; ++i) {
+            if (j * kBc + ((lane + 32 * i) >> 3) >= p.P + p.C) {
+              x[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+              *reinterpret_cast<float4*>(vb + (uint32_t)(lane + 32 * i) * 16u) = x[i];
+            }
           }
         }
 #pragma unroll
-        for (int rd = 0; rd < 4; ++rd) {
-          const uint32_t combo = (uint32_t)(quarter + 4 * rd);
-          const uint32_t kh = combo >> 3;
-          const uint32_t d0 = (uint32_t)(cw * 32) + 4u * ((x + combo) & 7u);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float e0 = i == 0 ? xv[rd][0].x : i == 1 ? xv[rd][0].y : i == 2 ? xv[rd][0].z : xv[rd][0].w;
-            const float e1 = i == 0 ? xv[rd][1].x : i == 1 ? xv[rd][1].y : i == 2 ? xv[rd][1].z : xv[rd][1].w;
-            const float e2 = i == 0 ? xv[rd][2].x : i == 1 ? xv[rd][2].y : i == 2 ? xv[rd][2].z : xv[rd][2].w;
-            const float e3 = i == 0 ? xv[rd][3].x : i == 1 ? xv[rd][3].y : i == 2 ? xv[rd][3].z : xv[rd][3].w;
-            const float4 hi = make_float4(tf32_hi(e0), tf32_hi(e1), tf32_hi(e2), tf32_hi(e3));
-            const uint32_t off = kh * kRegion + sw128((d0 + (uint32_t)i) * 128u + x * 16u);
-            *reinterpret_cast<float4*>(vt + off) = hi;
-            *reinterpret_cast<float4*>(vt + off + kHalf) = make_float4(e0 - hi.x, e1 - hi.y, e2 - hi.z, e3 - hi.w);
-          }
-        }
+        for (int i = 0; i < 16; ++i)
+          *reinterpret_cast<float4*>(vb + (uint32_t)(lane + 32 * i) * 16u + 2 * kHalf) =
+              make_float4(x[i].x - tf32_hi(x[i].x), x[i].y - tf32_hi(x[i].y), x[i].z - tf32_hi(x[i].z),
+                          x[i].w - tf32_hi(x[i].w));
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&bars.vrfree[vr]);
-          mbar_arrive(&bars.vconv[vs]);
-        }
+        if (lane == 0) mbar_arrive(&bars.vconv[vs]);
       }
     }
   vconv_done:;
@@ -863,7 +836,10 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
 // k, v [rows][8][64] as a 2-D tensor (head * 64 + d, row); a box is 32 floats
 // (one 128-byte swizzle row) x box_rows rows: 64 keys of a contiguous cache, or
 // one 16-token page of a paged cache ([pages * 16][8][64]).
-int encode_kv_map(const float* base, int rows, int box_rows, CUtensorMap* map) {
+// K lands in the 128-byte swizzle of K-major operands; V, an MN-major tf32
+// operand, in the 128-byte swizzle of 32-byte chunks that the tensor core
+// requires of MN-major 32-bit operands.
+int encode_kv_map(const float* base, int rows, int box_rows, CUtensorMapSwizzle swizzle, CUtensorMap* map) {
   auto enc = get_encoder();
   if (!enc) return ATTN_ETMA;
   const cuuint32_t ones[2] = {1, 1};
@@ -871,7 +847,7 @@ int encode_kv_map(const float* base, int rows, int box_rows, CUtensorMap* map) {
   const cuuint64_t strides[1] = {(cuuint64_t)kHKV * kD * 4};
   const cuuint32_t box[2] = {32, (cuuint32_t)box_rows};
   if (enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, ones,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return ATTN_ETMA;
   return ATTN_OK;
@@ -909,8 +885,8 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
   alignas(64) CUtensorMap mk, mv;
   const int rows = table ? num_pages * kPage : p.P + p.C;
   const int box_rows = table ? kPage : kBc;
-  int rc = encode_kv_map(p.k, rows, box_rows, &mk);
-  if (rc == ATTN_OK) rc = encode_kv_map(p.v, rows, box_rows, &mv);
+  int rc = encode_kv_map(p.k, rows, box_rows, CU_TENSOR_MAP_SWIZZLE_128B, &mk);
+  if (rc == ATTN_OK) rc = encode_kv_map(p.v, rows, box_rows, CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B, &mv);
   if (rc != ATTN_OK) return rc;
   Params prm;
   prm.p = p;

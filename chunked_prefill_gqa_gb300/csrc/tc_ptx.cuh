@@ -210,27 +210,47 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr) {
   return d;
 }
 
-// Instruction descriptor for kind::tf32, fp32 accumulate, both operands
-// K-major, dense. Bits: [4,6) D format (1 = f32), [7,10) A format (2 = tf32),
-// [10,13) B format, [15] A transpose, [16] B transpose, [17,23) N >> 3,
-// [24,29) M >> 4.
-__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
-  return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+// Instruction descriptor for kind::tf32, fp32 accumulate, dense, A K-major,
+// B K-major or (b_mn_major) MN-major. Bits: [4,6) D format (1 = f32), [7,10)
+// A format (2 = tf32), [10,13) B format, [15] A transpose, [16] B transpose,
+// [17,23) N >> 3, [24,29) M >> 4.
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N, bool b_mn_major = false) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
 }
 
-// Shared-memory descriptor of an MN-major 16-bit operand in the 128-byte
-// swizzled canonical layout: each 128-byte row holds 64 consecutive M/N
-// elements of one K index, 8 K rows form a 1024-byte swizzle atom, and atoms
-// follow each other along K every 1024 bytes (stride-dimension offset). The
-// leading-dimension offset (the next 64 M/N elements) is also set to 1024: an
-// operand of N = 64 spans a single atom along N and never uses it.
-__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t smem_addr) {
+// Shared-memory descriptor of an MN-major operand in the 128-byte swizzled
+// canonical layout: each 128-byte row holds the consecutive M/N elements of
+// one K index (64 of 16 bits, 32 of 32 bits), 8 K rows form a 1024-byte
+// swizzle atom, and atoms follow each other along K every 1024 bytes (the
+// stride-dimension offset). The leading-dimension offset is the distance to
+// the atom of the next 128 bytes of M/N elements; an operand that spans a
+// single atom along M/N never uses it.
+__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t smem_addr, uint32_t lbo_bytes = 1024) {
   uint64_t d = 0;
   d |= (uint64_t)((smem_addr & 0x3FFFF) >> 4);
-  d |= (uint64_t)(1024 >> 4) << 16;
+  d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFF) << 16;
   d |= (uint64_t)(1024 >> 4) << 32;
   d |= (uint64_t)1 << 46;
   d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// The same for an MN-major 32-bit (tf32) operand, which the tensor core reads
+// only in the 128-byte swizzle of 32-byte chunks (layout type 1 in bits
+// [61,64); TMA writes it with CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B): rows of 32
+// M/N elements per K index, chunk c of row r at chunk c ^ (r mod 4), so an
+// atom is 4 rows (512 bytes) and consecutive K rows take a stride-dimension
+// offset of 512; the atom of the next 32 M/N elements is lbo_bytes further.
+// (Measured on GB300 with a selection-matrix product: with the offset at 1024,
+// K indices 4-7 came from rows 8-11.)
+__device__ __forceinline__ uint64_t sdesc_sw128a32_mn(uint32_t smem_addr, uint32_t lbo_bytes) {
+  uint64_t d = 0;
+  d |= (uint64_t)((smem_addr & 0x3FFFF) >> 4);
+  d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)(512 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)1 << 61;
   return d;
 }
 
