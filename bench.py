@@ -633,10 +633,14 @@ def main():
         e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in zip(es, ee)), dev) / n_e2e
         # The host path runs the chunk as sub-chunks; the device call may split
         # its last round's units over CTA pairs (another summation order), so
-        # the two agree to rounding, far inside the oracle's tolerance.
+        # the two agree to rounding, far inside the oracle's tolerance. An
+        # output is a weighted mean of V rows, so its rounding scales with
+        # max |v| (here about 4), not with the output, which averaging over a
+        # long prefix makes small: the bound is 1e-5 (max |v| + |out|).
         dev_out = out.cpu().numpy()
         diff = float(np.max(np.abs(hout.numpy() - dev_out)))
-        ok = bool(np.allclose(hout.numpy(), dev_out, rtol=1e-5, atol=1e-6))
+        vmax = float(np.max(np.abs(inp.v)))
+        ok = bool(np.all(np.abs(hout.numpy() - dev_out) <= 1e-5 * (vmax + np.abs(dev_out))))
         e2e = {"value": world * flops / (e_ms * 1e-3) / 1e12, "unit": UNIT,
                "ms_per_step": e_ms, "steps": n_e2e,
                "h2d_bytes_per_step": int(hq.numel() * 4 + (hk.numel() + hv.numel()) * hk.element_size()),
