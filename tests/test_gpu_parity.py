@@ -60,6 +60,27 @@ def test_edge_sweep(cp, path, C, P, variant):
     _check(got, oracle.prefill(inp), f"{path} {inp.name}")
 
 
+@pytest.mark.parametrize("term", W.SPLIT_TERM_CASES)
+@pytest.mark.parametrize("path", ["attn_prefill", "attn_prefill_paged", "attn_prefill_ffma"])
+def test_split_term_cases(cp, path, term):
+    """Inputs on which a product that lost one lo part (of q, k, p or v) misses
+    the tolerance on most outputs (shown on the CPU by test_split_terms.py), so
+    passing them shows that the split-TF32 kernel carries every part; the FFMA
+    path computes in fp32 and must pass them too."""
+    inp = W.split_term_case(term)
+    if path == "attn_prefill_paged":
+        pg = W.to_pages(inp, seed=5)
+        kp, vp = torch.from_numpy(pg.k_pages).cuda(), torch.from_numpy(pg.v_pages).cuda()
+        tb = torch.from_numpy(pg.table).cuda()
+        fn = lambda q, k, v, out, P, stream: cp.attn_prefill_paged(q, kp, vp, tb, out, P, stream)
+    else:
+        fn = getattr(cp, path)
+    got, guards = run_entry(fn, inp)
+    assert guards
+    rep = _check(got, oracle.prefill(inp), f"{path} {inp.name}")
+    print(f"{path} {inp.name}: worst err/tol {rep['worst_ratio']:.3g}")
+
+
 @pytest.mark.parametrize("T", W.FULL_T_SMALL + W.FULL_T)
 @pytest.mark.parametrize("path", ["attn_prefill", "attn_prefill_bf16x3", "attn_prefill_ffma"])
 def test_full_causal(cp, path, T):

@@ -196,6 +196,47 @@ def long_prefix(seed: int = 1, C: int = 2048, P: int = 30720) -> Inputs:
     return make_inputs(C, P, seed, "normal", name=f"long C={C} P={P}")
 
 
+SPLIT_TERM_CASES = ("q", "k", "pv")
+
+
+def split_term_case(term: str, seed: int = 11) -> Inputs:
+    """Inputs on which each part of an error-compensated split-precision product
+    matters: an operand x carried as hi + lo (hi = x with its 13 low mantissa
+    bits cleared, tf32) must keep both parts, and these cases are built so that
+    dropping the lo part of one operand moves most outputs outside the oracle's
+    tolerance while the scores keep a moderate spread.
+
+    "q": q = 1 + u/16 (full 24-bit mantissas), k = +-32 with the signs of dims
+    32..63 the negation of dims 0..31, so q.k is small but the lo part of q
+    moves every score by about 1e-2. C = P = 64.
+    "k": the roles swapped: q = +-32, k = 1 + u/16. C = P = 64.
+    "pv": one chunk row at P = 1 against two keys of nearly equal score (key 0
+    is key 1 plus u/64) whose value rows are 8 (1 + u/16) and -8 (1 + u'/16):
+    the output nearly cancels, so the lo parts of the probabilities and of V
+    each show at the scale of |v| = 8.
+    """
+    if term == "q":
+        inp = make_inputs(64, 64, seed)
+        q = (1.0 + inp.q.astype(np.float64) / 16.0).astype(np.float32)
+        sign = np.where(inp.k[:, :, :32] >= 0, 32.0, -32.0)
+        k = np.concatenate([sign, -sign], axis=2).astype(np.float32)
+        return Inputs(q=q, k=k, v=inp.v, C=64, P=64, name="split-term q")
+    if term == "k":
+        inp = make_inputs(64, 64, seed)
+        q = np.where(inp.q >= 0, 32.0, -32.0).astype(np.float32)
+        k = (1.0 + inp.k.astype(np.float64) / 16.0).astype(np.float32)
+        return Inputs(q=q, k=k, v=inp.v, C=64, P=64, name="split-term k")
+    if term == "pv":
+        inp = make_inputs(1, 1, seed)
+        k = inp.k.copy()
+        k[0] = (k[1].astype(np.float64) + uniform(seed + 7, HKV * D).reshape(HKV, D) / 64.0).astype(np.float32)
+        v = np.empty_like(inp.v)
+        v[0] = (8.0 * (1.0 + inp.v[0].astype(np.float64) / 16.0)).astype(np.float32)
+        v[1] = (-8.0 * (1.0 + inp.v[1].astype(np.float64) / 16.0)).astype(np.float32)
+        return Inputs(q=inp.q, k=k, v=v, C=1, P=1, name="split-term pv")
+    raise ValueError(term)
+
+
 EDGE_C = (1, 17, 33, 64)
 EDGE_P = (0, 31, 1000)
 FULL_T = (512, 1024, 2048)
