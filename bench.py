@@ -74,6 +74,9 @@ def parse_args():
     ap.add_argument("--seed", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-peak", action="store_true",
+                    help="skip the live tensor-pipe rate measurement (the tf32 roofline then uses "
+                         "the measured bf16 peak x the nominal tf32/bf16 ratio)")
     ap.add_argument("--no-compare", action="store_true",
                     help="skip timing the FFMA path and the starter reference on the same inputs "
                          "(the page's SPEEDUP of the kernel over its starter design)")
@@ -196,6 +199,50 @@ def load_peaks():
             "sm_max_mhz": 2070.0, "source": "fallback"}
 
 
+TENSOR_PEAK_SHAPES = (("tf32", 128), ("tf32", 256), ("bf16", 256))
+
+
+def measure_tensor_peaks(cp, torch, stream, sms: int, target_ms: float = 20.0, reps: int = 10):
+    """The tensor pipe's dense rate on this GPU, measured live: every SM issues
+    M = 128, N = n tcgen05.mma instructions back to back (attn_tensor_peak),
+    each launch about `target_ms` long, 3 warm-up launches, then `reps` timed
+    with CUDA events; the median launch gives the rate. tf32 is the split-TF32
+    kernel's instruction kind (no library GEMM reports it); bf16 at N = 256
+    sits beside the driver's cuBLAS bf16 figure as a check of the method."""
+    out = {}
+    for kind, n in TENSOR_PEAK_SHAPES:
+        bf16 = kind == "bf16"
+        probe = 4096
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        cp.attn_tensor_peak(bf16, n, probe, sms, stream)
+        e0.record(stream)
+        cp.attn_tensor_peak(bf16, n, probe, sms, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        iters = int(min(1 << 22, max(probe, probe * target_ms / max(e0.elapsed_time(e1), 1e-3))))
+        for _ in range(3):
+            flops = cp.attn_tensor_peak(bf16, n, iters, sms, stream)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for a, b in ev:
+            a.record(stream)
+            cp.attn_tensor_peak(bf16, n, iters, sms, stream)
+            b.record(stream)
+        torch.cuda.synchronize()
+        ms = sorted(a.elapsed_time(b) for a, b in ev)
+        med = statistics.median(ms)
+        out[f"{kind}_n{n}"] = {"tflops": round(flops / (med * 1e-3) / 1e12, 2),
+                               "tflops_best": round(flops / (ms[0] * 1e-3) / 1e12, 2),
+                               "ms_median": round(med, 4), "iters": iters, "ctas": sms}
+    if cp.attn_get_device_error() != 0:
+        raise RuntimeError("device error in the tensor-peak measurement")
+    return out
+
+
+def tf32_peak_from(measured):
+    """The dense kind::tf32 peak: the faster of the N = 128 and N = 256 loops."""
+    return max(measured["tf32_n128"]["tflops"], measured["tf32_n256"]["tflops"])
+
+
 def kernel_source_hash(path_name: str) -> str:
     """Hash of the kernel source a profile was taken on (traffic goes stale with it)."""
     fname = {"attn_prefill": "tc.cu", "attn_prefill_bf16kv": "tc_bf16.cu", "attn_prefill_bf16x3": "tc_bf16.cu",
@@ -249,11 +296,19 @@ def roofline(path_name: str, kernel: str, flops: float, ms: float, peaks, worklo
              "tensor_passes": 3 if kernel.startswith("tcgen05-bf16x3") else 2,
              "frac_of_split_roof": None}
     elif kernel.startswith("tcgen05-split-tf32"):
-        peak = peaks["bf16_tflops"] * NOMINAL_TF32 / NOMINAL_BF16
-        r = {"bound": "tensor", "peak_dtype": "tf32",
-             "peak_note": f"{peaks['source']} bf16 burst x {NOMINAL_TF32}/{NOMINAL_BF16} (nominal tf32/bf16)",
+        nominal = peaks["bf16_tflops"] * NOMINAL_TF32 / NOMINAL_BF16
+        if peaks.get("tf32_tflops"):
+            peak = peaks["tf32_tflops"]
+            note = ("measured in this run: dense kind::tf32 tcgen05.mma loop on every SM "
+                    f"(attn_tensor_peak, best of N = 128 / 256, median of 10 launches)")
+        else:
+            peak = nominal
+            note = f"{peaks['source']} bf16 burst x {NOMINAL_TF32}/{NOMINAL_BF16} (nominal tf32/bf16)"
+        r = {"bound": "tensor", "peak_dtype": "tf32", "peak_note": note,
              "tensor_passes": 3,
-             "frac_of_split_roof": None}
+             "frac_of_split_roof": None,
+             "peak_nominal_ratio": round(nominal, 3),
+             "frac_of_nominal_ratio_peak": round(achieved / nominal, 4)}
     else:
         # FP32 FFMA pipe: 152 SMs x 128 lanes x 2 flop per clock at the maximum SM clock.
         peak = NUM_SMS * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
@@ -325,7 +380,8 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": desc, "C": inp.C, "P": inp.P, "parallelism": "host cores"},
+            "config": {"workload": desc, "C": inp.C, "P": inp.P, "hq": W.HQ, "hkv": W.HKV, "d": W.D,
+                       "path": "oracle", "parallelism": "host cores"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads() if threads <= 0 else threads,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -448,13 +504,26 @@ def run_matrix(args):
         ms = [sum(ev[i][j][0].elapsed_time(ev[i][j][1]) for i in range(n)) / n for j in range(len(steps))]
         visible = 32 * T * (T + 1) // 2
         matrix = 32 * T * T * 4
+        # What the matrix itself costs, apart from the contractions: its bytes
+        # through HBM (the scores kernel writes all of it, the softmax reads
+        # the visible part and writes all of it back, the weighted sum reads
+        # the visible part) at the measured copy bandwidth, against the two
+        # contractions (2 x 64 flop per visible pair each) at the FFMA peak.
+        matrix_bytes = matrix + 4 * visible + matrix + 4 * visible
+        matrix_ms = matrix_bytes / (peaks["hbm_gbs"] * 1e9) * 1e3
+        contraction_ms = 2 * (2 * 64 * visible) / (ffma_peak * 1e12) * 1e3
         table.append({
             "T": T, "matrix_mib": matrix / 2**20,
             "scores_ms": round(ms[0], 4), "softmax_ms": round(ms[1], 4), "weighted_sum_ms": round(ms[2], 4),
             "pipeline_ms": round(ms[0] + ms[1] + ms[2], 4), "flash_ms": round(ms[3], 4),
             "scores_tflops": round(2 * 64 * visible / (ms[0] * 1e-3) / 1e12, 2),
             "softmax_gbs": round((4 * visible + matrix) / (ms[1] * 1e-3) / 1e9, 1),
-            "weighted_sum_tflops": round(2 * 64 * visible / (ms[2] * 1e-3) / 1e12, 2)})
+            "weighted_sum_tflops": round(2 * 64 * visible / (ms[2] * 1e-3) / 1e12, 2),
+            "matrix_traffic_bytes": matrix_bytes,
+            "matrix_traffic_ms_at_hbm_peak": round(matrix_ms, 4),
+            "contractions_ms_at_ffma_peak": round(contraction_ms, 4),
+            "matrix_traffic_over_flash": round(matrix_ms / ms[3], 2),
+            "split_note": "pipeline time = matrix traffic + contractions at best; flash_ms has no matrix"})
         del ws
         torch.cuda.empty_cache()
     t_end = time.time()
@@ -641,12 +710,38 @@ def main():
         diff = float(np.max(np.abs(hout.numpy() - dev_out)))
         vmax = float(np.max(np.abs(inp.v)))
         ok = bool(np.all(np.abs(hout.numpy() - dev_out) <= 1e-5 * (vmax + np.abs(dev_out))))
+        h2d_bytes = int(hq.numel() * 4 + (hk.numel() + hv.numel()) * hk.element_size())
+        d2h_bytes = int(hout.numel()) * 4
+        # The link's own rates on this machine: the step's copies alone, one
+        # cudaMemcpyAsync per buffer (pinned host memory), best of 5. A step can
+        # take no less than the slowest of its copy-in, its copy-out (the two
+        # directions run at once) and its compute, so that maximum bounds e2e.
+        def copy_ms(fn_copy):
+            best = float("inf")
+            for _ in range(6):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn_copy()
+                b.record(stream)
+                torch.cuda.synchronize()
+                best = min(best, a.elapsed_time(b))
+            return best
+        h2d_ms = copy_ms(lambda: (dq.copy_(hq, non_blocking=True), dk.copy_(hk, non_blocking=True),
+                                  dv.copy_(hv, non_blocking=True)))
+        d2h_ms = copy_ms(lambda: hout.copy_(dout, non_blocking=True))
+        bound_ms, bound_by = max((h2d_ms, "host-to-device copy"), (d2h_ms, "device-to-host copy"),
+                                 (ms_mean, "compute"))
         e2e = {"value": world * flops / (e_ms * 1e-3) / 1e12, "unit": UNIT,
                "ms_per_step": e_ms, "steps": n_e2e,
-               "h2d_bytes_per_step": int(hq.numel() * 4 + (hk.numel() + hv.numel()) * hk.element_size()),
-               "d2h_bytes_per_step": int(hout.numel()) * 4,
+               "h2d_bytes_per_step": h2d_bytes,
+               "d2h_bytes_per_step": d2h_bytes,
                "api": (args.path + "_host") if host_fn is not None else f"copies + {args.path}",
-               "matches_device_timed_output": ok, "max_abs_diff_vs_device_timed_output": diff}
+               "matches_device_timed_output": ok, "max_abs_diff_vs_device_timed_output": diff,
+               "link": {"h2d_gbs": round(h2d_bytes / (h2d_ms * 1e-3) / 1e9, 1),
+                        "d2h_gbs": round(d2h_bytes / (d2h_ms * 1e-3) / 1e9, 1),
+                        "h2d_ms": round(h2d_ms, 4), "d2h_ms": round(d2h_ms, 4), "compute_ms": round(ms_mean, 4),
+                        "bound_ms": round(bound_ms, 4), "bound": bound_by,
+                        "frac_of_bound": round(bound_ms / e_ms, 4)}}
 
     compare = None
     if not args.no_compare and rank == 0 and args.kv == "fp32" and not args.paged:
@@ -683,8 +778,28 @@ def main():
         cpu["single_thread"] = {"value": f1 / dt1 / 1e12, "unit": UNIT, "cores": 1,
                                 "sample": f"{len(rows1)} of {C} chunk rows (every 64th + last), {dt1:.2f} s"}
 
+    # The tensor pipe's measured dense rate (after every timed region, so its
+    # second of full-power MMAs cannot lower the clocks the path was timed at).
+    tensor_peaks = None
+    if rank == 0 and not args.no_peak and kernel.startswith("tcgen05"):
+        psampler = ClockSampler(dev.index if world == 1 else local)
+        psampler.start()
+        p0 = time.time()
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        tensor_peaks = measure_tensor_peaks(cp, torch, stream, sms)
+        p1 = time.time()
+        psampler.stop()
+        pclk = psampler.summary(p0, p1)
+        tensor_peaks["clocks"] = pclk
+        if pclk.get("sm_mhz"):
+            for key, val in tensor_peaks.items():
+                if key != "clocks":
+                    val["flop_per_clk_per_sm"] = round(val["tflops"] * 1e12 / (sms * pclk["sm_mhz"] * 1e6), 1)
+
     if rank == 0:
         peaks = load_peaks()
+        if tensor_peaks is not None:
+            peaks["tf32_tflops"] = tf32_peak_from(tensor_peaks)
         line = {
             "metric": METRIC if args.workload == "serve" else METRIC_LONG,
             "value": round(value, 4), "unit": UNIT, "n_gpus": world,
@@ -708,6 +823,8 @@ def main():
         }
         if compare:
             line["compare"] = compare
+        if tensor_peaks is not None:
+            line["tensor_peaks"] = tensor_peaks
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()

@@ -43,7 +43,8 @@ EXPORTS = ("attn_prefill", "attn_prefill_bf16x3", "attn_prefill_bf16kv", "attn_p
            "attn_decode_workspace_bytes", "attn_decode_paged_noalloc",
            "attn_naive_workspace_bytes", "attn_naive_scores", "attn_naive_softmax", "attn_naive_weighted_sum",
            "attn_naive_prefill", "attn_prefill_ffma", "attn_reference_prefill", "attn_selftest_timeout",
-           "attn_selftest_decode_timeout", "attn_get_device_error", "attn_strerror", "attn_version")
+           "attn_selftest_decode_timeout", "attn_tensor_peak", "attn_get_device_error", "attn_strerror",
+           "attn_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -103,6 +104,8 @@ def load():
             lib.attn_naive_prefill.argtypes = [vp, vp, vp, vp, vp, ctypes.c_size_t, ci, ci, vp]
             lib.attn_full_causal.restype = ci
             lib.attn_full_causal.argtypes = [vp, vp, vp, vp, ci, vp]
+            lib.attn_tensor_peak.restype = ci
+            lib.attn_tensor_peak.argtypes = [ci, ci, ci, ci, vp]
             lib.attn_get_device_error.restype = ci
             lib.attn_get_device_error.argtypes = []
             lib.attn_strerror.restype = ctypes.c_char_p
@@ -432,6 +435,16 @@ def attn_selftest_timeout(q, kCache, vCache, out, P: int, stream=None):
     """Run the tensor-core kernel with a load withheld so a bounded wait expires
     (a failure-path test); read the outcome with attn_get_device_error()."""
     return _call("attn_selftest_timeout", q, kCache, vCache, out, P, stream)
+
+
+def attn_tensor_peak(bf16: bool, n: int, iters: int, ctas: int, stream=None) -> float:
+    """Launch the tensor-pipe rate measurement (one CTA per SM for ctas <= SMs:
+    ``iters`` dense M = 128, N = n MMAs each, kind::tf32 or, with bf16,
+    kind::f16); returns the flops one launch performs."""
+    rc = load().attn_tensor_peak(int(bool(bf16)), int(n), int(iters), int(ctas), _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_tensor_peak")
+    return float(ctas) * iters * 2 * 128 * n * (16 if bf16 else 8)
 
 
 def attn_get_device_error() -> int:

@@ -432,6 +432,16 @@ extern "C" int attn_selftest_timeout(const float* q, const float* kCache, const 
   return launch_tc_fault_test(p, stream);
 }
 
+extern "C" int attn_tensor_peak(int bf16, int n, int iters, int ctas, cudaStream_t stream) {
+  if ((bf16 != 0 && bf16 != 1) || n < 16 || n > 256 || (n & 15) != 0 || iters < 1 || iters > (1 << 22) ||
+      ctas < 1 || ctas > 65535)
+    return ATTN_EINVAL;
+  DeviceState* st = nullptr;
+  const int rc = current_device(&st);
+  if (rc != ATTN_OK) return rc;
+  return launch_tensor_peak(bf16, n, iters, ctas, st->err, stream);
+}
+
 extern "C" int attn_get_device_error(void) {
   DeviceState* st = nullptr;
   const int rc = current_device(&st);

@@ -79,4 +79,8 @@ int launch_tc_bf16x3(const Problem& p, cudaStream_t stream);
 // Paged K/V: p.k / p.v point at [num_pages * 16][8][64] page pools.
 int launch_tc_paged(const Problem& p, const int* table, int num_pages, cudaStream_t stream);
 
+// Tensor-pipe rate measurement (peak.cu): `ctas` CTAs each issue `iters`
+// dense M = 128, N = n MMAs (kind::tf32, or kind::f16 with bf16 operands).
+int launch_tensor_peak(int bf16, int n, int iters, int ctas, unsigned* err, cudaStream_t stream);
+
 }  // namespace attn

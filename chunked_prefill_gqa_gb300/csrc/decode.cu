@@ -250,7 +250,13 @@ decode_split_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constan
     // A tile did not land in time: record it and give the copies still in
     // flight (tiles it .. it + kStages - 1: the last was issued before the
     // wait) a bounded wait before the block's shared memory is released. The
-    // output is not written.
+    // output is not written. The segment's partial record is written empty
+    // (m = -inf, l = 0), as for an empty segment, so the merge never weights
+    // whatever an earlier call left in a reused workspace or scratch.
+    if (part && tid < kGroup) {
+      part[kGroup * kD + tid] = -INFINITY;
+      part[kGroup * kD + kGroup + tid] = 0.f;
+    }
     if (tid == 0) {
       record_error(a.err, kDevErrTimeout);
       const int last = min(ntiles - 1, it + kStages - 1);

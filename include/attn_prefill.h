@@ -261,10 +261,15 @@ size_t attn_decode_workspace_bytes(int B, int maxContext, int numSplits);
  * The segment partials go to one fixed buffer of ATTN_DECODE_SCRATCH_BYTES
  * (4 MiB) that is part of the library's device image, so the call allocates
  * nothing, neither here nor in any library it calls. That buffer holds
- * B * 8 * splits records of 1056 bytes; the automatic split count keeps B * splits
- * below 2 * SMs / 8 + B, under 1 MiB on a 152-SM GB300. A call whose partials would not fit (a large
- * explicit numSplits with many sequences) returns ATTN_ESCRATCH and enqueues
- * nothing; one segment per sequence uses no scratch at all.
+ * B * 8 * splits records of 1056 bytes. The automatic split count (numSplits =
+ * 0) weighs fill against waves of the device's resident split blocks (its
+ * slot count: SMs x the blocks per SM the occupancy query reports, 3 x 152 =
+ * 456 on a GB300); when it splits at all, B * 8 * splits stays at or below 7
+ * slot counts (a sweep of B = 1 .. 65535 and maxContext = 256 .. 2^24), i.e.
+ * at most 3192 records, 3.2 MiB, on a GB300, so automatic calls fit there. A
+ * call whose partials would not fit (a large explicit numSplits with many
+ * sequences) returns ATTN_ESCRATCH and enqueues nothing; one segment per
+ * sequence uses no scratch at all.
  *
  * Sharing. All calls on a device use the same buffer, which keeps whatever the
  * last call left there (nothing in it needs to start at zero: each call writes
@@ -365,6 +370,25 @@ int attn_selftest_decode_timeout(const float *q, const float *kPages, const floa
                                  const int *contextLens, float *out, int B, int maxBlocks, int numPages,
                                  int maxContext, int numSplits, void *workspace, size_t workspaceBytes,
                                  cudaStream_t stream);
+
+/*
+ * attn_tensor_peak -- a measurement of this GPU's tensor pipe, not an
+ * attention computation: the rate against which the prefill kernels'
+ * contractions are judged compute-bound or not (page 1, "Inference Attention
+ * 2: Flash Prefill Against a Cached Prefix", What you will learn: read SM
+ * throughput to decide what bounds a kernel). Launches `ctas` CTAs (one per
+ * SM when ctas <= SMs); each issues `iters` dense tcgen05.mma instructions of
+ * M = 128, N = n back to back from shared-memory operands holding
+ * pseudo-random values, K = 8 tf32 elements (bf16 = 0: kind::tf32) or K = 16
+ * bf16 elements (bf16 = 1: kind::f16), fp32 accumulation in tensor memory.
+ * One launch performs ctas * iters * 2 * 128 * n * K flops; time it with
+ * events on `stream`. Nothing is read or written outside the CTAs' own
+ * shared and tensor memory; no device memory is allocated. Arguments: bf16
+ * 0 or 1, n a multiple of 16 in [16, 256], iters in [1, 2^22], ctas in
+ * [1, 65535] (ATTN_EINVAL otherwise). An expired completion wait (2 s) is
+ * recorded as ATTN_ETIMEOUT in the device error word.
+ */
+int attn_tensor_peak(int bf16, int n, int iters, int ctas, cudaStream_t stream);
 
 /*
  * attn_get_device_error -- synchronises the current device, then returns and

@@ -150,3 +150,14 @@ def test_decode_and_matrix_argument_checks_return_before_any_cuda_call():
     assert h(good, good, good, good, good, 1 << 30, -1, 0, None) == cp.ATTN_EINVAL
     assert h(None, None, None, None, None, 0, 0, 7, None) == cp.ATTN_OK
     assert cp.raw("attn_prefill_bf16kv")(good, good + 2, good, good, 4, 0, None) == cp.ATTN_EALIGN
+
+
+def test_tensor_peak_argument_checks_return_before_any_cuda_call():
+    f = cp.raw("attn_tensor_peak")
+    assert f(2, 128, 16, 1, None) == cp.ATTN_EINVAL       # kind is 0 (tf32) or 1 (bf16)
+    assert f(0, 0, 16, 1, None) == cp.ATTN_EINVAL         # n in [16, 256], a multiple of 16
+    assert f(0, 264, 16, 1, None) == cp.ATTN_EINVAL
+    assert f(0, 120, 16, 1, None) == cp.ATTN_EINVAL
+    assert f(0, 128, 0, 1, None) == cp.ATTN_EINVAL        # iters in [1, 2^22]
+    assert f(0, 128, (1 << 22) + 1, 1, None) == cp.ATTN_EINVAL
+    assert f(1, 256, 16, 0, None) == cp.ATTN_EINVAL       # ctas in [1, 65535]

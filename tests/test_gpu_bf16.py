@@ -10,7 +10,8 @@ import workloads as W
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-from gpu_util import GuardedOut, sample_rows  # noqa: E402
+import full_refs  # noqa: E402
+from gpu_util import GuardedOut  # noqa: E402
 
 
 @pytest.fixture(scope="module")
@@ -68,20 +69,33 @@ def test_full_prompts(cp):
         check(got, oracle.prefill_bf16kv(inp.q, kv.k, kv.v, 0), f"T={T}")
 
 
-def test_serving_chunk_sampled(cp):
-    inp = W.serve()
+def test_serving_chunk_full(cp):
+    """Every element of the serving chunk against the oracle on the stored values."""
+    inp, kv, ref = full_refs.serve_bf16()
+    got, guards, _ = run_bf16(cp, inp, kv)
+    assert guards
+    check(got, ref, "serve")
+
+
+def test_long_prefix_full(cp):
+    """Every element of the long prefix (C = 2048, P = 30720) against the oracle."""
+    inp, kv, ref = full_refs.long_prefix_bf16()
+    got, guards, _ = run_bf16(cp, inp, kv)
+    assert guards
+    check(got, ref, "long prefix")
+
+
+@pytest.mark.parametrize("term", ["q", "pv1"])
+def test_split_term_cases(cp, term):
+    """Inputs on which a lost second bf16 term of q or of the probabilities
+    misses the tolerance on most outputs (shown on the CPU by
+    test_split_terms_bf16.py); K and V are used as stored, so they have none."""
+    inp = W.split_term_case(term)
     got, guards, kv = run_bf16(cp, inp)
-    assert guards and np.isfinite(got).all()
-    rows = sample_rows(inp.C, n_random=24, seed=5)
-    check(got[rows], oracle.prefill_bf16kv(inp.q, kv.k, kv.v, inp.P, rows=rows), "serve sampled")
-
-
-def test_long_prefix_sampled(cp):
-    inp = W.long_prefix()
-    got, _, kv = run_bf16(cp, inp)
-    assert np.isfinite(got).all()
-    rows = sample_rows(inp.C, n_random=6, seed=6)
-    check(got[rows], oracle.prefill_bf16kv(inp.q, kv.k, kv.v, inp.P, rows=rows), "long prefix sampled")
+    assert guards
+    rep = oracle.check(got, oracle.prefill_bf16kv(inp.q, kv.k, kv.v, inp.P))
+    assert rep["n_bad"] == 0, f"{inp.name}: {rep}"
+    print(f"attn_prefill_bf16kv {inp.name}: worst err/tol {rep['worst_ratio']:.3g}")
 
 
 def test_agrees_with_the_fp32_kernel_on_the_same_values(cp):

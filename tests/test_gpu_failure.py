@@ -75,3 +75,28 @@ def test_decode_expired_wait_is_reported_and_context_survives(cp, splits):
 def test_decode_selftest_rejects_empty_batch(cp):
     f = cp.raw("attn_selftest_decode_timeout")
     assert f(None, None, None, None, None, None, 0, 1, 1, 16, 0, None, 0, None) == cp.ATTN_EINVAL
+
+
+def test_decode_expired_wait_leaves_no_stale_partial(cp):
+    """A block whose wait expires writes its segment record empty (m = -inf,
+    l = 0): a workspace still holding a finished call's finite records must
+    not leak them into the merge. Every block of the self-test fails, so every
+    record is empty and the merged output is exactly zero."""
+    assert cp.attn_get_device_error() == 0
+    batch = W.decode_batch([300, 1000], seed=22)
+    q = torch.from_numpy(batch.q).cuda()
+    kp = torch.from_numpy(batch.k_pages).cuda()
+    vp = torch.from_numpy(batch.v_pages).cuda()
+    tb = torch.from_numpy(batch.table).cuda()
+    cl = torch.from_numpy(batch.ctx).cuda()
+    out = torch.empty_like(q)
+    splits = 3
+    nbytes = cp.attn_decode_workspace_bytes(2, batch.max_context, splits)
+    ws = torch.empty(max(nbytes, 16) // 4, dtype=torch.float32, device="cuda")
+    cp.attn_decode_paged(q, kp, vp, tb, cl, out, batch.max_context, splits, ws)  # finite records
+    assert cp.attn_get_device_error() == 0
+    assert torch.isfinite(out).all() and out.abs().max().item() > 0
+    out.fill_(float("nan"))
+    cp.attn_selftest_decode_timeout(q, kp, vp, tb, cl, out, batch.max_context, splits, ws)
+    assert cp.attn_get_device_error() == cp.ATTN_ETIMEOUT
+    assert torch.equal(out, torch.zeros_like(out))

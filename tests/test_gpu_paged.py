@@ -10,7 +10,8 @@ import workloads as W
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-from gpu_util import GuardedOut, sample_rows  # noqa: E402
+import full_refs  # noqa: E402
+from gpu_util import GuardedOut  # noqa: E402
 
 
 @pytest.fixture(scope="module")
@@ -57,13 +58,23 @@ def test_paged_planted_and_lastkey(cp):
         check(got, oracle.prefill(inp), inp.name)
 
 
-def test_paged_serving_chunk_sampled(cp):
-    inp = W.serve()
+def test_paged_serving_chunk_full(cp):
+    """Every element of the serving chunk on a shuffled, NaN-padded pool."""
+    inp, ref = full_refs.serve()
     pg = W.to_pages(inp, seed=5, spare_pages=37)
     got, guards = run_paged(cp, inp, pg)
-    assert guards and np.isfinite(got).all()
-    rows = sample_rows(inp.C, n_random=24, seed=2)
-    check(got[rows], oracle.prefill(inp, rows=rows), "paged serve")
+    assert guards
+    check(got, ref, "paged serve")
+
+
+def test_paged_long_prefix_full(cp):
+    """Every element of the long prefix (C = 2048, P = 30720) on a shuffled,
+    NaN-padded pool of 2,176 pages."""
+    inp, ref = full_refs.long_prefix()
+    pg = W.to_pages(inp, seed=6, spare_pages=11)
+    got, guards = run_paged(cp, inp, pg)
+    assert guards
+    check(got, ref, "paged long prefix")
 
 
 def test_shared_prefix_pages(cp):

@@ -112,3 +112,16 @@ def test_partials_beyond_the_scratch_are_rejected(cp):
     got = no_alloc(cp, d, 1024, 0)
     want, _ = with_workspace(cp, d, 1024, 0)
     check(got, want, "automatic splits, B=64")
+
+
+def test_automatic_split_count_fits_the_scratch(cp):
+    """With numSplits = 0 the partials of any batch fit the fixed scratch on
+    this device, so an automatic call never returns ATTN_ESCRATCH: a sweep of B
+    and maxContext through attn_decode_workspace_bytes (no launch)."""
+    worst = (0, 0, 0)
+    for ctx in (256, 512, 1000, 2048, 4096, 16384, 1 << 20, 1 << 24):
+        for B in list(range(1, 2049)) + list(range(2049, 65536, 211)):
+            nbytes = cp.attn_decode_workspace_bytes(B, ctx, 0)
+            if nbytes > worst[0]:
+                worst = (nbytes, B, ctx)
+    assert 0 < worst[0] <= cp.DECODE_SCRATCH_BYTES, worst

@@ -197,6 +197,11 @@ def long_prefix(seed: int = 1, C: int = 2048, P: int = 30720) -> Inputs:
 
 
 SPLIT_TERM_CASES = ("q", "k", "pv")
+# The cases for the bf16-piece paths (x = x1 + x2, two bf16 terms, 16
+# significant bits together): "q" and "k" as above, and "pv1", the "pv" case
+# with value rows of about +1 and -1 instead of +8 and -8 (at |v| = 8 a 16-bit
+# split is itself at the tolerance's absolute floor).
+BF16_SPLIT_TERM_CASES = ("q", "k", "pv1")
 
 
 def split_term_case(term: str, seed: int = 11) -> Inputs:
@@ -214,6 +219,7 @@ def split_term_case(term: str, seed: int = 11) -> Inputs:
     is key 1 plus u/64) whose value rows are 8 (1 + u/16) and -8 (1 + u'/16):
     the output nearly cancels, so the lo parts of the probabilities and of V
     each show at the scale of |v| = 8.
+    "pv1": the same with value rows 1 + u/16 and -(1 + u'/16).
     """
     if term == "q":
         inp = make_inputs(64, 64, seed)
@@ -226,14 +232,15 @@ def split_term_case(term: str, seed: int = 11) -> Inputs:
         q = np.where(inp.q >= 0, 32.0, -32.0).astype(np.float32)
         k = (1.0 + inp.k.astype(np.float64) / 16.0).astype(np.float32)
         return Inputs(q=q, k=k, v=inp.v, C=64, P=64, name="split-term k")
-    if term == "pv":
+    if term in ("pv", "pv1"):
+        scale = 8.0 if term == "pv" else 1.0
         inp = make_inputs(1, 1, seed)
         k = inp.k.copy()
         k[0] = (k[1].astype(np.float64) + uniform(seed + 7, HKV * D).reshape(HKV, D) / 64.0).astype(np.float32)
         v = np.empty_like(inp.v)
-        v[0] = (8.0 * (1.0 + inp.v[0].astype(np.float64) / 16.0)).astype(np.float32)
-        v[1] = (-8.0 * (1.0 + inp.v[1].astype(np.float64) / 16.0)).astype(np.float32)
-        return Inputs(q=inp.q, k=k, v=v, C=1, P=1, name="split-term pv")
+        v[0] = (scale * (1.0 + inp.v[0].astype(np.float64) / 16.0)).astype(np.float32)
+        v[1] = (-scale * (1.0 + inp.v[1].astype(np.float64) / 16.0)).astype(np.float32)
+        return Inputs(q=inp.q, k=k, v=v, C=1, P=1, name=f"split-term {term}")
     raise ValueError(term)
 
 
