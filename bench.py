@@ -202,7 +202,7 @@ def load_peaks():
 TENSOR_PEAK_SHAPES = (("tf32", 128), ("tf32", 256), ("bf16", 256))
 
 
-def measure_tensor_peaks(cp, torch, stream, sms: int, target_ms: float = 20.0, reps: int = 10):
+def measure_tensor_peaks(cp, torch, stream, sms: int, target_ms: float = 20.0, reps: int = 10, windows=None):
     """The tensor pipe's dense rate on this GPU, measured live: every SM issues
     M = 128, N = n tcgen05.mma instructions back to back (attn_tensor_peak),
     each launch about `target_ms` long, 3 warm-up launches, then `reps` timed
@@ -223,11 +223,15 @@ def measure_tensor_peaks(cp, torch, stream, sms: int, target_ms: float = 20.0, r
         for _ in range(3):
             flops = cp.attn_tensor_peak(bf16, n, iters, sms, stream)
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        torch.cuda.synchronize()
+        w0 = time.time()
         for a, b in ev:
             a.record(stream)
             cp.attn_tensor_peak(bf16, n, iters, sms, stream)
             b.record(stream)
         torch.cuda.synchronize()
+        if windows is not None:
+            windows[f"{kind}_n{n}"] = (w0, time.time())
         ms = sorted(a.elapsed_time(b) for a, b in ev)
         med = statistics.median(ms)
         out[f"{kind}_n{n}"] = {"tflops": round(flops / (med * 1e-3) / 1e12, 2),
@@ -784,17 +788,18 @@ def main():
     if rank == 0 and not args.no_peak and kernel.startswith("tcgen05"):
         psampler = ClockSampler(dev.index if world == 1 else local)
         psampler.start()
-        p0 = time.time()
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
-        tensor_peaks = measure_tensor_peaks(cp, torch, stream, sms)
-        p1 = time.time()
+        windows = {}
+        tensor_peaks = measure_tensor_peaks(cp, torch, stream, sms, windows=windows)
         psampler.stop()
-        pclk = psampler.summary(p0, p1)
-        tensor_peaks["clocks"] = pclk
-        if pclk.get("sm_mhz"):
-            for key, val in tensor_peaks.items():
-                if key != "clocks":
-                    val["flop_per_clk_per_sm"] = round(val["tflops"] * 1e12 / (sms * pclk["sm_mhz"] * 1e6), 1)
+        # each shape's own clocks (a dense loop can run power-capped), and its
+        # rate per clock per SM at the median clock of its timed launches
+        for key, (w0, w1) in windows.items():
+            clk = psampler.summary(w0, w1)
+            tensor_peaks[key]["clocks"] = clk
+            if clk.get("sm_mhz"):
+                tensor_peaks[key]["flop_per_clk_per_sm"] = round(
+                    tensor_peaks[key]["tflops"] * 1e12 / (sms * clk["sm_mhz"] * 1e6), 1)
 
     if rank == 0:
         peaks = load_peaks()

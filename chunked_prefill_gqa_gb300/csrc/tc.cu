@@ -143,7 +143,7 @@ struct Bars {
   uint64_t* qready;  // Q hi/lo in shared memory (softmax warps)
   uint64_t* drain;   // [2] drain of each MMA issuer on abort (QK, PV)
   uint64_t* partner;   // tail kernel, rank 0: rank 1's share of the unit is in place (128 remote arrivals)
-  uint64_t* slotfree;  // tail kernel, rank 1: rank 0 has taken it (128 remote arrivals)
+  uint64_t* slotfree;  // tail kernel, rank 1: rank 0's Q region is free for that share (128 remote arrivals)
 };
 
 __device__ __forceinline__ Bars carve_bars(uint8_t* base) {
@@ -241,14 +241,24 @@ __device__ __forceinline__ float ex2(float x) {
 // Epilogue of a unit split over the CTA pair, for one softmax thread (row).
 // Each CTA holds O (the two stacked halves of O' added), m and l of its own
 // key tiles relative to its own reference maximum (none when it got no tile).
-// Rank 1 writes its normalised share to the output row and sends m and l to
-// rank 0's slot; rank 0 merges, m = max(m0, m1) with weights e^(m_s - m)
-// (in log2 units, (m_s - m) c), one division per element. `mu` counts the
-// CTA's earlier split units (the slot's phase). Kept out of line: it runs
-// once per CTA at most and stays out of the hot loop's code.
-__device__ __noinline__ bool split_epilogue(uint32_t lane_tmem, int n, bool has, const Bars& bars, const Params& prm,
-                                            volatile int* abort_flag, float* slot, uint32_t rank, int row,
-                                            float m_ref, float l, float c, bool store, float* dst, uint32_t mu) {
+// The output is only written, never read back: rank 0, once its last PV has
+// completed (so its Q region is idle), tells rank 1 so; rank 1 writes its
+// unnormalised O row into rank 0's Q region and its m and l into rank 0's
+// slot through distributed shared memory, then arrives on rank 0's partner
+// barrier (release at cluster scope); rank 0 merges with the split-K rule, m =
+// max(m0, m1), weights e^(m_s - m) (in log2 units, (m_s - m) c), one division
+// per element, and stores the row. A row is 256 bytes in the Q region, its
+// 16-byte chunk i at chunk i ^ (row mod 16), so the 32 rows of a warp spread
+// over the banks. Kept out of line: it runs once per CTA at most and stays out
+// of the hot loop's code.
+__device__ __forceinline__ uint32_t share_offset(int row, int i) {
+  return (uint32_t)row * 256u + (uint32_t)((i ^ (row & 15)) * 16);
+}
+
+__device__ __noinline__ bool split_epilogue(uint8_t* smem, uint32_t lane_tmem, int n, bool has, const Bars& bars,
+                                            const Params& prm, volatile int* abort_flag, float* slot,
+                                            uint32_t rank, int row, float m_ref, float l, float c, bool store,
+                                            float* dst) {
   float o[64];
   if (has) {
     const int pb = (n - 1) % kNumS;
@@ -268,34 +278,34 @@ __device__ __noinline__ bool split_epilogue(uint32_t lane_tmem, int n, bool has,
     for (int i = 0; i < 64; ++i) o[i] = 0.f;
   }
   const uint32_t peer = rank ^ 1u;
+  uint8_t* share = smem + kSmemQ;
   if (rank == 1) {
-    if (mu > 0 && !wait_bar_cluster_warp(bars.slotfree, (mu - 1) & 1, prm, abort_flag)) return false;
-    if (store) {
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+    if (!wait_bar_cluster_warp(bars.slotfree, 0, prm, abort_flag)) return false;
+    const uint32_t remote = mapa_shared(smem_u32(share), peer);
 #pragma unroll
-      for (int i = 0; i < 64; i += 4)
-        *reinterpret_cast<float4*>(dst + i) = make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
-    }
+    for (int i = 0; i < 16; ++i)
+      st_shared_cluster_v4(remote + share_offset(row, i), o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
     st_shared_cluster_f32(mapa_shared(smem_u32(slot + row), peer), m_ref);
     st_shared_cluster_f32(mapa_shared(smem_u32(slot + kM + row), peer), l);
     mbar_arrive_remote(mapa_shared(smem_u32(bars.partner), peer));
   } else {
-    if (!wait_bar_cluster_warp(bars.partner, mu & 1, prm, abort_flag)) return false;
+    // Every PV of this CTA is complete: its Q region may be overwritten.
+    mbar_arrive_remote(mapa_shared(smem_u32(bars.slotfree), peer));
+    if (!wait_bar_cluster_warp(bars.partner, 0, prm, abort_flag)) return false;
     const float m1 = slot[row], l1 = slot[kM + row];
     const float m = fmaxf(l > 0.f ? m_ref : -INFINITY, l1 > 0.f ? m1 : -INFINITY);
     const float e0 = l > 0.f ? ex2((m_ref - m) * c) : 0.f;
-    const float w1 = l1 > 0.f ? ex2((m1 - m) * c) * l1 : 0.f;
-    const float inv = 1.f / fmaf(e0, l, w1);  // > 0: the unit sees at least key 0
+    const float e1 = l1 > 0.f ? ex2((m1 - m) * c) : 0.f;
+    const float inv = 1.f / fmaf(e0, l, e1 * l1);  // > 0: the unit sees at least key 0
     if (store) {
 #pragma unroll
-      for (int i = 0; i < 64; i += 4) {
-        const float4 x1 = __ldcg(reinterpret_cast<const float4*>(dst + i));
-        *reinterpret_cast<float4*>(dst + i) =
-            make_float4(fmaf(e0, o[i], w1 * x1.x) * inv, fmaf(e0, o[i + 1], w1 * x1.y) * inv,
-                        fmaf(e0, o[i + 2], w1 * x1.z) * inv, fmaf(e0, o[i + 3], w1 * x1.w) * inv);
+      for (int i = 0; i < 16; ++i) {
+        const float4 x1 = *reinterpret_cast<const float4*>(share + share_offset(row, i));
+        *reinterpret_cast<float4*>(dst + 4 * i) =
+            make_float4(fmaf(e0, o[4 * i], e1 * x1.x) * inv, fmaf(e0, o[4 * i + 1], e1 * x1.y) * inv,
+                        fmaf(e0, o[4 * i + 2], e1 * x1.z) * inv, fmaf(e0, o[4 * i + 3], e1 * x1.w) * inv);
       }
     }
-    mbar_arrive_remote(mapa_shared(smem_u32(bars.slotfree), peer));
   }
   return true;
 }
@@ -764,8 +774,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
       }
       if constexpr (kMode == kTail) {
         float* dst = p.out + ((size_t)pos * kHQ + w.g * kGroup + (row & 3)) * kD;
-        if (!split_epilogue(lane_tmem, n, has, bars, prm, abort_flag, reinterpret_cast<float*>(smem + kSmemSlot),
-                            rank, row, m_ref, l, c, pos < p.C, dst, 0))
+        if (!split_epilogue(smem, lane_tmem, n, has, bars, prm, abort_flag, reinterpret_cast<float*>(smem + kSmemSlot),
+                            rank, row, m_ref, l, c, pos < p.C, dst))
           goto softmax_done;
         tc_fence_before();
         continue;

@@ -130,7 +130,7 @@ struct Bars {
   uint64_t* drain;   // [2] MMA issuers' drain on abort
   uint64_t* pair;    // [4] row-set exchanges of the softmax warps
   uint64_t* partner;   // tail kernel, rank 0: rank 1's share of the unit is in place (256 remote arrivals)
-  uint64_t* slotfree;  // tail kernel, rank 1: rank 0 has taken it (256 remote arrivals)
+  uint64_t* slotfree;  // tail kernel, rank 1: rank 0's K ring is free for that share (256 remote arrivals)
 };
 
 template <bool kF32>
@@ -641,10 +641,15 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
       if constexpr (kTail) {
         // A unit split over the CTA pair; this thread holds 32 of its row's 64
         // output dims (head dims 32 kh ..), and l and the reference maximum of
-        // this CTA's key tiles (none when it got no tile). Rank 1 writes its
-        // normalised share and sends m and l (one warp of the row set) to rank
-        // 0's slot; rank 0 merges, m = max(m0, m1) with weights e^(m_s - m)
-        // (in log2 units, (m_s - m) c), one division per element.
+        // this CTA's key tiles (none when it got no tile). The output is only
+        // written: rank 0, once its last PV has completed (its K ring is then
+        // idle), tells rank 1 so; rank 1 writes its unnormalised O (row `row`
+        // of a [128][64] fp32 share at the start of rank 0's K ring, 16-byte
+        // chunk i of the row at chunk i ^ (row mod 16)) and, from one warp of
+        // the row set, m and l into rank 0's slot through distributed shared
+        // memory, then arrives on rank 0's partner barrier (release at cluster
+        // scope); rank 0 merges, m = max(m0, m1) with weights e^(m_s - m) (in
+        // log2 units, (m_s - m) c), one division per element, and stores.
         float o[32];
         if (has) {
           const int pb = (n - 1) % kNumS;
@@ -657,35 +662,38 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
           for (int i = 0; i < 32; ++i) o[i] = 0.f;
         }
         float* slot = reinterpret_cast<float*>(smem + L::kSmemSlot);  // [m of rank 1][l of rank 1], per row
-        float* dst = p.out + ((size_t)pos * kHQ + w.g * kGroup + (row & 3)) * kD + kh * 32;
+        uint8_t* share = smem + kSmemK;
+        auto share_offset = [&](int i) -> uint32_t {  // this thread's chunk i (4 floats) of its row
+          return (uint32_t)row * 256u + (uint32_t)(((kh * 8 + i) ^ (row & 15)) * 16);
+        };
         const uint32_t peer = rank ^ 1u;
         if (rank == 1) {
-          if (pos < p.C) {
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+          if (!wait_bar_cluster_warp(bars.slotfree, 0, prm, abort_flag)) goto softmax_done;
+          const uint32_t remote = mapa_shared(smem_u32(share), peer);
 #pragma unroll
-            for (int i = 0; i < 32; i += 4)
-              *reinterpret_cast<float4*>(dst + i) =
-                  make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
-          }
+          for (int i = 0; i < 8; ++i)
+            st_shared_cluster_v4(remote + share_offset(i), o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
           if (kh == 0) {
             st_shared_cluster_f32(mapa_shared(smem_u32(slot + row), peer), m_ref);
             st_shared_cluster_f32(mapa_shared(smem_u32(slot + 128 + row), peer), l);
           }
           mbar_arrive_remote(mapa_shared(smem_u32(bars.partner), peer));
         } else {
+          mbar_arrive_remote(mapa_shared(smem_u32(bars.slotfree), peer));
           if (!wait_bar_cluster_warp(bars.partner, 0, prm, abort_flag)) goto softmax_done;
           const float m1 = slot[row], l1 = slot[128 + row];
           const float m = fmaxf(l > 0.f ? m_ref : -INFINITY, l1 > 0.f ? m1 : -INFINITY);
           const float e0 = l > 0.f ? ex2((m_ref - m) * c) : 0.f;
-          const float w1 = l1 > 0.f ? ex2((m1 - m) * c) * l1 : 0.f;
-          const float inv = 1.f / fmaf(e0, l, w1);  // > 0: the unit sees at least key 0
+          const float e1 = l1 > 0.f ? ex2((m1 - m) * c) : 0.f;
+          const float inv = 1.f / fmaf(e0, l, e1 * l1);  // > 0: the unit sees at least key 0
           if (pos < p.C) {
+            float* dst = p.out + ((size_t)pos * kHQ + w.g * kGroup + (row & 3)) * kD + kh * 32;
 #pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-              const float4 x1 = __ldcg(reinterpret_cast<const float4*>(dst + i));
-              *reinterpret_cast<float4*>(dst + i) =
-                  make_float4(fmaf(e0, o[i], w1 * x1.x) * inv, fmaf(e0, o[i + 1], w1 * x1.y) * inv,
-                              fmaf(e0, o[i + 2], w1 * x1.z) * inv, fmaf(e0, o[i + 3], w1 * x1.w) * inv);
+            for (int i = 0; i < 8; ++i) {
+              const float4 x1 = *reinterpret_cast<const float4*>(share + share_offset(i));
+              *reinterpret_cast<float4*>(dst + 4 * i) =
+                  make_float4(fmaf(e0, o[4 * i], e1 * x1.x) * inv, fmaf(e0, o[4 * i + 1], e1 * x1.y) * inv,
+                              fmaf(e0, o[4 * i + 2], e1 * x1.z) * inv, fmaf(e0, o[4 * i + 3], e1 * x1.w) * inv);
             }
           }
         }
