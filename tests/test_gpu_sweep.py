@@ -90,3 +90,42 @@ def test_sweep_decode_mixes(cp, seed):
         torch.cuda.synchronize()
         check(out.cpu().numpy(), ref, f"decode seed={seed} splits={splits}")
     assert cp.attn_get_device_error() == 0
+
+
+def _large_shapes(n=5, seed=77):
+    """Chunks of 19 k + m query tiles of 32 rows (m in 1..9, the last tile
+    ragged) against 1000..6000 cached keys: on 152 SMs their last round holds
+    8 m <= 72 units of at least 1024 keys, so a pair grid splits them."""
+    r = W.splitmix64(seed, 4 * n)
+    out = []
+    for i in range(n):
+        tiles = 19 * (1 + int(r[4 * i] % np.uint64(4))) + 1 + int(r[4 * i + 1] % np.uint64(9))
+        C = 32 * tiles - int(r[4 * i + 2] % np.uint64(32))
+        P = 1000 + int(r[4 * i + 3] % np.uint64(5000))
+        out.append((C, P))
+    return out
+
+
+@pytest.mark.parametrize("C,P", _large_shapes())
+def test_sweep_large_chunks(cp, C, P):
+    """Chunks of several rounds of units, where the whole-unit grid and the
+    split-unit pair grid share the work (the pair grid merging its two halves
+    through distributed shared memory): every output of the three kernels that
+    have a pair grid against the oracle."""
+    inp = W.edge(C, P, seed=C * 7 + P)
+    ref = oracle.prefill(inp)
+    q, k, v = device_inputs(inp)
+    for path in ("attn_prefill", "attn_prefill_bf16x3"):
+        g = GuardedOut(C)
+        getattr(cp, path)(q, k, v, g.out, P)
+        torch.cuda.synchronize()
+        assert g.guards_intact(), path
+        check(g.numpy(), ref, f"{path} C={C} P={P}")
+    kv = W.to_bf16(inp)
+    g = GuardedOut(C)
+    cp.attn_prefill_bf16kv(q, torch.from_numpy(kv.k.view(np.int16)).cuda().view(torch.bfloat16),
+                           torch.from_numpy(kv.v.view(np.int16)).cuda().view(torch.bfloat16), g.out, P)
+    torch.cuda.synchronize()
+    assert g.guards_intact()
+    check(g.numpy(), oracle.prefill_bf16kv(inp.q, kv.k, kv.v, P), f"bf16kv C={C} P={P}")
+    assert cp.attn_get_device_error() == 0
