@@ -13,14 +13,19 @@
 //       O += p1 V   + p2 V                   (8 + 8 MMAs of 128 x 64 x 16)
 //   fp32 cache: converter warps split each landed K/V tile in place into
 //   [x1 | x2], and each product keeps three of its four terms,
-//       S  = q1 k1^T + q1 k2^T + q2 k1^T     (3 x 4 MMAs)
-//       O += p1 v1   + p1 v2   + p2 v1       (3 x 8 MMAs)
+//       S  = q1 k1^T + q1 k2^T + q2 k1^T     (3 x 4 MMAs of 128 x 128 x 16)
+//       O' = p1 [v1 | v2] + p2 v1            (8 MMAs of 128 x 128 x 16 on the
+//                                             stacked [v1 | v2] operand, then 8
+//                                             of 128 x 64 x 16 into O'[:, :64])
+//       O  = O'[:, :64] + O'[:, 64:]          (added in the epilogue)
 //   dropping only x2 y2, below 2^-15 of |x y| (hi rounded to nearest: |x2| <=
 //   2^-8 |x|; p1 truncated: |p2| < 2^-7 p); the kept terms carry the residual
 //   of each split, at most 2^-9 |x2|.
 // K is a K-major operand and V an MN-major one ([key][d] rows, 128-byte
-// swizzle), so V needs no transpose. q, P and the accumulators live in TMEM; P
+// swizzle), so V needs no transpose. P and the accumulators live in TMEM; P
 // (p1 | p2) overwrites the S columns it came from, two bf16 per 32-bit column.
+// q1 | q2 is a TMEM operand with the bf16 cache and a shared-memory one with the
+// fp32 cache, whose TMEM holds the 128-column O' instead.
 //
 // Work unit (as in tc.cu): 32 chunk positions x the 4 query heads of one KV
 // head = 128 rows, one TMEM lane each. Keys come in tiles of 128; tiles past
@@ -29,9 +34,10 @@
 // Warp roles:
 //   0-7   softmax: warp w owns TMEM lanes 32 (w % 4) .. + 31 and keys
 //         64 (w / 4) .. + 63 of every tile; the two warps of a row set exchange
-//         partial maxima and sums through shared memory. They split q into
-//         TMEM, run the online softmax, write p1/p2, rescale O when the
-//         reference maximum moves, and write the output.
+//         partial maxima and sums through shared memory. They split q (into
+//         TMEM, or shared memory with the fp32 cache), run the online softmax,
+//         write p1/p2, rescale O when the reference maximum moves, and write the
+//         output.
 //   8     K producer, 9 V producer: TMA loads of whole tiles.
 //   10    QK issuer (allocates TMEM): QK(n) once K(n) is ready and S buffer
 //         n % 3 is free (PV(n-3) complete).
@@ -57,8 +63,6 @@ using namespace tc;
 constexpr int kBq = 32;           // chunk positions per unit
 constexpr int kM = kBq * kGroup;  // 128 rows = TMEM lanes
 constexpr int kBc = 128;          // keys per tile
-template <bool kF32>
-constexpr int stages_of() { return kF32 ? 3 : 4; }  // K and V rings (the fp32 stage is twice the size)
 constexpr int kNumS = 3;          // S / P buffers in TMEM
 
 constexpr int kSoftmaxWarps = 8;
@@ -73,26 +77,34 @@ constexpr int threads_of() {
   return 32 * (kF32 ? kFirstConvWarp + 2 * kConvWarpsPerOperand : kPvWarp + 1);
 }
 
-// TMEM columns (32-bit each).
+// TMEM columns (32-bit each). bf16 cache: q1 [0,32), q2 [32,64), three S
+// buffers [64,448), O [448,512). fp32 cache (q in shared memory): three S
+// buffers [0,384), O' = [p1 v1 + p2 v1 | p1 v2] [384,512).
 constexpr uint32_t kColQhi = 0;   // 64 bf16 per row = 32 columns
 constexpr uint32_t kColQlo = 32;
-constexpr uint32_t kColS = 64;    // three 128-column S buffers; p1 | p2 (64 columns each) overwrite them
-constexpr uint32_t kColO = 448;   // 64 fp32 columns
+template <bool kF32>
+__host__ __device__ constexpr uint32_t col_s() { return kF32 ? 0u : 64u; }  // 128-column S buffers; p1 | p2 overwrite them
+template <bool kF32>
+__host__ __device__ constexpr uint32_t col_o() { return kF32 ? 384u : 448u; }
 constexpr uint32_t kTmemCols = 512;
 
 // Shared memory (byte offsets from a 1024-aligned base). A bf16 operand tile
 // is 128 keys x 64 values = 128 rows of 128 bytes in the 128-byte swizzle
 // (16 KB). With an fp32 cache a stage is 32 KB: TMA lands d 0-31 and d 32-63
-// as two such 16 KB regions, and the converters overwrite them with x1 and x2.
+// as two such 16 KB regions, and the converters overwrite them with x1 and x2;
+// q1 and q2 come first (two 16 KB K-major operands), then three K stages and two
+// V stages. The bf16 cache has four stages of each.
 constexpr uint32_t kOperandBytes = kBc * kD * 2;  // 16 KB
 template <bool kF32>
 struct Layout {
-  static constexpr int kStages = stages_of<kF32>();
+  static constexpr int kKS = kF32 ? 3 : 4;  // K ring stages
+  static constexpr int kVS = kF32 ? 2 : 4;  // V ring stages (an fp32 V stage is converted while up to two wait)
   static constexpr uint32_t kStageBytes = kF32 ? 2 * kOperandBytes : kOperandBytes;
-  static constexpr uint32_t kSmemK = 0;
-  static constexpr uint32_t kSmemV = kSmemK + kStages * kStageBytes;
-  static constexpr uint32_t kSmemBar = kSmemV + kStages * kStageBytes;
-  static constexpr uint32_t kNumBars = 9 * kStages + 1 + 2 + 4 + 2;
+  static constexpr uint32_t kSmemQ = 0;  // fp32 cache: q1 | q2, K-major bf16 operands of 16 KB each
+  static constexpr uint32_t kSmemK = kSmemQ + (kF32 ? 2 * kOperandBytes : 0);
+  static constexpr uint32_t kSmemV = kSmemK + kKS * kStageBytes;
+  static constexpr uint32_t kSmemBar = kSmemV + kVS * kStageBytes;
+  static constexpr uint32_t kNumBars = 3 * kKS + 3 * kVS + 9 + 1 + 2 + 4 + 2;
   static constexpr uint32_t kSmemRed = kSmemBar + kNumBars * 8 + 16;  // [2 tile parities][2 key halves][128 rows]
   static constexpr uint32_t kSmemLsum = kSmemRed + 2 * 2 * 128 * 4;   // [2 key halves][128 rows]
   static constexpr uint32_t kSmemSlot = kSmemLsum + 2 * 128 * 4;    // tail kernel: rank 1's m and l per row
@@ -102,10 +114,12 @@ struct Layout {
 };
 
 static_assert(kM == 128 && kD == 64 && kBc == 128, "the MMA shapes below assume 128 x 128 x 64");
-static_assert(kColS + kNumS * 128 <= kColO && kColO + kD <= kTmemCols, "TMEM layout");
+static_assert(col_s<false>() + 3 * 128 <= col_o<false>() && col_o<false>() + kD <= kTmemCols, "TMEM layout");
+static_assert(col_s<true>() + 3 * 128 <= col_o<true>() && col_o<true>() + 2 * kD <= kTmemCols, "TMEM layout");
 
 constexpr uint32_t kIdescQK = idesc_bf16(128, 128, false);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 64, true);
+constexpr uint32_t kIdescPV128 = idesc_bf16(128, 128, true);
 constexpr float kStaleLog2 = 8.0f;  // see tc.cu: a stale reference maximum keeps p <= 2^8
 
 struct Params {
@@ -117,12 +131,12 @@ struct Params {
 };
 
 struct Bars {
-  uint64_t* kfull;   // [kStages] TMA K landed
-  uint64_t* kconv;   // [kStages] K split into k1 | k2 (fp32 cache)
-  uint64_t* vconv;   // [kStages] V split into v1 | v2 (fp32 cache)
-  uint64_t* kempty;  // [kStages] QK done with the stage
-  uint64_t* vfull;   // [kStages] TMA V landed
-  uint64_t* vempty;  // [kStages] PV done with the stage
+  uint64_t* kfull;   // [K stages] TMA K landed
+  uint64_t* kconv;   // [K stages] K split into k1 | k2 (fp32 cache)
+  uint64_t* vconv;   // [V stages] V split into v1 | v2 (fp32 cache)
+  uint64_t* kempty;  // [K stages] QK done with the stage
+  uint64_t* vfull;   // [V stages] TMA V landed
+  uint64_t* vempty;  // [V stages] PV done with the stage
   uint64_t* sfull;   // [kNumS] S written (MMA commit)
   uint64_t* pfull;   // [kNumS] P written and O rescaled (softmax warps)
   uint64_t* odone;   // [kNumS] PV(n) complete, barrier n % 3
@@ -136,14 +150,14 @@ struct Bars {
 template <bool kF32>
 __device__ __forceinline__ Bars carve_bars(uint8_t* base) {
   uint64_t* b = reinterpret_cast<uint64_t*>(base + Layout<kF32>::kSmemBar);
-  constexpr int kStages = Layout<kF32>::kStages;
+  constexpr int kKS = Layout<kF32>::kKS, kVS = Layout<kF32>::kVS;
   Bars r;
-  r.kfull = b; b += kStages;
-  r.kconv = b; b += kStages;
-  r.vconv = b; b += kStages;
-  r.kempty = b; b += kStages;
-  r.vfull = b; b += kStages;
-  r.vempty = b; b += kStages;
+  r.kfull = b; b += kKS;
+  r.kconv = b; b += kKS;
+  r.vconv = b; b += kVS;
+  r.kempty = b; b += kKS;
+  r.vfull = b; b += kVS;
+  r.vempty = b; b += kVS;
   r.sfull = b; b += kNumS;
   r.pfull = b; b += kNumS;
   r.odone = b; b += kNumS;
@@ -272,9 +286,11 @@ __global__ void __launch_bounds__(threads_of<kF32>(), 1)
 tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                const Params prm) {
   using L = Layout<kF32>;
+  constexpr uint32_t kColO = col_o<kF32>();
   constexpr uint32_t kSmemK = L::kSmemK, kSmemV = L::kSmemV, kSmemBar = L::kSmemBar, kNumBars = L::kNumBars;
   constexpr uint32_t kSmemRed = L::kSmemRed, kSmemLsum = L::kSmemLsum, kStageBytes = L::kStageBytes;
-  constexpr int kStages = L::kStages;
+  constexpr int kKS = L::kKS, kVS = L::kVS;
+  constexpr uint32_t kColS = col_s<kF32>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const Bars bars = carve_bars<kF32>(smem);
@@ -285,11 +301,13 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kKS; ++s) {
       mbar_init(&bars.kfull[s], 1);
       mbar_init(&bars.kconv[s], kConvWarpsPerOperand);
-      mbar_init(&bars.vconv[s], kConvWarpsPerOperand);
       mbar_init(&bars.kempty[s], 1);
+    }
+    for (int s = 0; s < kVS; ++s) {
+      mbar_init(&bars.vconv[s], kConvWarpsPerOperand);
       mbar_init(&bars.vfull[s], 1);
       mbar_init(&bars.vempty[s], 1);
     }
@@ -344,6 +362,7 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
         const Unit w = decode_unit(u, prm);
         int jb, je;
         unit_range<kTail>(w, rank, &jb, &je);
+        const int kStages = is_k ? kKS : kVS;
         for (int j = jb; j < je; ++j, ++n) {
           const int st = n % kStages;
           uint64_t* freed = is_k ? &bars.kempty[st] : &bars.vempty[st];
@@ -386,7 +405,8 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
         }
         for (int j = jb; j < je; ++j, ++n) {
           const int b = n % kNumS;
-          const int st = n % kStages;
+          const int st = n % (is_qk ? kKS : kVS);
+          const int kStages = is_qk ? kKS : kVS;
           if (is_qk) {
             // S buffer b is free once PV(n-3) has read P(n-3) from it; odone[b]
             // cannot be further ahead, since PV(n) needs S(n), issued below.
@@ -396,17 +416,25 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
             tc_fence_after();
             const uint32_t kb = smem_u32(smem + kSmemK + st * kStageBytes);
             const uint32_t d = tmem + kColS + b * 128;
-#pragma unroll
-            for (int s = 0; s < 4; ++s)
-              mma_f16_ts(d, tmem + kColQhi + s * 8, sdesc_sw128(kb + s * 32), kIdescQK, s > 0);
-            if (kF32) {
+            if (kF32) {  // q1 | q2 from shared memory
+              const uint32_t qb = smem_u32(smem + L::kSmemQ);
 #pragma unroll
               for (int s = 0; s < 4; ++s)
-                mma_f16_ts(d, tmem + kColQhi + s * 8, sdesc_sw128(kb + kOperandBytes + s * 32), kIdescQK, 1);
-            }
+                mma_f16_ss(d, sdesc_sw128(qb + s * 32), sdesc_sw128(kb + s * 32), kIdescQK, s > 0);
 #pragma unroll
-            for (int s = 0; s < 4; ++s)
-              mma_f16_ts(d, tmem + kColQlo + s * 8, sdesc_sw128(kb + s * 32), kIdescQK, 1);
+              for (int s = 0; s < 4; ++s)
+                mma_f16_ss(d, sdesc_sw128(qb + s * 32), sdesc_sw128(kb + kOperandBytes + s * 32), kIdescQK, 1);
+#pragma unroll
+              for (int s = 0; s < 4; ++s)
+                mma_f16_ss(d, sdesc_sw128(qb + kOperandBytes + s * 32), sdesc_sw128(kb + s * 32), kIdescQK, 1);
+            } else {
+#pragma unroll
+              for (int s = 0; s < 4; ++s)
+                mma_f16_ts(d, tmem + kColQhi + s * 8, sdesc_sw128(kb + s * 32), kIdescQK, s > 0);
+#pragma unroll
+              for (int s = 0; s < 4; ++s)
+                mma_f16_ts(d, tmem + kColQlo + s * 8, sdesc_sw128(kb + s * 32), kIdescQK, 1);
+            }
             mma_commit(&bars.sfull[b]);
             mma_commit(&bars.kempty[st]);
           } else {
@@ -417,14 +445,16 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
             const uint32_t vb = smem_u32(smem + kSmemV + st * kStageBytes);
             const uint32_t phi = tmem + kColS + b * 128;
             const bool first = j == jb;
-#pragma unroll
-            for (int s = 0; s < 8; ++s)  // 16 keys per step: 2048 bytes of V rows
-              mma_f16_ts(tmem + kColO, phi + s * 8, sdesc_sw128_mn(vb + s * 2048), kIdescPV,
-                         (first && s == 0) ? 0u : 1u);
             if (kF32) {
 #pragma unroll
-              for (int s = 0; s < 8; ++s)
-                mma_f16_ts(tmem + kColO, phi + s * 8, sdesc_sw128_mn(vb + kOperandBytes + s * 2048), kIdescPV, 1);
+              for (int s = 0; s < 8; ++s)  // [p1 v1 | p1 v2]: v2 is the N block kOperandBytes further
+                mma_f16_ts(tmem + kColO, phi + s * 8, sdesc_sw128_mn(vb + s * 2048, kOperandBytes), kIdescPV128,
+                           (first && s == 0) ? 0u : 1u);
+            } else {
+#pragma unroll
+              for (int s = 0; s < 8; ++s)  // 16 keys per step: 2048 bytes of V rows
+                mma_f16_ts(tmem + kColO, phi + s * 8, sdesc_sw128_mn(vb + s * 2048), kIdescPV,
+                           (first && s == 0) ? 0u : 1u);
             }
 #pragma unroll
             for (int s = 0; s < 8; ++s)
@@ -463,6 +493,7 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
         const Unit w = decode_unit(u, prm);
         int jb, je;
         unit_range<kTail>(w, rank, &jb, &je);
+        const int kStages = is_k ? kKS : kVS;
         for (int j = jb; j < je; ++j, ++n) {
           const int st = n % kStages;
           if (!wait_bar_warp(is_k ? &bars.kfull[st] : &bars.vfull[st], (n / kStages) & 1, prm, abort_flag))
@@ -536,10 +567,21 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
       }
       uint32_t hi[16], lo[16];
       split_pack_rn<16>(x, hi, lo);
-      tmem_st16(lane_tmem + kColQhi + kh * 16, hi);
-      tmem_st16(lane_tmem + kColQlo + kh * 16, lo);
-      tmem_wait_st();
-      tc_fence_before();
+      if (kF32) {  // this warp's 32 dims: 16-byte chunks 4 kh .. 4 kh + 3 of the row's 128-byte swizzle row
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t off = sw128((uint32_t)row * 128u + (uint32_t)(kh * 4 + c) * 16u);
+          *reinterpret_cast<uint4*>(smem + L::kSmemQ + off) = make_uint4(hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
+          *reinterpret_cast<uint4*>(smem + L::kSmemQ + kOperandBytes + off) =
+              make_uint4(lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
+        }
+        fence_proxy_async_smem();
+      } else {
+        tmem_st16(lane_tmem + kColQhi + kh * 16, hi);
+        tmem_st16(lane_tmem + kColQlo + kh * 16, lo);
+        tmem_wait_st();
+        tc_fence_before();
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(bars.qready);
     };
@@ -622,6 +664,13 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] *= alpha;
           tmem_st32(lane_tmem + kColO + kh * 32, o);
+          if (kF32) {
+            tmem_ld32(lane_tmem + kColO + 64 + kh * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tmem_st32(lane_tmem + kColO + 64 + kh * 32, o);
+          }
           tmem_wait_st();
         }
         tc_fence_before();
@@ -657,6 +706,13 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
           tc_fence_after();
           tmem_ld32(lane_tmem + kColO + kh * 32, o);
           tmem_wait_ld();
+          if (kF32) {
+            float o2[32];
+            tmem_ld32(lane_tmem + kColO + 64 + kh * 32, o2);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] += o2[i];
+          }
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = 0.f;
@@ -709,6 +765,13 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
         float a[32];
         tmem_ld32(lane_tmem + kColO + kh * 32, a);
         tmem_wait_ld();
+        if (kF32) {
+          float a2[32];
+          tmem_ld32(lane_tmem + kColO + 64 + kh * 32, a2);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) a[i] += a2[i];
+        }
         if (pos < p.C) {
           float* dst = p.out + ((size_t)pos * kHQ + w.g * kGroup + (row & 3)) * kD + kh * 32;
           const float inv = 1.f / l;
