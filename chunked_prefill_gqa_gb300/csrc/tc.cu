@@ -780,13 +780,15 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
         tc_fence_before();
         continue;
       }
-      // Epilogue: wait for the last PV, add the two stacked halves of O', one
-      // division per element.
+      // Epilogue: wait for the last PV, add the two stacked halves of O' and
+      // scale by the row's 1 / l: one reciprocal per row and a multiply per
+      // element, measured faster than 64 IEEE divisions per thread.
       {
         const int pb = (n - 1) % kNumS;
         if (!wait_bar_warp(&bars.odone[pb], ((n - 1) / kNumS) & 1, prm, abort_flag)) goto softmax_done;
       }
       tc_fence_after();
+      const float inv = 1.f / l;
 #pragma unroll
       for (int dh = 0; dh < 2; ++dh) {
         float a[32], b[32];
@@ -798,8 +800,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
 #pragma unroll
           for (int i = 0; i < 32; i += 4)
             *reinterpret_cast<float4*>(dst + i) =
-                make_float4((a[i] + b[i]) / l, (a[i + 1] + b[i + 1]) / l, (a[i + 2] + b[i + 2]) / l,
-                            (a[i + 3] + b[i + 3]) / l);
+                make_float4((a[i] + b[i]) * inv, (a[i + 1] + b[i + 1]) * inv, (a[i + 2] + b[i + 2]) * inv,
+                            (a[i + 3] + b[i + 3]) * inv);
         }
       }
       tc_fence_before();
