@@ -6,7 +6,7 @@
 // rows at positions P..P+C-1 against keys 0..P+C-1, row i seeing j <= P+i,
 // query head h reading KV head h/4, scale 1/8. Per tile with maximum m_tile:
 // m_new = max(m_old, m_tile), alpha = exp(m_old - m_new), l and the
-// accumulator rescaled by alpha, one division by l at the very end.
+// accumulator rescaled by alpha, normalised by 1 / l at the very end.
 //
 // Work unit: 32 chunk positions x the 4 query heads that share KV head g
 // (GQA packing, "FlashAttention and inference kernels", GQA read
@@ -246,16 +246,16 @@ __device__ __forceinline__ float ex2(float x) {
 // unnormalised O row into rank 0's Q region and its m and l into rank 0's
 // slot through distributed shared memory, then arrives on rank 0's partner
 // barrier (release at cluster scope); rank 0 merges with the split-K rule, m =
-// max(m0, m1), weights e^(m_s - m) (in log2 units, (m_s - m) c), one division
-// per element, and stores the row. A row is 256 bytes in the Q region, its
+// max(m0, m1), weights e^(m_s - m) (in log2 units, (m_s - m) c), one
+// reciprocal of the merged denominator per row, and stores the row. A row is 256 bytes in the Q region, its
 // 16-byte chunk i at chunk i ^ (row mod 16), so the 32 rows of a warp spread
-// over the banks. Kept out of line: it runs once per CTA at most and stays out
-// of the hot loop's code.
+// over the banks. Inlined: out of line, the reference to the barrier set put
+// it on the stack, and the pair grid measured slower.
 __device__ __forceinline__ uint32_t share_offset(int row, int i) {
   return (uint32_t)row * 256u + (uint32_t)((i ^ (row & 15)) * 16);
 }
 
-__device__ __noinline__ bool split_epilogue(uint8_t* smem, uint32_t lane_tmem, int n, bool has, const Bars& bars,
+__device__ __forceinline__ bool split_epilogue(uint8_t* smem, uint32_t lane_tmem, int n, bool has, const Bars& bars,
                                             const Params& prm, volatile int* abort_flag, float* slot,
                                             uint32_t rank, int row, float m_ref, float l, float c, bool store,
                                             float* dst) {
@@ -341,7 +341,7 @@ __device__ __forceinline__ int work_unit(int k, int cta, int grid, const Params&
 template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-          const Params prm) {
+          const __grid_constant__ Params prm) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const Bars bars = carve_bars(smem);

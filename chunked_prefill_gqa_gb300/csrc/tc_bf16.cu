@@ -698,7 +698,7 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
         // the row set, m and l into rank 0's slot through distributed shared
         // memory, then arrives on rank 0's partner barrier (release at cluster
         // scope); rank 0 merges, m = max(m0, m1) with weights e^(m_s - m) (in
-        // log2 units, (m_s - m) c), one division per element, and stores.
+        // log2 units, (m_s - m) c), one reciprocal per row, and stores.
         float o[32];
         if (has) {
           const int pb = (n - 1) % kNumS;
