@@ -4,10 +4,10 @@
 // Cached Prefix" (Lesson): a tile of query rows stays resident, each K/V
 // tile is staged in shared memory once and consumed by every resident row,
 // and m, l and the accumulator are carried across tiles with the rescale by
-// exp(m_old - m_new) and one division at the end. GQA packing ("FlashAttention
-// and inference kernels", GQA read amplification): a block owns 16 chunk
-// positions x the 4 query heads of one KV head = 64 rows, so one K/V tile
-// feeds all four heads. Causal skipping: the block loads keys [0, P + last
+// exp(m_old - m_new) and the division by l at the end (one reciprocal per
+// row). GQA packing ("FlashAttention and inference kernels", GQA read
+// amplification): a block owns 16 chunk positions x the 4 query heads of one
+// KV head = 64 rows, so one K/V tile feeds all four heads. Causal skipping: the block loads keys [0, P + last
 // row] only and masks elementwise only on tiles that cross the diagonal
 // (same page, "How FlashAttention evolved", the causal mask).
 //
@@ -41,6 +41,11 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
 
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 __device__ __forceinline__ void st4(float* p, float a, float b, float c, float d) {
   *reinterpret_cast<float4*>(p) = make_float4(a, b, c, d);
@@ -165,11 +170,13 @@ ffma_kernel(Problem p, int n_qtiles) {
       for (int off = 8; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
       const float mnew = fmaxf(m[r], mx);
       const float mref = mnew == -INFINITY ? 0.f : mnew;  // fully masked so far: no NaN
-      const float alpha = exp2f((m[r] - mref) * kLog2e);
+      // e^(s - m) = 2^(s log2(e) - m log2(e)): one FFMA and one ex2.
+      const float alpha = ex2((m[r] - mref) * kLog2e);
+      const float mc = mref * kLog2e;
       float lsum = 0.f;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const float pj = exp2f((s[r][c] - mref) * kLog2e);
+        const float pj = ex2(fmaf(s[r][c], kLog2e, -mc));
         s[r][c] = pj;
         lsum += pj;
       }
@@ -204,7 +211,7 @@ ffma_kernel(Problem p, int n_qtiles) {
     __syncthreads();
   }
 
-  // One division per element at the very end.
+  // Normalise by l at the very end: one reciprocal per row.
 #pragma unroll
   for (int r = 0; r < 8; ++r) {
     float lr = l[r];
@@ -214,7 +221,8 @@ ffma_kernel(Problem p, int n_qtiles) {
     const int pos = t0 + (row >> 2);
     if (pos < p.C) {
       float* dst = p.out + ((size_t)pos * kHQ + g * kGroup + (row & 3)) * kD + kg * 4;
-      st4(dst, o[r][0] / lr, o[r][1] / lr, o[r][2] / lr, o[r][3] / lr);
+      const float inv = 1.f / lr;
+      st4(dst, o[r][0] * inv, o[r][1] * inv, o[r][2] * inv, o[r][3] * inv);
     }
   }
 }
