@@ -88,6 +88,15 @@ __device__ __forceinline__ void st_shared_cluster_v4(uint32_t cluster_addr, floa
                "f"(d)
                : "memory");
 }
+// Copy `bytes` (a multiple of 16, both addresses 16-byte aligned) from this
+// CTA's shared memory to another CTA's of the cluster; the bytes complete as
+// transactions on that CTA's mbarrier `bar_cluster`.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, const void* src, uint32_t bytes,
+                                                     uint32_t bar_cluster) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst_cluster), "r"(smem_u32(src)), "r"(bytes), "r"(bar_cluster)
+               : "memory");
+}
 // Arrive on an mbarrier of another CTA of the cluster, releasing this thread's
 // earlier memory operations at cluster scope.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
