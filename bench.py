@@ -313,6 +313,11 @@ def roofline(path_name: str, kernel: str, flops: float, ms: float, peaks, worklo
              "frac_of_split_roof": None,
              "peak_nominal_ratio": round(nominal, 3),
              "frac_of_nominal_ratio_peak": round(achieved / nominal, 4)}
+        if peaks.get("tf32_n128_tflops"):
+            # The kernel's MMAs are N <= 128 (its tensor memory holds no wider S
+            # buffer); the N = 128 loop is the pipe's rate for that shape. The
+            # tensor work is the three split products per algorithmic flop.
+            r["tensor_work_frac_of_n128_loop"] = round(3 * achieved / peaks["tf32_n128_tflops"], 4)
     else:
         # FP32 FFMA pipe: 152 SMs x 128 lanes x 2 flop per clock at the maximum SM clock.
         peak = NUM_SMS * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
@@ -821,6 +826,7 @@ def main():
         peaks = load_peaks()
         if tensor_peaks is not None:
             peaks["tf32_tflops"] = tf32_peak_from(tensor_peaks)
+            peaks["tf32_n128_tflops"] = tensor_peaks["tf32_n128"]["tflops"]
         line = {
             "metric": METRIC if args.workload == "serve" else METRIC_LONG,
             "value": round(value, 4), "unit": UNIT, "n_gpus": world,
