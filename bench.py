@@ -199,7 +199,7 @@ def load_peaks():
             "sm_max_mhz": 2070.0, "source": "fallback"}
 
 
-TENSOR_PEAK_SHAPES = (("tf32", 128), ("tf32", 256), ("bf16", 256))
+TENSOR_PEAK_SHAPES = (("tf32", 128), ("tf32", 256), ("bf16", 128), ("bf16", 256))
 
 
 def measure_tensor_peaks(cp, torch, stream, sms: int, target_ms: float = 20.0, reps: int = 10, windows=None):
@@ -208,7 +208,8 @@ def measure_tensor_peaks(cp, torch, stream, sms: int, target_ms: float = 20.0, r
     each launch about `target_ms` long, 3 warm-up launches, then `reps` timed
     with CUDA events; the median launch gives the rate. tf32 is the split-TF32
     kernel's instruction kind (no library GEMM reports it); bf16 at N = 256
-    sits beside the driver's cuBLAS bf16 figure as a check of the method."""
+    sits beside the driver's cuBLAS bf16 figure as a check of the method; N =
+    128 is the widest instruction the prefill kernels issue."""
     out = {}
     for kind, n in TENSOR_PEAK_SHAPES:
         bf16 = kind == "bf16"
@@ -299,6 +300,10 @@ def roofline(path_name: str, kernel: str, flops: float, ms: float, peaks, worklo
              "peak_note": f"{peaks['source']} bf16 burst",
              "tensor_passes": 3 if kernel.startswith("tcgen05-bf16x3") else 2,
              "frac_of_split_roof": None}
+        if peaks.get("bf16_n128_tflops"):
+            # As for tf32: the kernel's MMAs are N <= 128; its tensor work
+            # against the pipe's measured rate at N = 128.
+            r["tensor_work_frac_of_n128_loop"] = round(r["tensor_passes"] * achieved / peaks["bf16_n128_tflops"], 4)
     elif kernel.startswith("tcgen05-split-tf32"):
         nominal = peaks["bf16_tflops"] * NOMINAL_TF32 / NOMINAL_BF16
         if peaks.get("tf32_tflops"):
@@ -827,6 +832,7 @@ def main():
         if tensor_peaks is not None:
             peaks["tf32_tflops"] = tf32_peak_from(tensor_peaks)
             peaks["tf32_n128_tflops"] = tensor_peaks["tf32_n128"]["tflops"]
+            peaks["bf16_n128_tflops"] = tensor_peaks["bf16_n128"]["tflops"]
         line = {
             "metric": METRIC if args.workload == "serve" else METRIC_LONG,
             "value": round(value, 4), "unit": UNIT, "n_gpus": world,
