@@ -95,18 +95,20 @@ int naive_prepare(int C, int P, DeviceState** st) {
 
 // ---------------------------------------------------------------------------
 // Host-buffer calls: the chunk is run as up to kMaxSlices consecutive
-// sub-chunks of whole 32-row query tiles, each one full round of units. Sub-chunk s (rows r0 .. r1-1) is the
-// prefill of those rows against positions 0 .. P+r1-1, the same rows of the
-// whole call's result. Its copy-in adds only its query rows and the K/V rows
-// past the previous sub-chunk's end, so copy-in of s+1 and copy-out of s-1
-// overlap the compute of s.
+// sub-chunks of whole 32-row query tiles, each one full round of units.
+// Sub-chunk s (rows r0 .. r1-1) is the prefill of those rows against positions
+// 0 .. P+r1-1, the same rows of the whole call's result. Its copy-in adds only
+// its query rows and the K/V rows past the previous sub-chunk's end, so
+// copy-in of s+1 and copy-out of s-1 overlap the compute of s; sub-chunks
+// compute alternately on the caller's stream and a library stream, so the
+// next one's blocks take SMs as the previous one's leave.
 constexpr int kMaxSlices = 4;
 
 struct HostPipe {
   std::mutex mu;  // held for a whole enqueue: every call re-records the events
   bool made = false;
   int sms = 0;
-  cudaStream_t in = nullptr, out = nullptr;
+  cudaStream_t in = nullptr, out = nullptr, comp2 = nullptr;
   cudaEvent_t start = nullptr, done = nullptr;
   cudaEvent_t loaded[kMaxSlices] = {}, computed[kMaxSlices] = {};
 };
@@ -138,6 +140,7 @@ int make_pipe(HostPipe* hp) {
   if (hp->made) return ATTN_OK;
   if (cudaStreamCreateWithFlags(&hp->in, cudaStreamNonBlocking) != cudaSuccess ||
       cudaStreamCreateWithFlags(&hp->out, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&hp->comp2, cudaStreamNonBlocking) != cudaSuccess ||
       cudaEventCreateWithFlags(&hp->start, cudaEventDisableTiming) != cudaSuccess ||
       cudaEventCreateWithFlags(&hp->done, cudaEventDisableTiming) != cudaSuccess)
     return ATTN_ECUDA;
@@ -166,7 +169,8 @@ int run_from_host(const float* q_h, const void* k_h, const void* v_h, float* out
   rc = make_pipe(hp);
   if (rc != ATTN_OK) return rc;
   if (cudaEventRecord(hp->start, stream) != cudaSuccess || cudaStreamWaitEvent(hp->in, hp->start, 0) != cudaSuccess ||
-      cudaStreamWaitEvent(hp->out, hp->start, 0) != cudaSuccess)
+      cudaStreamWaitEvent(hp->out, hp->start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(hp->comp2, hp->start, 0) != cudaSuccess)
     return ATTN_ECUDA;
   constexpr size_t kQRow = sizeof(float) * ATTN_HQ * ATTN_D;
   auto* kd = static_cast<char*>(k_d);
@@ -184,7 +188,7 @@ int run_from_host(const float* q_h, const void* k_h, const void* v_h, float* out
         cudaMemcpyAsync(kd + kv0, kh + kv0, kv1 - kv0, cudaMemcpyDefault, hp->in) != cudaSuccess ||
         cudaMemcpyAsync(vd + kv0, vh + kv0, kv1 - kv0, cudaMemcpyDefault, hp->in) != cudaSuccess ||
         cudaEventRecord(hp->loaded[s], hp->in) != cudaSuccess ||
-        cudaStreamWaitEvent(stream, hp->loaded[s], 0) != cudaSuccess) {
+        cudaStreamWaitEvent((s & 1) ? hp->comp2 : stream, hp->loaded[s], 0) != cudaSuccess) {
       rc = ATTN_ECUDA;
       break;
     }
@@ -194,15 +198,20 @@ int run_from_host(const float* q_h, const void* k_h, const void* v_h, float* out
     ps.out = out_d + (size_t)r0 * ATTN_HQ * ATTN_D;
     ps.C = r1 - r0;
     ps.P = P + r0;
-    rc = launch(ps, stream);
+    // Consecutive sub-chunks alternate between two streams, so the next one's
+    // blocks take SMs as the previous one's finish.
+    cudaStream_t cs = (s & 1) ? hp->comp2 : stream;
+    rc = launch(ps, cs);
     if (rc != ATTN_OK) break;
-    if (cudaEventRecord(hp->computed[s], stream) != cudaSuccess ||
+    if (cudaEventRecord(hp->computed[s], cs) != cudaSuccess ||
         cudaStreamWaitEvent(hp->out, hp->computed[s], 0) != cudaSuccess ||
         cudaMemcpyAsync((char*)out_h + q0, (const char*)out_d + q0, nq, cudaMemcpyDefault, hp->out) != cudaSuccess)
       rc = ATTN_ECUDA;
   }
   // Whatever was enqueued, `stream` waits for both library streams.
   const bool joined = cudaEventRecord(hp->done, hp->in) == cudaSuccess &&
+                      cudaStreamWaitEvent(stream, hp->done, 0) == cudaSuccess &&
+                      cudaEventRecord(hp->done, hp->comp2) == cudaSuccess &&
                       cudaStreamWaitEvent(stream, hp->done, 0) == cudaSuccess &&
                       cudaEventRecord(hp->done, hp->out) == cudaSuccess &&
                       cudaStreamWaitEvent(stream, hp->done, 0) == cudaSuccess;
