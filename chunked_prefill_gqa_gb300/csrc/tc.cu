@@ -435,6 +435,11 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
         for (int j = jb; j < je; ++j, ++n) {
           const int st = n % stages;
           uint64_t* freed = is_k ? &bars.kempty[st] : &bars.vempty[st];
+          // Page pools: each lane's block-table entry is read before the wait
+          // for the stage, so its latency passes while the stage drains.
+          const int lp = j * (kBc / kPage) + lane;
+          int phys = 0;
+          if (kMode == kPaged && lp * kPage < p.P + p.C) phys = __ldg(prm.table + lp);
           if constexpr (kMode == kPaged) {
             // The four lanes leave together or not at all.
             const bool ok = n < stages || wait_bar(freed, ((n / stages) - 1) & 1, prm, abort_flag);
@@ -451,10 +456,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
             // Lane 0 posts the tile's bytes before any of its boxes is issued.
             if (lane == 0) mbar_arrive_expect_tx(full, 2 * kHalf);
             __syncwarp((1u << kLanes) - 1);
-            const int lp = j * (kBc / kPage) + lane;
             int y = prm.num_pages * kPage;
             if (lp * kPage < p.P + p.C) {
-              const int phys = __ldg(prm.table + lp);
               if (phys >= 0 && phys < prm.num_pages)
                 y = phys * kPage;
               else
