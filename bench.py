@@ -265,7 +265,7 @@ def launches_per_call(path: str, C: int, P: int) -> int:
     the library's own rule for its split-unit grid, on 32-row query tiles x 8
     KV heads and the device's SMs. A second grid of CTA pairs takes the last
     round's units when that round would leave more than half of the SMs idle
-    and every unit sees 1024 keys or more (8192 for the bf16 paths). With at most
+    and every unit sees 1024 keys or more. With at most
     half as many units as SMs, long units are all split in a single grid of
     pairs instead of the whole-unit grid: still one launch."""
     if path not in ("attn_prefill", "attn_prefill_bf16x3", "attn_prefill_bf16kv"):
@@ -273,7 +273,7 @@ def launches_per_call(path: str, C: int, P: int) -> int:
     units = -(-C // 32) * 8
     if units > NUM_SMS:
         rem = units % NUM_SMS
-        ok = P + min(32, C) >= (8192 if path != "attn_prefill" else 1024)  # the shortest unit's keys
+        ok = P + min(32, C) >= 1024  # the shortest unit's keys
         return 2 if rem > 0 and 2 * rem <= (NUM_SMS & ~1) and ok else 1
     return 1  # one grid: whole units, or (at most half as many units as SMs) all split
 

@@ -95,6 +95,8 @@ constexpr uint32_t kTmemCols = 512;
 // q1 and q2 come first (two 16 KB K-major operands), then three K stages and two
 // V stages. The bf16 cache has four stages of each.
 constexpr uint32_t kOperandBytes = kBc * kD * 2;  // 16 KB
+constexpr uint32_t kShareO = 128 * 256;          // split-unit share: O rows, then m and l
+constexpr uint32_t kShareBytes = kShareO + 2 * 128 * 4;
 template <bool kF32>
 struct Layout {
   static constexpr int kKS = kF32 ? 3 : 4;  // K ring stages
@@ -107,8 +109,7 @@ struct Layout {
   static constexpr uint32_t kNumBars = 3 * kKS + 3 * kVS + 9 + 1 + 2 + 4 + 2;
   static constexpr uint32_t kSmemRed = kSmemBar + kNumBars * 8 + 16;  // [2 tile parities][2 key halves][128 rows]
   static constexpr uint32_t kSmemLsum = kSmemRed + 2 * 2 * 128 * 4;   // [2 key halves][128 rows]
-  static constexpr uint32_t kSmemSlot = kSmemLsum + 2 * 128 * 4;    // tail kernel: rank 1's m and l per row
-  static constexpr uint32_t kSmemTotal = kSmemSlot + 2 * 128 * 4;
+  static constexpr uint32_t kSmemTotal = kSmemLsum + 2 * 128 * 4;
   static constexpr uint32_t kSmemAlloc = kSmemTotal + 1024;
   static_assert(kSmemAlloc <= 232448, "exceeds the 227 KB per-block shared memory limit");
 };
@@ -143,7 +144,7 @@ struct Bars {
   uint64_t* qready;  // Q hi/lo in TMEM
   uint64_t* drain;   // [2] MMA issuers' drain on abort
   uint64_t* pair;    // [4] row-set exchanges of the softmax warps
-  uint64_t* partner;   // tail kernel, rank 0: rank 1's share of the unit is in place (256 remote arrivals)
+  uint64_t* partner;   // tail kernel, rank 0: rank 1's share of the unit has landed (one arrival + bulk-copy bytes)
   uint64_t* slotfree;  // tail kernel, rank 1: rank 0's K ring is free for that share (256 remote arrivals)
 };
 
@@ -321,7 +322,7 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
     mbar_init(&bars.drain[1], 1);
     for (int q = 0; q < 4; ++q) mbar_init(&bars.pair[q], 2);
     if constexpr (kTail) {
-      mbar_init(bars.partner, kSoftmaxWarps * 32);
+      mbar_init(bars.partner, 1);
       mbar_init(bars.slotfree, kSoftmaxWarps * 32);
     }
     *abort_flag = 0;
@@ -691,14 +692,13 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
         // A unit split over the CTA pair; this thread holds 32 of its row's 64
         // output dims (head dims 32 kh ..), and l and the reference maximum of
         // this CTA's key tiles (none when it got no tile). The output is only
-        // written: rank 0, once its last PV has completed (its K ring is then
-        // idle), tells rank 1 so; rank 1 writes its unnormalised O (row `row`
-        // of a [128][64] fp32 share at the start of rank 0's K ring, 16-byte
-        // chunk i of the row at chunk i ^ (row mod 16)) and, from one warp of
-        // the row set, m and l into rank 0's slot through distributed shared
-        // memory, then arrives on rank 0's partner barrier (release at cluster
-        // scope); rank 0 merges, m = max(m0, m1) with weights e^(m_s - m) (in
-        // log2 units, (m_s - m) c), one reciprocal per row, and stores.
+        // written: rank 1 stages its unnormalised O, m and l in its own K ring;
+        // rank 0, once its last PV has completed (its K ring is then idle),
+        // tells rank 1 so, and each warp of rank 1 copies its part in bulk
+        // (cp.async.bulk between the CTAs' shared memories) into rank 0's K
+        // ring, the bytes completing on rank 0's partner barrier; rank 0
+        // merges, m = max(m0, m1) with weights e^(m_s - m) (in log2 units,
+        // (m_s - m) c), one reciprocal per row, and stores.
         float o[32];
         if (has) {
           const int pb = (n - 1) % kNumS;
@@ -717,27 +717,44 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = 0.f;
         }
-        float* slot = reinterpret_cast<float*>(smem + L::kSmemSlot);  // [m of rank 1][l of rank 1], per row
+        // The share: [head-dim half kh][row][32 floats], a row's 16-byte chunk
+        // i at chunk i ^ (row mod 8), then the 128 maxima and the 128 sums.
         uint8_t* share = smem + kSmemK;
-        auto share_offset = [&](int i) -> uint32_t {  // this thread's chunk i (4 floats) of its row
-          return (uint32_t)row * 256u + (uint32_t)(((kh * 8 + i) ^ (row & 15)) * 16);
+        float* ml = reinterpret_cast<float*>(share + kShareO);
+        auto share_offset = [&](int i) -> uint32_t {  // this thread's chunk i (4 floats) of its row half
+          return (uint32_t)kh * 16384u + (uint32_t)row * 128u + (uint32_t)((i ^ (row & 7)) * 16);
         };
         const uint32_t peer = rank ^ 1u;
         if (rank == 1) {
-          if (!wait_bar_cluster_warp(bars.slotfree, 0, prm, abort_flag)) goto softmax_done;
-          const uint32_t remote = mapa_shared(smem_u32(share), peer);
+          // Stage in this CTA's own K ring (its MMAs are complete); once rank
+          // 0's K ring is free, each warp copies its 32 row halves (and, for
+          // kh = 0, their maxima and sums) in bulk into rank 0's, completing
+          // on rank 0's partner barrier.
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            st_shared_cluster_v4(remote + share_offset(i), o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+            *reinterpret_cast<float4*>(share + share_offset(i)) =
+                make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
           if (kh == 0) {
-            st_shared_cluster_f32(mapa_shared(smem_u32(slot + row), peer), m_ref);
-            st_shared_cluster_f32(mapa_shared(smem_u32(slot + 128 + row), peer), l);
+            ml[row] = m_ref;
+            ml[128 + row] = l;
           }
-          mbar_arrive_remote(mapa_shared(smem_u32(bars.partner), peer));
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (!wait_bar_cluster_warp(bars.slotfree, 0, prm, abort_flag)) goto softmax_done;
+          if ((row & 31) == 0) {
+            const uint32_t bar = mapa_shared(smem_u32(bars.partner), peer);
+            uint8_t* part = share + (uint32_t)kh * 16384u + (uint32_t)row * 128u;
+            bulk_copy_to_cluster(mapa_shared(smem_u32(part), peer), part, 32 * 128, bar);
+            if (kh == 0) {
+              bulk_copy_to_cluster(mapa_shared(smem_u32(ml + row), peer), ml + row, 32 * 4, bar);
+              bulk_copy_to_cluster(mapa_shared(smem_u32(ml + 128 + row), peer), ml + 128 + row, 32 * 4, bar);
+            }
+          }
         } else {
           mbar_arrive_remote(mapa_shared(smem_u32(bars.slotfree), peer));
+          if (row == 0 && kh == 0) mbar_arrive_expect_tx(bars.partner, kShareBytes);
           if (!wait_bar_cluster_warp(bars.partner, 0, prm, abort_flag)) goto softmax_done;
-          const float m1 = slot[row], l1 = slot[128 + row];
+          const float m1 = ml[row], l1 = ml[128 + row];
           const float m = fmaxf(l > 0.f ? m_ref : -INFINITY, l1 > 0.f ? m1 : -INFINITY);
           const float e0 = l > 0.f ? ex2((m_ref - m) * c) : 0.f;
           const float e1 = l1 > 0.f ? ex2((m1 - m) * c) : 0.f;
@@ -879,15 +896,15 @@ int launch_impl(const Problem& p, cudaStream_t stream) {
   // Split units, as for the split-TF32 kernel: with several rounds, a short
   // last round's units go to a second grid of CTA pairs that each split one;
   // with at most half as many units as SMs, every unit is split over a pair.
-  // This kernel only splits units of 8192 keys or more:
-  // measured, with the serving chunk's 2080 to 4096 the split costs about 1 %
-  // more than the imbalance it removes.
+  // Units of 1024 keys or more, as there: with the bulk-copy hand-off the
+  // split measured 329.7 -> 334.1 TFLOP/s at the serving chunk for bf16x3
+  // (the bf16 cache unchanged); with the remote stores it had cost about 1 %.
   Params main_prm = prm, tail_prm = prm;
   int main_grid = grid, tail_units = 0;
   if (prm.n_units > grid) {
     const int full = prm.n_units / grid * grid;
     const int rem = prm.n_units - full;
-    if (rem > 0 && 2 * rem <= (num_sms & ~1) && unit_keys(p.P, p.C, 0, kBq) >= 8192) {
+    if (rem > 0 && 2 * rem <= (num_sms & ~1) && unit_keys(p.P, p.C, 0, kBq) >= 1024) {
       main_prm.n_units = full;
       tail_prm.unit_base = full;
       tail_units = rem;

@@ -52,7 +52,7 @@ def test_ffma_roofline_is_the_fp32_pipe():
     ("attn_prefill", 256, 32768, 1),      # 64 units: all split in one pair grid
     ("attn_prefill", 608, 0, 1),          # exactly one round
     ("attn_prefill", 640, 0, 1),          # the shortest unit sees fewer than 1024 keys
-    ("attn_prefill_bf16kv", 2048, 2048, 1),  # the bf16 paths split only units of 8192 keys or more
+    ("attn_prefill_bf16kv", 2048, 2048, 2),  # the bf16 paths take the same last-round rule
     ("attn_prefill_bf16kv", 2048, 30720, 2),
     ("attn_decode_paged", 16, 16384, 1),
 ])

@@ -70,6 +70,7 @@ def test_every_unit_split_max_in_last_tile(cp, variant):
 # query tile 24 rows short.
 @pytest.mark.parametrize("path,C,P", [
     ("attn_prefill", 2040, 100), ("attn_prefill_paged", 2040, 100), ("attn_prefill_bf16kv", 2040, 8200),
+    ("attn_prefill_bf16kv", 2040, 1000), ("attn_prefill_bf16x3", 2040, 1000),
 ])
 def test_tail_grid_ragged(cp, path, C, P):
     run(cp, path, W.edge(C, P, seed=7))
