@@ -896,12 +896,13 @@ int launch_impl(const Problem& p, cudaStream_t stream) {
   // Split units, as for the split-TF32 kernel: with several rounds, a short
   // last round's units go to a second grid of CTA pairs that each split one;
   // with at most half as many units as SMs, every unit is split over a pair.
-  // The same rules as there (the last round: units of 1024 keys or more;
-  // every unit: the longest of 2048 or more). With the bulk-copy hand-off the
-  // last-round split measured 329.7 -> 334.1 TFLOP/s at the serving chunk for
-  // bf16x3 (the bf16 cache unchanged), and splitting every unit of small
-  // chunks against 2048-8192 keys 1.27-1.6x (with the remote stores both had
-  // been kept to units of 8192 keys or more).
+  // Rules as there (the last round: units of 1024 keys or more; every unit:
+  // the longest of 1024 or more, these 128-key tiles making shorter halves
+  // too small). With the bulk-copy hand-off the last-round split measured
+  // 329.7 -> 334.1 TFLOP/s at the serving chunk for bf16x3 (the bf16 cache
+  // unchanged), and splitting every unit of small chunks against 1024-8192
+  // keys 1.1-1.6x (with the remote stores both had been kept to units of
+  // 8192 keys or more).
   Params main_prm = prm, tail_prm = prm;
   int main_grid = grid, tail_units = 0;
   if (prm.n_units > grid) {
@@ -912,7 +913,7 @@ int launch_impl(const Problem& p, cudaStream_t stream) {
       tail_prm.unit_base = full;
       tail_units = rem;
     }
-  } else if (2 * prm.n_units <= num_sms && unit_keys(p.P, p.C, (prm.n_qtiles - 1) * kBq, kBq) >= 2048) {
+  } else if (2 * prm.n_units <= num_sms && unit_keys(p.P, p.C, (prm.n_qtiles - 1) * kBq, kBq) >= 1024) {
     // Measured: splitting only some of the units (more than half as many
     // units as SMs) costs more than it gains.
     const int split = prm.n_units;

@@ -1,8 +1,8 @@
 """The split-unit grids against the oracle, every element checked on a poisoned,
 guarded output: chunks small enough that every unit is split over a CTA pair
-(the longest unit of 2048 keys or more), and chunks whose last round of units
-goes to the pair grid (the tail), including a ragged last query tile and a
-paged cache."""
+(the longest unit of 512 keys or more, 1024 for the bf16 kernels), and chunks
+whose last round of units goes to the pair grid (the tail), including a ragged
+last query tile and a paged cache."""
 import numpy as np
 import pytest
 
@@ -55,6 +55,8 @@ def run(cp, path, inp):
     ("attn_prefill", 288, 2500), ("attn_prefill_paged", 100, 3000), ("attn_prefill_paged", 17, 4100),
     ("attn_prefill_bf16kv", 64, 8200), ("attn_prefill_bf16kv", 288, 8192), ("attn_prefill_bf16x3", 100, 8300),
     ("attn_prefill_bf16kv", 256, 2048), ("attn_prefill_bf16x3", 64, 3000), ("attn_prefill_bf16kv", 17, 4100),
+    ("attn_prefill", 128, 700), ("attn_prefill", 33, 500), ("attn_prefill_paged", 64, 900),
+    ("attn_prefill_bf16kv", 64, 1200), ("attn_prefill_bf16x3", 100, 1000),
 ])
 def test_every_unit_split(cp, path, C, P):
     run(cp, path, W.edge(C, P, seed=C + P))
