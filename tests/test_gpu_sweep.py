@@ -110,8 +110,9 @@ def _large_shapes(n=5, seed=77):
 def test_sweep_large_chunks(cp, C, P):
     """Chunks of several rounds of units, where the whole-unit grid and the
     split-unit pair grid share the work (the pair grid merging its two halves
-    through distributed shared memory): every output of the three kernels that
-    have a pair grid against the oracle."""
+    through distributed shared memory): every output of the four paths that
+    have a pair grid (contiguous and paged split-TF32, bf16x3, bf16 cache)
+    against the oracle."""
     inp = W.edge(C, P, seed=C * 7 + P)
     ref = oracle.prefill(inp)
     q, k, v = device_inputs(inp)
@@ -121,6 +122,13 @@ def test_sweep_large_chunks(cp, C, P):
         torch.cuda.synchronize()
         assert g.guards_intact(), path
         check(g.numpy(), ref, f"{path} C={C} P={P}")
+    pg = W.to_pages(inp, seed=C + 3 * P)
+    g = GuardedOut(C)
+    cp.attn_prefill_paged(q, torch.from_numpy(pg.k_pages).cuda(), torch.from_numpy(pg.v_pages).cuda(),
+                          torch.from_numpy(pg.table).cuda(), g.out, P)
+    torch.cuda.synchronize()
+    assert g.guards_intact()
+    check(g.numpy(), ref, f"paged C={C} P={P}")
     kv = W.to_bf16(inp)
     g = GuardedOut(C)
     cp.attn_prefill_bf16kv(q, torch.from_numpy(kv.k.view(np.int16)).cuda().view(torch.bfloat16),
