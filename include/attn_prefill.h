@@ -95,7 +95,8 @@ extern "C" {
  * error-compensated split-TF32: each fp32 operand x = hi + lo with hi exactly
  * representable in tf32, and each product accumulates hi*hi + hi*lo + lo*hi in
  * fp32, so the result matches exact fp32 products to about 2^-20 relative.
- * When the last round of units would leave more than half of the SMs idle, a
+ * When the last round of units would leave at least half of the SMs idle and
+ * every unit sees 1024 keys or more, a
  * second grid of two-CTA clusters takes those units, each pair splitting one
  * along its keys and merging the two partials with the split-K rule (same
  * page, Flash-Decoding and the split-K merge); a chunk with at most half as
@@ -149,7 +150,7 @@ int attn_prefill_bf16kv(const float *q, const uint16_t *kCache, const uint16_t *
  * compute of sub-chunk s, on two copy streams the library keeps per device,
  * and consecutive sub-chunks compute alternately on `stream` and on a third
  * library stream, so a sub-chunk's blocks take SMs as the previous one's
- * finish (serving chunk end to end: 0.360 -> 0.332 ms). Each sub-chunk's rows are exactly
+ * finish (serving chunk end to end: 0.351 -> 0.325 ms). Each sub-chunk's rows are exactly
  * those of the device-pointer entry point called on that sub-chunk; against one
  * call on the whole chunk they agree to rounding (that call may split its last
  * round's units over CTA pairs, another summation order).
@@ -171,8 +172,8 @@ int attn_prefill_bf16kv(const float *q, const uint16_t *kCache, const uint16_t *
  * call, and `stream` waits for the last copy-out: synchronising `stream`
  * observes out_host complete. Calls from several host threads are serialised
  * while they enqueue (the library's per-device streams and events are shared).
- * Set-up. The first call on a device creates two non-blocking streams and ten
- * events (no device memory); they live until the process ends.
+ * Set-up. The first call on a device creates three non-blocking streams and
+ * ten events (no device memory); they live until the process ends.
  * Errors: those of the device-pointer entry point for the device buffers and
  * sizes; ATTN_EINVAL for a NULL host pointer with C > 0; ATTN_ECUDA when a copy
  * or a stream or event call fails. After an error, copies may already have
