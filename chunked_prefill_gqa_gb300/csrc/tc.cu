@@ -326,13 +326,108 @@ __device__ __forceinline__ bool split_epilogue(uint8_t* smem, uint32_t lane_tmem
   return true;
 }
 
+// The same for a unit split over a cluster of four CTAs: ranks 1-3 stage
+// their shares in their own Q regions, and once rank 0's last PV has
+// completed (its Q region and K ring are then idle) they copy them in bulk
+// into three consecutive slots there (rank r into slot r - 1); rank 0 merges
+// the four partials with the same rule, m = the largest maximum of a CTA with
+// tiles, each partial weighted by e^(m_s - m).
+static_assert(kSmemQ + 3 * kShareBytes <= kSmemV, "three shares fit in the Q region and the K ring");
+__device__ __forceinline__ bool split_epilogue4(uint8_t* smem, uint32_t lane_tmem, int n, bool has, const Bars& bars,
+                                                const Params& prm, volatile int* abort_flag, uint32_t rank, int row,
+                                                float m_ref, float l, float c, bool store, float* dst) {
+  float o[64];
+  if (has) {
+    const int pb = (n - 1) % kNumS;
+    if (!wait_bar_warp(&bars.odone[pb], ((n - 1) / kNumS) & 1, prm, abort_flag)) return false;
+    tc_fence_after();
+#pragma unroll
+    for (int dh = 0; dh < 2; ++dh) {
+      float a[32], b[32];
+      tmem_ld32(lane_tmem + kColO + dh * 32, a);
+      tmem_ld32(lane_tmem + kColO + 64 + dh * 32, b);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) o[dh * 32 + i] = a[i] + b[i];
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 64; ++i) o[i] = 0.f;
+  }
+  uint8_t* share = smem + kSmemQ;
+  if (rank != 0) {
+    float* ml = reinterpret_cast<float*>(share + kShareO);  // [m of the rows][l of the rows]
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      *reinterpret_cast<float4*>(share + share_offset(row, i)) =
+          make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+    ml[row] = m_ref;
+    ml[kM + row] = l;
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (!wait_bar_cluster_warp(bars.slotfree, 0, prm, abort_flag)) return false;
+    if ((row & 31) == 0) {
+      const uint32_t bar = mapa_shared(smem_u32(bars.partner), 0);
+      const uint32_t slot = smem_u32(share) + (rank - 1) * kShareBytes;  // the same offset in rank 0
+      const uint32_t o_off = (uint32_t)row * 256u;
+      bulk_copy_to_cluster(mapa_shared(slot + o_off, 0), share + o_off, 32 * 256, bar);
+      bulk_copy_to_cluster(mapa_shared(slot + kShareO + row * 4, 0), ml + row, 32 * 4, bar);
+      bulk_copy_to_cluster(mapa_shared(slot + kShareO + (kM + row) * 4, 0), ml + kM + row, 32 * 4, bar);
+    }
+  } else {
+#pragma unroll
+    for (uint32_t r = 1; r < 4; ++r) mbar_arrive_remote(mapa_shared(smem_u32(bars.slotfree), r));
+    if (row == 0) mbar_arrive_expect_tx(bars.partner, 3 * kShareBytes);
+    if (!wait_bar_cluster_warp(bars.partner, 0, prm, abort_flag)) return false;
+    float ms[3], ls[3];
+    float m = l > 0.f ? m_ref : -INFINITY;
+#pragma unroll
+    for (int r = 0; r < 3; ++r) {
+      const float* ml = reinterpret_cast<const float*>(share + r * kShareBytes + kShareO);
+      ms[r] = ml[row];
+      ls[r] = ml[kM + row];
+      if (ls[r] > 0.f) m = fmaxf(m, ms[r]);
+    }
+    const float e0 = l > 0.f ? ex2((m_ref - m) * c) : 0.f;
+    float den = e0 * l;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) o[i] *= e0;
+#pragma unroll
+    for (int r = 0; r < 3; ++r) {
+      const uint8_t* slot = share + r * kShareBytes;
+      const float er = ls[r] > 0.f ? ex2((ms[r] - m) * c) : 0.f;
+      den = fmaf(er, ls[r], den);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float4 x = *reinterpret_cast<const float4*>(slot + share_offset(row, i));
+        o[4 * i] = fmaf(er, x.x, o[4 * i]);
+        o[4 * i + 1] = fmaf(er, x.y, o[4 * i + 1]);
+        o[4 * i + 2] = fmaf(er, x.z, o[4 * i + 2]);
+        o[4 * i + 3] = fmaf(er, x.w, o[4 * i + 3]);
+      }
+    }
+    const float inv = 1.f / den;  // > 0: the unit sees at least key 0
+    if (store) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        *reinterpret_cast<float4*>(dst + 4 * i) =
+            make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv, o[4 * i + 3] * inv);
+    }
+  }
+  return true;
+}
+
 // Instantiations. kMain: whole units in snake order; it decides by prm.table
 // at run time (it is the one launched for contiguous caches; measured,
 // dropping its paged branch slows it). kPaged: the same for page pools only.
 // kTail: launched after kMain as clusters of two CTAs; pair p splits unit
 // unit_base + p along its key tiles (rank 0 the first half, rank 1 the rest)
 // and merges the two online-softmax partials through distributed shared memory.
-constexpr int kMain = 0, kPaged = 1, kTail = 2;
+// kTail4: the same with clusters of four CTAs, each a quarter of the unit's
+// tiles (small chunks, whose units are too few to fill the SMs as pairs).
+constexpr int kMain = 0, kPaged = 1, kTail = 2, kTail4 = 3;
+template <int kMode>
+__host__ __device__ constexpr bool is_tail() { return kMode == kTail || kMode == kTail4; }
 
 // Unit u's tiles for this CTA: all of them, or the tail kernel's half.
 template <int kMode>
@@ -340,17 +435,21 @@ __device__ __forceinline__ void unit_range(const Unit& w, uint32_t rank, int* jb
   if constexpr (kMode == kTail) {
     *jb = rank == 0 ? 0 : w.ntiles / 2;
     *je = rank == 0 ? w.ntiles / 2 : w.ntiles;
+  } else if constexpr (kMode == kTail4) {
+    *jb = (int)rank * w.ntiles / 4;
+    *je = ((int)rank + 1) * w.ntiles / 4;
   } else {
     *jb = 0;
     *je = w.ntiles;
   }
 }
 
-// The CTA's k-th unit (kMain, kPaged: snake order; kTail: one per pair), or
-// n_units when it has none.
+// The CTA's k-th unit (kMain, kPaged: snake order; kTail, kTail4: one per
+// cluster), or n_units when it has none.
 template <int kMode>
 __device__ __forceinline__ int work_unit(int k, int cta, int grid, const Params& prm) {
   if constexpr (kMode == kTail) return k == 0 ? prm.unit_base + (cta >> 1) : prm.n_units;
+  else if constexpr (kMode == kTail4) return k == 0 ? prm.unit_base + (cta >> 2) : prm.n_units;
   else return unit_index(k, cta, grid);
 }
 
@@ -386,7 +485,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
     mbar_init(bars.qready, kSoftmaxWarps);
     mbar_init(&bars.drain[0], 1);
     mbar_init(&bars.drain[1], 1);
-    if constexpr (kMode == kTail) {
+    if constexpr (is_tail<kMode>()) {
       mbar_init(bars.partner, 1);
       mbar_init(bars.slotfree, kSoftmaxWarps * 32);
     }
@@ -403,16 +502,16 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  if constexpr (kMode == kTail) {
-    // Both CTAs of the pair are running and their barriers initialised before
-    // either can touch the other's shared memory.
+  if constexpr (is_tail<kMode>()) {
+    // Every CTA of the cluster is running and its barriers initialised before
+    // any can touch another's shared memory.
     cluster_sync_all();
   } else {
     // A tail launch after this one (a programmatic dependent) may start its
     // blocks on SMs as soon as blocks of this grid leave them.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   }
-  const uint32_t rank = kMode == kTail ? cluster_ctarank() : 0u;
+  const uint32_t rank = is_tail<kMode>() ? cluster_ctarank() : 0u;
 
   const int cta = blockIdx.x, grid = gridDim.x;
   const Problem& p = prm.p;
@@ -515,7 +614,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
         const Unit w = decode_unit(u, prm);
         int jb, je;
         unit_range<kMode>(w, rank, &jb, &je);
-        if constexpr (kMode == kTail) {
+        if constexpr (is_tail<kMode>()) {
           if (jb == je) continue;  // no tiles here (its Q is not loaded either)
         }
         if (is_qk) {
@@ -798,6 +897,13 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
           goto softmax_done;
         tc_fence_before();
         continue;
+      } else if constexpr (kMode == kTail4) {
+        float* dst = p.out + ((size_t)pos * kHQ + w.g * kGroup + (row & 3)) * kD;
+        if (!split_epilogue4(smem, lane_tmem, n, has, bars, prm, abort_flag, rank, row, m_ref, l, c, pos < p.C,
+                             dst))
+          goto softmax_done;
+        tc_fence_before();
+        continue;
       }
       // Epilogue: wait for the last PV, add the two stacked halves of O' and
       // normalise by the row's l: one reciprocal per row and a multiply per
@@ -837,13 +943,13 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if constexpr (kMode == kTail) {
-    // Neither CTA of the pair leaves while the other may still write its
-    // shared memory or arrive on its barriers.
+  if constexpr (is_tail<kMode>()) {
+    // No CTA of the cluster leaves while another may still write its shared
+    // memory or arrive on its barriers.
     cluster_sync_all();
   }
   if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
-  if constexpr (kMode == kTail) {
+  if constexpr (is_tail<kMode>()) {
     // This grid ends only after the grid of whole units it overlaps: work
     // ordered after it on the stream sees both complete.
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -892,6 +998,7 @@ int encode_kv_map(const float* base, int rows, int box_rows, CUtensorMapSwizzle 
 struct TcDeviceState {
   bool ready = false;
   int num_sms = 0;
+  int quads = 0;  // clusters of four tail CTAs the device holds at once
 };
 TcDeviceState g_tc_state[64];
 std::mutex g_tc_state_mu;
@@ -900,7 +1007,7 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
                    const int* table = nullptr, int num_pages = 0) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ECUDA;
-  int num_sms = 0;
+  int num_sms = 0, quads = 0;
   {
     std::lock_guard<std::mutex> lock(g_tc_state_mu);
     TcDeviceState& st = g_tc_state[dev];
@@ -912,11 +1019,31 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
           cudaFuncSetAttribute(tc_kernel<kPaged>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc) !=
               cudaSuccess ||
           cudaFuncSetAttribute(tc_kernel<kTail>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc) !=
+              cudaSuccess ||
+          cudaFuncSetAttribute(tc_kernel<kTail4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc) !=
               cudaSuccess)
         return ATTN_ECUDA;
+      // How many clusters of four fit at once (0 when the query fails: no
+      // four-way split then).
+      cudaLaunchConfig_t qc = {};
+      qc.gridDim = dim3(4 * kHKV);
+      qc.blockDim = dim3(kThreads);
+      qc.dynamicSmemBytes = kSmemAlloc;
+      cudaLaunchAttribute qa[1];
+      qa[0].id = cudaLaunchAttributeClusterDimension;
+      qa[0].val.clusterDim.x = 4;
+      qa[0].val.clusterDim.y = 1;
+      qa[0].val.clusterDim.z = 1;
+      qc.attrs = qa;
+      qc.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&st.quads, tc_kernel<kTail4>, &qc) != cudaSuccess) {
+        st.quads = 0;
+        (void)cudaGetLastError();
+      }
       st.ready = true;
     }
     num_sms = st.num_sms;
+    quads = st.quads;
   }
   alignas(64) CUtensorMap mk, mv;
   const int rows = table ? num_pages * kPage : p.P + p.C;
@@ -937,15 +1064,18 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
   // Split units. With several rounds, when the last round of whole units would
   // leave more than half of the SMs idle, the full rounds run as one grid and
   // the remaining units as a second grid of CTA pairs that each split one unit.
-  // With at most half as many units as SMs and the longest unit of 512 keys or
+  // With at most half as many units as SMs and the longest unit of 256 keys or
   // more, every unit is split over a pair (with the bulk-copy hand-off,
   // measured 1.1-1.3x faster for chunks against 500-2000 keys; from 2048 keys
-  // it already was). (The two grids can also split only the longest s units,
-  // the whole-unit grid starting s / 8 q-tiles down.) The pair grid
-  // is a programmatic dependent of the whole-unit grid: its pairs take SMs as
-  // soon as they are free.
+  // it already was; 1.1x against 250-500 keys), and over a cluster of four
+  // when the device holds one for every unit (chunks of 128 rows or less on
+  // 152 SMs: measured 1.4-1.9x faster than pairs against 2000-32768 keys,
+  // 1.1-1.2x against 600-1500). (The two grids can also split only the
+  // longest s units, the whole-unit grid starting s / 8 q-tiles down.) The
+  // pair grid is a programmatic dependent of the whole-unit grid: its pairs
+  // take SMs as soon as they are free.
   Params main_prm = prm, tail_prm = prm;
-  int main_grid = grid, tail_units = 0;
+  int main_grid = grid, tail_units = 0, split = 2;
   if (prm.n_units > grid) {
     // (Only when even the shortest unit sees 1024 keys: measured, a full
     // prompt's last round of 32-224 keys runs slower split.)
@@ -956,18 +1086,13 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
       tail_prm.unit_base = full;
       tail_units = rem;
     }
-  } else if (2 * prm.n_units <= num_sms && unit_keys(p.P, p.C, (prm.n_qtiles - 1) * kBq, kBq) >= 512) {
+  } else if (2 * prm.n_units <= num_sms && unit_keys(p.P, p.C, (prm.n_qtiles - 1) * kBq, kBq) >= 256) {
     // Measured: splitting only some of the units (more than half as many
     // units as SMs) costs more than it gains.
-    const int split = prm.n_units;
-    {
-      main_prm.n_qtiles -= split / kHKV;
-      main_prm.n_units -= split;
-      main_grid = main_prm.n_units;
-      tail_prm.unit_base = 0;
-      tail_prm.n_units = split;
-      tail_units = split;
-    }
+    main_prm.n_units = 0;
+    tail_prm.unit_base = 0;
+    tail_units = prm.n_units;
+    if (prm.n_units <= quads) split = 4;
   }
   if (main_prm.n_units > 0) {
     if (table)
@@ -978,20 +1103,21 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
   }
   if (tail_units == 0) return ATTN_OK;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * tail_units);
+  cfg.gridDim = dim3(split * tail_units);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemAlloc;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = split;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = main_prm.n_units > 0 ? 2 : 1;  // a dependent only of a whole-unit grid
-  if (cudaLaunchKernelEx(&cfg, tc_kernel<kTail>, mk, mv, tail_prm) != cudaSuccess) return ATTN_ELAUNCH;
+  if (cudaLaunchKernelEx(&cfg, split == 4 ? tc_kernel<kTail4> : tc_kernel<kTail>, mk, mv, tail_prm) != cudaSuccess)
+    return ATTN_ELAUNCH;
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ELAUNCH;
 }
 

@@ -187,20 +187,25 @@ __device__ __forceinline__ Unit decode_unit(int u, const Params& prm) {
   return w;
 }
 
-// kTail == false: whole units in snake order. kTail: launched after that grid
-// as clusters of two CTAs; pair p splits unit unit_base + p along its key tiles
-// (rank 0 the first half, rank 1 the rest) and merges the two online-softmax
-// partials through distributed shared memory.
-template <bool kTail>
+// kSplit == 1: whole units in snake order. kSplit == 2: launched after that
+// grid as clusters of two CTAs; pair p splits unit unit_base + p along its key
+// tiles (rank 0 the first half, rank 1 the rest) and merges the two
+// online-softmax partials through distributed shared memory. kSplit == 4: the
+// same with clusters of four CTAs, a quarter of the tiles each (small chunks).
+template <int kSplit>
 __device__ __forceinline__ int work_unit(int k, int cta, int grid, const Params& prm) {
-  if constexpr (kTail) return k == 0 ? prm.unit_base + (cta >> 1) : prm.n_units;
+  if constexpr (kSplit == 2) return k == 0 ? prm.unit_base + (cta >> 1) : prm.n_units;
+  else if constexpr (kSplit == 4) return k == 0 ? prm.unit_base + (cta >> 2) : prm.n_units;
   else return unit_index(k, cta, grid);
 }
-template <bool kTail>
+template <int kSplit>
 __device__ __forceinline__ void unit_range(const Unit& w, uint32_t rank, int* jb, int* je) {
-  if constexpr (kTail) {
+  if constexpr (kSplit == 2) {
     *jb = rank == 0 ? 0 : w.ntiles / 2;
     *je = rank == 0 ? w.ntiles / 2 : w.ntiles;
+  } else if constexpr (kSplit == 4) {
+    *jb = (int)rank * w.ntiles / 4;
+    *je = ((int)rank + 1) * w.ntiles / 4;
   } else {
     *jb = 0;
     *je = w.ntiles;
@@ -282,10 +287,11 @@ __device__ __forceinline__ void split_pack_rn(const float* x, uint32_t* hi, uint
   }
 }
 
-template <bool kF32, bool kTail>
+template <bool kF32, int kSplit>
 __global__ void __launch_bounds__(threads_of<kF32>(), 1)
 tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                const Params prm) {
+  constexpr bool kTail = kSplit > 1;
   using L = Layout<kF32>;
   constexpr uint32_t kColO = col_o<kF32>();
   constexpr uint32_t kSmemK = L::kSmemK, kSmemV = L::kSmemV, kSmemBar = L::kSmemBar, kNumBars = L::kNumBars;
@@ -339,8 +345,8 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
   if constexpr (kTail) {
-    // Both CTAs of the pair are running and their barriers initialised before
-    // either can touch the other's shared memory.
+    // Every CTA of the cluster is running and its barriers initialised before
+    // any can touch another's shared memory.
     cluster_sync_all();
   } else {
     // A tail launch after this one (a programmatic dependent) may start its
@@ -358,11 +364,11 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
     if (lane == 0) {
       int n = 0;
       for (int k = 0;; ++k) {
-        const int u = work_unit<kTail>(k, cta, grid, prm);
+        const int u = work_unit<kSplit>(k, cta, grid, prm);
         if (u >= prm.n_units) break;
         const Unit w = decode_unit(u, prm);
         int jb, je;
-        unit_range<kTail>(w, rank, &jb, &je);
+        unit_range<kSplit>(w, rank, &jb, &je);
         const int kStages = is_k ? kKS : kVS;
         for (int j = jb; j < je; ++j, ++n) {
           const int st = n % kStages;
@@ -392,11 +398,11 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
     if (lane == 0) {
       int n = 0, lu = 0;
       for (int k = 0;; ++k) {
-        const int u = work_unit<kTail>(k, cta, grid, prm);
+        const int u = work_unit<kSplit>(k, cta, grid, prm);
         if (u >= prm.n_units) break;
         const Unit w = decode_unit(u, prm);
         int jb, je;
-        unit_range<kTail>(w, rank, &jb, &je);
+        unit_range<kSplit>(w, rank, &jb, &je);
         if constexpr (kTail) {
           if (jb == je) continue;  // no tiles here (its Q is not loaded either)
         }
@@ -489,11 +495,11 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
       const int cw = (warp - kFirstConvWarp) % kConvWarpsPerOperand;
       int n = 0;
       for (int k = 0;; ++k) {
-        const int u = work_unit<kTail>(k, cta, grid, prm);
+        const int u = work_unit<kSplit>(k, cta, grid, prm);
         if (u >= prm.n_units) break;
         const Unit w = decode_unit(u, prm);
         int jb, je;
-        unit_range<kTail>(w, rank, &jb, &je);
+        unit_range<kSplit>(w, rank, &jb, &je);
         const int kStages = is_k ? kKS : kVS;
         for (int j = jb; j < je; ++j, ++n) {
           const int st = n % kStages;
@@ -589,11 +595,11 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
 
     bool q_loaded = false;
     for (int k = 0;; ++k) {
-      const int u = work_unit<kTail>(k, cta, grid, prm);
+      const int u = work_unit<kSplit>(k, cta, grid, prm);
       if (u >= prm.n_units) break;
       const Unit w = decode_unit(u, prm);
       int jb, je;
-      unit_range<kTail>(w, rank, &jb, &je);
+      unit_range<kSplit>(w, rank, &jb, &je);
       const bool has = jb < je;
       if (has && !q_loaded) load_q(w);
       q_loaded = false;
@@ -679,7 +685,7 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
         if (lane == 0) mbar_arrive(&bars.pfull[b]);
       }
       {
-        const int u_next = work_unit<kTail>(k + 1, cta, grid, prm);
+        const int u_next = work_unit<kSplit>(k + 1, cta, grid, prm);
         if (u_next < prm.n_units) {
           load_q(decode_unit(u_next, prm));
           q_loaded = true;
@@ -688,7 +694,104 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
       lred[kh * 128 + row] = l;
       if (!pair_sync()) goto softmax_done;
       l += lred[(kh ^ 1) * 128 + row];
-      if constexpr (kTail) {
+      if constexpr (kSplit == 4) {
+        // A unit split over a cluster of four, as over a pair below: ranks 1-3
+        // stage their shares in their own K rings and, once rank 0's last PV
+        // has completed (its K and V rings are then idle), copy them in bulk
+        // into three consecutive slots there (rank r into slot r - 1); rank 0
+        // merges the four partials, m = the largest maximum of a CTA with
+        // tiles, each weighted by e^(m_s - m).
+        static_assert(kSmemK + 3 * kShareBytes <= kSmemBar, "three shares fit in the K and V rings");
+        float o[32];
+        if (has) {
+          const int pb = (n - 1) % kNumS;
+          if (!wait_bar_warp(&bars.odone[pb], ((n - 1) / kNumS) & 1, prm, abort_flag)) goto softmax_done;
+          tc_fence_after();
+          tmem_ld32(lane_tmem + kColO + kh * 32, o);
+          tmem_wait_ld();
+          if (kF32) {
+            float o2[32];
+            tmem_ld32(lane_tmem + kColO + 64 + kh * 32, o2);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] += o2[i];
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = 0.f;
+        }
+        uint8_t* share = smem + kSmemK;
+        auto share_offset = [&](int i) -> uint32_t {  // this thread's chunk i (4 floats) of its row half
+          return (uint32_t)kh * 16384u + (uint32_t)row * 128u + (uint32_t)((i ^ (row & 7)) * 16);
+        };
+        if (rank != 0) {
+          float* ml = reinterpret_cast<float*>(share + kShareO);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            *reinterpret_cast<float4*>(share + share_offset(i)) =
+                make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+          if (kh == 0) {
+            ml[row] = m_ref;
+            ml[128 + row] = l;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (!wait_bar_cluster_warp(bars.slotfree, 0, prm, abort_flag)) goto softmax_done;
+          if ((row & 31) == 0) {
+            const uint32_t bar = mapa_shared(smem_u32(bars.partner), 0);
+            const uint32_t slot = smem_u32(share) + (rank - 1) * kShareBytes;  // the same offset in rank 0
+            const uint32_t part = (uint32_t)kh * 16384u + (uint32_t)row * 128u;
+            bulk_copy_to_cluster(mapa_shared(slot + part, 0), share + part, 32 * 128, bar);
+            if (kh == 0) {
+              bulk_copy_to_cluster(mapa_shared(slot + kShareO + row * 4, 0), ml + row, 32 * 4, bar);
+              bulk_copy_to_cluster(mapa_shared(slot + kShareO + (128 + row) * 4, 0), ml + 128 + row, 32 * 4, bar);
+            }
+          }
+        } else {
+#pragma unroll
+          for (uint32_t r = 1; r < 4; ++r) mbar_arrive_remote(mapa_shared(smem_u32(bars.slotfree), r));
+          if (row == 0 && kh == 0) mbar_arrive_expect_tx(bars.partner, 3 * kShareBytes);
+          if (!wait_bar_cluster_warp(bars.partner, 0, prm, abort_flag)) goto softmax_done;
+          float ms[3], ls[3];
+          float m = l > 0.f ? m_ref : -INFINITY;
+#pragma unroll
+          for (int r = 0; r < 3; ++r) {
+            const float* ml = reinterpret_cast<const float*>(share + r * kShareBytes + kShareO);
+            ms[r] = ml[row];
+            ls[r] = ml[128 + row];
+            if (ls[r] > 0.f) m = fmaxf(m, ms[r]);
+          }
+          const float e0 = l > 0.f ? ex2((m_ref - m) * c) : 0.f;
+          float den = e0 * l;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= e0;
+#pragma unroll
+          for (int r = 0; r < 3; ++r) {
+            const uint8_t* slot = share + r * kShareBytes;
+            const float er = ls[r] > 0.f ? ex2((ms[r] - m) * c) : 0.f;
+            den = fmaf(er, ls[r], den);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 x = *reinterpret_cast<const float4*>(slot + share_offset(i));
+              o[4 * i] = fmaf(er, x.x, o[4 * i]);
+              o[4 * i + 1] = fmaf(er, x.y, o[4 * i + 1]);
+              o[4 * i + 2] = fmaf(er, x.z, o[4 * i + 2]);
+              o[4 * i + 3] = fmaf(er, x.w, o[4 * i + 3]);
+            }
+          }
+          const float inv = 1.f / den;  // > 0: the unit sees at least key 0
+          if (pos < p.C) {
+            float* dst = p.out + ((size_t)pos * kHQ + w.g * kGroup + (row & 3)) * kD + kh * 32;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              *reinterpret_cast<float4*>(dst + 4 * i) =
+                  make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv, o[4 * i + 3] * inv);
+          }
+        }
+        tc_fence_before();
+        continue;
+      }
+      if constexpr (kSplit == 2) {
         // A unit split over the CTA pair; this thread holds 32 of its row's 64
         // output dims (head dims 32 kh ..), and l and the reference maximum of
         // this CTA's key tiles (none when it got no tile). The output is only
@@ -808,8 +911,8 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
   __syncthreads();
   tc_fence_after();
   if constexpr (kTail) {
-    // Neither CTA of the pair leaves while the other may still write its
-    // shared memory or arrive on its barriers.
+    // No CTA of the cluster leaves while another may still write its shared
+    // memory or arrive on its barriers.
     cluster_sync_all();
   }
   if (warp == kQkWarp) tmem_dealloc(tmem, kTmemCols);
@@ -856,8 +959,9 @@ int encode_kv_tile_map(const void* base, int rows, bool f32, CUtensorMap* map) {
 }
 
 struct DevState {
-  bool ready[2] = {false, false};  // per cache type, both instantiations set up
+  bool ready[2] = {false, false};  // per cache type, its instantiations set up
   int num_sms = 0;
+  int quads[2] = {0, 0};  // per cache type: clusters of four tail CTAs the device holds at once
 };
 DevState g_state[64];
 std::mutex g_state_mu;
@@ -866,21 +970,41 @@ template <bool kF32>
 int launch_impl(const Problem& p, cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ECUDA;
-  int num_sms = 0;
+  int num_sms = 0, quads = 0;
   {
     std::lock_guard<std::mutex> lock(g_state_mu);
     DevState& st = g_state[dev];
     if (!st.ready[kF32]) {
       if (cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return ATTN_ECUDA;
-      if (cudaFuncSetAttribute(tc_bf16_kernel<kF32, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      if (cudaFuncSetAttribute(tc_bf16_kernel<kF32, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)Layout<kF32>::kSmemAlloc) != cudaSuccess ||
-          cudaFuncSetAttribute(tc_bf16_kernel<kF32, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+          cudaFuncSetAttribute(tc_bf16_kernel<kF32, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)Layout<kF32>::kSmemAlloc) != cudaSuccess ||
+          cudaFuncSetAttribute(tc_bf16_kernel<kF32, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)Layout<kF32>::kSmemAlloc) != cudaSuccess)
         return ATTN_ECUDA;
+      // How many clusters of four fit at once (0 when the query fails: no
+      // four-way split then).
+      cudaLaunchConfig_t qc = {};
+      qc.gridDim = dim3(4 * kHKV);
+      qc.blockDim = dim3(threads_of<kF32>());
+      qc.dynamicSmemBytes = Layout<kF32>::kSmemAlloc;
+      cudaLaunchAttribute qa[1];
+      qa[0].id = cudaLaunchAttributeClusterDimension;
+      qa[0].val.clusterDim.x = 4;
+      qa[0].val.clusterDim.y = 1;
+      qa[0].val.clusterDim.z = 1;
+      qc.attrs = qa;
+      qc.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&st.quads[kF32], tc_bf16_kernel<kF32, 4>, &qc) != cudaSuccess) {
+        st.quads[kF32] = 0;
+        (void)cudaGetLastError();
+      }
       st.ready[kF32] = true;
     }
     num_sms = st.num_sms;
+    quads = st.quads[kF32];
   }
   alignas(64) CUtensorMap mk, mv;
   int rc = encode_kv_tile_map(p.k, p.P + p.C, kF32, &mk);
@@ -902,9 +1026,12 @@ int launch_impl(const Problem& p, cudaStream_t stream) {
   // 329.7 -> 334.1 TFLOP/s at the serving chunk for bf16x3 (the bf16 cache
   // unchanged), and splitting every unit of small chunks against 1024-8192
   // keys 1.1-1.6x (with the remote stores both had been kept to units of
-  // 8192 keys or more).
+  // 8192 keys or more). Every unit is split over a cluster of four instead
+  // when the device holds one for every unit (chunks of 128 rows or less on
+  // 152 SMs: measured 1.3-1.8x faster than pairs against 4096-32768 keys,
+  // 1.1x against 1200-2500).
   Params main_prm = prm, tail_prm = prm;
-  int main_grid = grid, tail_units = 0;
+  int main_grid = grid, tail_units = 0, split = 2;
   if (prm.n_units > grid) {
     const int full = prm.n_units / grid * grid;
     const int rem = prm.n_units - full;
@@ -916,37 +1043,34 @@ int launch_impl(const Problem& p, cudaStream_t stream) {
   } else if (2 * prm.n_units <= num_sms && unit_keys(p.P, p.C, (prm.n_qtiles - 1) * kBq, kBq) >= 1024) {
     // Measured: splitting only some of the units (more than half as many
     // units as SMs) costs more than it gains.
-    const int split = prm.n_units;
-    {
-      main_prm.n_qtiles -= split / kHKV;
-      main_prm.n_units -= split;
-      main_grid = main_prm.n_units;
-      tail_prm.unit_base = 0;
-      tail_prm.n_units = split;
-      tail_units = split;
-    }
+    main_prm.n_units = 0;
+    tail_prm.unit_base = 0;
+    tail_units = prm.n_units;
+    if (prm.n_units <= quads) split = 4;
   }
   if (main_prm.n_units > 0) {
-    tc_bf16_kernel<kF32, false><<<main_grid, threads_of<kF32>(), Layout<kF32>::kSmemAlloc, stream>>>(mk, mv,
+    tc_bf16_kernel<kF32, 1><<<main_grid, threads_of<kF32>(), Layout<kF32>::kSmemAlloc, stream>>>(mk, mv,
                                                                                                    main_prm);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ELAUNCH;
   }
   if (tail_units == 0) return ATTN_OK;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * tail_units);
+  cfg.gridDim = dim3(split * tail_units);
   cfg.blockDim = dim3(threads_of<kF32>());
   cfg.dynamicSmemBytes = Layout<kF32>::kSmemAlloc;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = split;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = main_prm.n_units > 0 ? 2 : 1;  // a dependent only of a whole-unit grid
-  if (cudaLaunchKernelEx(&cfg, tc_bf16_kernel<kF32, true>, mk, mv, tail_prm) != cudaSuccess) return ATTN_ELAUNCH;
+  if (cudaLaunchKernelEx(&cfg, split == 4 ? tc_bf16_kernel<kF32, 4> : tc_bf16_kernel<kF32, 2>, mk, mv, tail_prm) !=
+      cudaSuccess)
+    return ATTN_ELAUNCH;
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ELAUNCH;
 }
 

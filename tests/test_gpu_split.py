@@ -1,6 +1,8 @@
 """The split-unit grids against the oracle, every element checked on a poisoned,
-guarded output: chunks small enough that every unit is split over a CTA pair
-(the longest unit of 512 keys or more, 1024 for the bf16 kernels), and chunks
+guarded output: chunks small enough that every unit is split (the longest unit
+of 256 keys or more, 1024 for the bf16 kernels) over a cluster of four CTAs
+(at most as many units as the device holds such clusters at once: chunks of
+up to 128 rows on 152 SMs) or over a CTA pair (up to 304 rows), and chunks
 whose last round of units goes to the pair grid (the tail), including a ragged
 last query tile and a paged cache."""
 import numpy as np
@@ -49,7 +51,8 @@ def run(cp, path, inp):
     assert cp.attn_get_device_error() == 0
 
 
-# Every unit split (at most 76 units, i.e. C <= 304 rows, on 152 SMs).
+# Every unit split (at most 76 units, i.e. C <= 304 rows, on 152 SMs): over
+# clusters of four up to 128 rows, over pairs beyond.
 @pytest.mark.parametrize("path,C,P", [
     ("attn_prefill", 1, 2048), ("attn_prefill", 33, 2048), ("attn_prefill", 100, 3000),
     ("attn_prefill", 288, 2500), ("attn_prefill_paged", 100, 3000), ("attn_prefill_paged", 17, 4100),
@@ -57,6 +60,12 @@ def run(cp, path, inp):
     ("attn_prefill_bf16kv", 256, 2048), ("attn_prefill_bf16x3", 64, 3000), ("attn_prefill_bf16kv", 17, 4100),
     ("attn_prefill", 128, 700), ("attn_prefill", 33, 500), ("attn_prefill_paged", 64, 900),
     ("attn_prefill_bf16kv", 64, 1200), ("attn_prefill_bf16x3", 100, 1000),
+    # pairs (more units than clusters of four)
+    ("attn_prefill", 200, 1500), ("attn_prefill_paged", 160, 2000), ("attn_prefill_bf16x3", 250, 3000),
+    # clusters of four at the thresholds: 257 and 384 keys (5 and 6 tiles of 64 over four CTAs),
+    # 1032 keys (9 tiles of 128), a one-row chunk
+    ("attn_prefill", 17, 240), ("attn_prefill", 128, 256), ("attn_prefill_bf16kv", 32, 1000),
+    ("attn_prefill_bf16x3", 1, 1100), ("attn_prefill_paged", 3, 5000),
 ])
 def test_every_unit_split(cp, path, C, P):
     run(cp, path, W.edge(C, P, seed=C + P))
@@ -65,7 +74,7 @@ def test_every_unit_split(cp, path, C, P):
 @pytest.mark.parametrize("variant", ["lastkey", "ramp"])
 def test_every_unit_split_max_in_last_tile(cp, variant):
     """A row's maximum in its final key tile: with the unit split, that tile
-    belongs to rank 1 and the merge must carry it."""
+    belongs to the last rank of the cluster and the merge must carry it."""
     run(cp, "attn_prefill", W.edge(64, 3000, variant=variant))
 
 
