@@ -100,8 +100,10 @@ extern "C" {
  * second grid of two-CTA clusters takes those units, each pair splitting one
  * along its keys and merging the two partials with the split-K rule (same
  * page, Flash-Decoding and the split-K merge); a chunk with at most half as
- * many units as SMs and a longest unit of 512 keys or more runs as that pair
- * grid alone. Neither needs device memory.
+ * many units as SMs and a longest unit of 256 keys or more runs as that split
+ * grid alone, over clusters of four CTAs (each a quarter of a unit's keys)
+ * when the device holds a cluster of four for every unit (chunks of up to 128
+ * rows on 152 SMs). Neither needs device memory.
  */
 int attn_prefill(const float *q, const float *kCache, const float *vCache, float *out,
                  int C, int P, cudaStream_t stream);
