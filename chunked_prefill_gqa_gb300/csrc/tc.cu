@@ -326,16 +326,21 @@ __device__ __forceinline__ bool split_epilogue(uint8_t* smem, uint32_t lane_tmem
   return true;
 }
 
-// The same for a unit split over a cluster of four CTAs: ranks 1-3 stage
-// their shares in their own Q regions, and once rank 0's last PV has
-// completed (its Q region and K ring are then idle) they copy them in bulk
-// into three consecutive slots there (rank r into slot r - 1); rank 0 merges
-// the four partials with the same rule, m = the largest maximum of a CTA with
-// tiles, each partial weighted by e^(m_s - m).
-static_assert(kSmemQ + 3 * kShareBytes <= kSmemV, "three shares fit in the Q region and the K ring");
-__device__ __forceinline__ bool split_epilogue4(uint8_t* smem, uint32_t lane_tmem, int n, bool has, const Bars& bars,
-                                                const Params& prm, volatile int* abort_flag, uint32_t rank, int row,
-                                                float m_ref, float l, float c, bool store, float* dst) {
+// The same for a unit split over a cluster of four or eight CTAs. With four,
+// ranks 1-3 stage their shares in their own Q regions and, once rank 0's last
+// PV has completed (its Q region and K ring are then idle), copy them in bulk
+// into consecutive slots there (rank r into slot r - 1). With eight, ranks 2-4
+// send to rank 0's slots 0-2 and ranks 5-7 to rank 1's; rank 1 merges its
+// three with its own partial and sends that, staged in its idle V ring, to
+// rank 0's slot 3. A receiver merges its partials with the same rule: m = the
+// largest maximum of a part with tiles, each part weighted by e^(m_s - m).
+static_assert(kSmemQ + 4 * kShareBytes <= kSmemBar, "four shares fit in the Q region and the K and V rings");
+template <int kSplit>
+__device__ __forceinline__ bool split_epilogue_many(uint8_t* smem, uint32_t lane_tmem, int n, bool has,
+                                                    const Bars& bars, const Params& prm, volatile int* abort_flag,
+                                                    uint32_t rank, int row, float m_ref, float l, float c,
+                                                    bool store, float* dst) {
+  static_assert(kSplit == 4 || kSplit == 8, "clusters of four or eight");
   float o[64];
   if (has) {
     const int pb = (n - 1) % kNumS;
@@ -355,48 +360,30 @@ __device__ __forceinline__ bool split_epilogue4(uint8_t* smem, uint32_t lane_tme
     for (int i = 0; i < 64; ++i) o[i] = 0.f;
   }
   uint8_t* share = smem + kSmemQ;
-  if (rank != 0) {
-    float* ml = reinterpret_cast<float*>(share + kShareO);  // [m of the rows][l of the rows]
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-      *reinterpret_cast<float4*>(share + share_offset(row, i)) =
-          make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
-    ml[row] = m_ref;
-    ml[kM + row] = l;
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (!wait_bar_cluster_warp(bars.slotfree, 0, prm, abort_flag)) return false;
-    if ((row & 31) == 0) {
-      const uint32_t bar = mapa_shared(smem_u32(bars.partner), 0);
-      const uint32_t slot = smem_u32(share) + (rank - 1) * kShareBytes;  // the same offset in rank 0
-      const uint32_t o_off = (uint32_t)row * 256u;
-      bulk_copy_to_cluster(mapa_shared(slot + o_off, 0), share + o_off, 32 * 256, bar);
-      bulk_copy_to_cluster(mapa_shared(slot + kShareO + row * 4, 0), ml + row, 32 * 4, bar);
-      bulk_copy_to_cluster(mapa_shared(slot + kShareO + (kM + row) * 4, 0), ml + kM + row, 32 * 4, bar);
-    }
-  } else {
-#pragma unroll
-    for (uint32_t r = 1; r < 4; ++r) mbar_arrive_remote(mapa_shared(smem_u32(bars.slotfree), r));
-    if (row == 0) mbar_arrive_expect_tx(bars.partner, 3 * kShareBytes);
+  // Receive `nslots` shares into slots 0.. of this CTA's Q region onward from
+  // `first` .. first + nslots - 1, and fold them into (o, m_ref, l): o and l
+  // end up relative to the merged maximum, returned in m_ref.
+  auto receive = [&](uint32_t first, int nslots) -> bool {
+    for (int r = 0; r < nslots; ++r) mbar_arrive_remote(mapa_shared(smem_u32(bars.slotfree), first + (uint32_t)r));
+    if (row == 0) mbar_arrive_expect_tx(bars.partner, (uint32_t)nslots * kShareBytes);
     if (!wait_bar_cluster_warp(bars.partner, 0, prm, abort_flag)) return false;
-    float ms[3], ls[3];
     float m = l > 0.f ? m_ref : -INFINITY;
-#pragma unroll
-    for (int r = 0; r < 3; ++r) {
+#pragma unroll 4
+    for (int r = 0; r < nslots; ++r) {
       const float* ml = reinterpret_cast<const float*>(share + r * kShareBytes + kShareO);
-      ms[r] = ml[row];
-      ls[r] = ml[kM + row];
-      if (ls[r] > 0.f) m = fmaxf(m, ms[r]);
+      if (ml[kM + row] > 0.f) m = fmaxf(m, ml[row]);
     }
     const float e0 = l > 0.f ? ex2((m_ref - m) * c) : 0.f;
     float den = e0 * l;
 #pragma unroll
     for (int i = 0; i < 64; ++i) o[i] *= e0;
-#pragma unroll
-    for (int r = 0; r < 3; ++r) {
+#pragma unroll 4
+    for (int r = 0; r < nslots; ++r) {
       const uint8_t* slot = share + r * kShareBytes;
-      const float er = ls[r] > 0.f ? ex2((ms[r] - m) * c) : 0.f;
-      den = fmaf(er, ls[r], den);
+      const float* ml = reinterpret_cast<const float*>(slot + kShareO);
+      const float lr = ml[kM + row];
+      const float er = lr > 0.f ? ex2((ml[row] - m) * c) : 0.f;
+      den = fmaf(er, lr, den);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const float4 x = *reinterpret_cast<const float4*>(slot + share_offset(row, i));
@@ -406,15 +393,54 @@ __device__ __forceinline__ bool split_epilogue4(uint8_t* smem, uint32_t lane_tme
         o[4 * i + 3] = fmaf(er, x.w, o[4 * i + 3]);
       }
     }
-    const float inv = 1.f / den;  // > 0: the unit sees at least key 0
+    m_ref = m;
+    l = den;
+    return true;
+  };
+  // Stage (o, m_ref, l) at `stage` in this CTA and, once the receiver says its
+  // slots are free, copy each warp's 32 rows in bulk into slot `slot` of CTA
+  // `to`, completing on that CTA's partner barrier.
+  auto send = [&](uint8_t* stage, uint32_t to, uint32_t slot) -> bool {
+    float* ml = reinterpret_cast<float*>(stage + kShareO);  // [m of the rows][l of the rows]
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      *reinterpret_cast<float4*>(stage + share_offset(row, i)) =
+          make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+    ml[row] = m_ref;
+    ml[kM + row] = l;
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (!wait_bar_cluster_warp(bars.slotfree, 0, prm, abort_flag)) return false;
+    if ((row & 31) == 0) {
+      const uint32_t bar = mapa_shared(smem_u32(bars.partner), to);
+      const uint32_t dst_slot = smem_u32(share) + slot * kShareBytes;  // the same offset in `to`
+      const uint32_t o_off = (uint32_t)row * 256u;
+      bulk_copy_to_cluster(mapa_shared(dst_slot + o_off, to), stage + o_off, 32 * 256, bar);
+      bulk_copy_to_cluster(mapa_shared(dst_slot + kShareO + row * 4, to), ml + row, 32 * 4, bar);
+      bulk_copy_to_cluster(mapa_shared(dst_slot + kShareO + (kM + row) * 4, to), ml + kM + row, 32 * 4, bar);
+    }
+    return true;
+  };
+  if (rank == 0) {
+    if (!receive(1, kSplit == 4 ? 3 : 4)) return false;
+    const float inv = 1.f / l;  // > 0: the unit sees at least key 0
     if (store) {
 #pragma unroll
       for (int i = 0; i < 16; ++i)
         *reinterpret_cast<float4*>(dst + 4 * i) =
             make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv, o[4 * i + 3] * inv);
     }
+    return true;
   }
-  return true;
+  if constexpr (kSplit == 8) {
+    if (rank == 1) {
+      if (!receive(5, 3)) return false;
+      return send(smem + kSmemV, 0, 3);
+    }
+    return rank < 5 ? send(share, 0, rank - 2) : send(share, 1, rank - 5);
+  } else {
+    return send(share, 0, rank - 1);
+  }
 }
 
 // Instantiations. kMain: whole units in snake order; it decides by prm.table
@@ -423,11 +449,12 @@ __device__ __forceinline__ bool split_epilogue4(uint8_t* smem, uint32_t lane_tme
 // kTail: launched after kMain as clusters of two CTAs; pair p splits unit
 // unit_base + p along its key tiles (rank 0 the first half, rank 1 the rest)
 // and merges the two online-softmax partials through distributed shared memory.
-// kTail4: the same with clusters of four CTAs, each a quarter of the unit's
-// tiles (small chunks, whose units are too few to fill the SMs as pairs).
-constexpr int kMain = 0, kPaged = 1, kTail = 2, kTail4 = 3;
+// kTail4, kTail8: the same with clusters of four or eight CTAs, each a
+// quarter or an eighth of the unit's tiles (small chunks, whose units are too
+// few to fill the SMs as pairs).
+constexpr int kMain = 0, kPaged = 1, kTail = 2, kTail4 = 3, kTail8 = 4;
 template <int kMode>
-__host__ __device__ constexpr bool is_tail() { return kMode == kTail || kMode == kTail4; }
+__host__ __device__ constexpr bool is_tail() { return kMode == kTail || kMode == kTail4 || kMode == kTail8; }
 
 // Unit u's tiles for this CTA: all of them, or the tail kernel's half.
 template <int kMode>
@@ -435,21 +462,23 @@ __device__ __forceinline__ void unit_range(const Unit& w, uint32_t rank, int* jb
   if constexpr (kMode == kTail) {
     *jb = rank == 0 ? 0 : w.ntiles / 2;
     *je = rank == 0 ? w.ntiles / 2 : w.ntiles;
-  } else if constexpr (kMode == kTail4) {
-    *jb = (int)rank * w.ntiles / 4;
-    *je = ((int)rank + 1) * w.ntiles / 4;
+  } else if constexpr (kMode == kTail4 || kMode == kTail8) {
+    constexpr int kS = kMode == kTail4 ? 4 : 8;
+    *jb = (int)rank * w.ntiles / kS;
+    *je = ((int)rank + 1) * w.ntiles / kS;
   } else {
     *jb = 0;
     *je = w.ntiles;
   }
 }
 
-// The CTA's k-th unit (kMain, kPaged: snake order; kTail, kTail4: one per
+// The CTA's k-th unit (kMain, kPaged: snake order; the tail modes: one per
 // cluster), or n_units when it has none.
 template <int kMode>
 __device__ __forceinline__ int work_unit(int k, int cta, int grid, const Params& prm) {
   if constexpr (kMode == kTail) return k == 0 ? prm.unit_base + (cta >> 1) : prm.n_units;
   else if constexpr (kMode == kTail4) return k == 0 ? prm.unit_base + (cta >> 2) : prm.n_units;
+  else if constexpr (kMode == kTail8) return k == 0 ? prm.unit_base + (cta >> 3) : prm.n_units;
   else return unit_index(k, cta, grid);
 }
 
@@ -897,10 +926,10 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
           goto softmax_done;
         tc_fence_before();
         continue;
-      } else if constexpr (kMode == kTail4) {
+      } else if constexpr (kMode == kTail4 || kMode == kTail8) {
         float* dst = p.out + ((size_t)pos * kHQ + w.g * kGroup + (row & 3)) * kD;
-        if (!split_epilogue4(smem, lane_tmem, n, has, bars, prm, abort_flag, rank, row, m_ref, l, c, pos < p.C,
-                             dst))
+        if (!split_epilogue_many<kMode == kTail4 ? 4 : 8>(smem, lane_tmem, n, has, bars, prm, abort_flag, rank, row,
+                                                          m_ref, l, c, pos < p.C, dst))
           goto softmax_done;
         tc_fence_before();
         continue;
@@ -998,7 +1027,8 @@ int encode_kv_map(const float* base, int rows, int box_rows, CUtensorMapSwizzle 
 struct TcDeviceState {
   bool ready = false;
   int num_sms = 0;
-  int quads = 0;  // clusters of four tail CTAs the device holds at once
+  int quads = 0;   // clusters of four tail CTAs the device holds at once
+  int octets = 0;  // clusters of eight
 };
 TcDeviceState g_tc_state[64];
 std::mutex g_tc_state_mu;
@@ -1007,7 +1037,7 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
                    const int* table = nullptr, int num_pages = 0) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ECUDA;
-  int num_sms = 0, quads = 0;
+  int num_sms = 0, quads = 0, octets = 0;
   {
     std::lock_guard<std::mutex> lock(g_tc_state_mu);
     TcDeviceState& st = g_tc_state[dev];
@@ -1021,29 +1051,38 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
           cudaFuncSetAttribute(tc_kernel<kTail>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc) !=
               cudaSuccess ||
           cudaFuncSetAttribute(tc_kernel<kTail4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc) !=
+              cudaSuccess ||
+          cudaFuncSetAttribute(tc_kernel<kTail8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc) !=
               cudaSuccess)
         return ATTN_ECUDA;
-      // How many clusters of four fit at once (0 when the query fails: no
-      // four-way split then).
-      cudaLaunchConfig_t qc = {};
-      qc.gridDim = dim3(4 * kHKV);
-      qc.blockDim = dim3(kThreads);
-      qc.dynamicSmemBytes = kSmemAlloc;
-      cudaLaunchAttribute qa[1];
-      qa[0].id = cudaLaunchAttributeClusterDimension;
-      qa[0].val.clusterDim.x = 4;
-      qa[0].val.clusterDim.y = 1;
-      qa[0].val.clusterDim.z = 1;
-      qc.attrs = qa;
-      qc.numAttrs = 1;
-      if (cudaOccupancyMaxActiveClusters(&st.quads, tc_kernel<kTail4>, &qc) != cudaSuccess) {
-        st.quads = 0;
-        (void)cudaGetLastError();
-      }
+      // How many clusters of four and of eight fit at once (0 when a query
+      // fails: no such split then).
+      auto clusters_of = [&](int size, void (*kernel)(CUtensorMap, CUtensorMap, Params)) {
+        cudaLaunchConfig_t qc = {};
+        qc.gridDim = dim3(size * kHKV);
+        qc.blockDim = dim3(kThreads);
+        qc.dynamicSmemBytes = kSmemAlloc;
+        cudaLaunchAttribute qa[1];
+        qa[0].id = cudaLaunchAttributeClusterDimension;
+        qa[0].val.clusterDim.x = size;
+        qa[0].val.clusterDim.y = 1;
+        qa[0].val.clusterDim.z = 1;
+        qc.attrs = qa;
+        qc.numAttrs = 1;
+        int nc = 0;
+        if (cudaOccupancyMaxActiveClusters(&nc, kernel, &qc) != cudaSuccess) {
+          (void)cudaGetLastError();
+          nc = 0;
+        }
+        return nc;
+      };
+      st.quads = clusters_of(4, tc_kernel<kTail4>);
+      st.octets = clusters_of(8, tc_kernel<kTail8>);
       st.ready = true;
     }
     num_sms = st.num_sms;
     quads = st.quads;
+    octets = st.octets;
   }
   alignas(64) CUtensorMap mk, mv;
   const int rows = table ? num_pages * kPage : p.P + p.C;
@@ -1067,13 +1106,16 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
   // With at most half as many units as SMs and the longest unit of 256 keys or
   // more, every unit is split over a pair (with the bulk-copy hand-off,
   // measured 1.1-1.3x faster for chunks against 500-2000 keys; from 2048 keys
-  // it already was; 1.1x against 250-500 keys), and over a cluster of four
-  // when the device holds one for every unit (chunks of 128 rows or less on
-  // 152 SMs: measured 1.4-1.9x faster than pairs against 2000-32768 keys,
-  // 1.1-1.2x against 600-1500). (The two grids can also split only the
-  // longest s units, the whole-unit grid starting s / 8 q-tiles down.) The
-  // pair grid is a programmatic dependent of the whole-unit grid: its pairs
-  // take SMs as soon as they are free.
+  // it already was; 1.1x against 250-500 keys), over a cluster of four when
+  // the device holds one for every unit (chunks of 128 rows or less on 152
+  // SMs: measured 1.4-1.9x faster than pairs against 2000-32768 keys, 1.1-1.2x
+  // against 600-1500), and over a cluster of eight when it holds one of those
+  // for every unit and the longest unit sees 1024 keys or more (15 on a GB300:
+  // chunks of 32 rows or less, 1.7x faster than fours against 32768 keys).
+  // (The two grids can also split only the longest s units, the whole-unit
+  // grid starting s / 8 q-tiles down.) The pair grid is a programmatic
+  // dependent of the whole-unit grid: its pairs take SMs as soon as they are
+  // free.
   Params main_prm = prm, tail_prm = prm;
   int main_grid = grid, tail_units = 0, split = 2;
   if (prm.n_units > grid) {
@@ -1092,7 +1134,10 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
     main_prm.n_units = 0;
     tail_prm.unit_base = 0;
     tail_units = prm.n_units;
-    if (prm.n_units <= quads) split = 4;
+    if (prm.n_units <= octets && unit_keys(p.P, p.C, (prm.n_qtiles - 1) * kBq, kBq) >= 1024)
+      split = 8;
+    else if (prm.n_units <= quads)
+      split = 4;
   }
   if (main_prm.n_units > 0) {
     if (table)
@@ -1116,8 +1161,8 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = main_prm.n_units > 0 ? 2 : 1;  // a dependent only of a whole-unit grid
-  if (cudaLaunchKernelEx(&cfg, split == 4 ? tc_kernel<kTail4> : tc_kernel<kTail>, mk, mv, tail_prm) != cudaSuccess)
-    return ATTN_ELAUNCH;
+  auto* tail = split == 8 ? tc_kernel<kTail8> : split == 4 ? tc_kernel<kTail4> : tc_kernel<kTail>;
+  if (cudaLaunchKernelEx(&cfg, tail, mk, mv, tail_prm) != cudaSuccess) return ATTN_ELAUNCH;
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ELAUNCH;
 }
 

@@ -190,12 +190,14 @@ __device__ __forceinline__ Unit decode_unit(int u, const Params& prm) {
 // kSplit == 1: whole units in snake order. kSplit == 2: launched after that
 // grid as clusters of two CTAs; pair p splits unit unit_base + p along its key
 // tiles (rank 0 the first half, rank 1 the rest) and merges the two
-// online-softmax partials through distributed shared memory. kSplit == 4: the
-// same with clusters of four CTAs, a quarter of the tiles each (small chunks).
+// online-softmax partials through distributed shared memory. kSplit == 4, 8:
+// the same with clusters of four or eight CTAs, a quarter or an eighth of the
+// tiles each (small chunks).
 template <int kSplit>
 __device__ __forceinline__ int work_unit(int k, int cta, int grid, const Params& prm) {
   if constexpr (kSplit == 2) return k == 0 ? prm.unit_base + (cta >> 1) : prm.n_units;
   else if constexpr (kSplit == 4) return k == 0 ? prm.unit_base + (cta >> 2) : prm.n_units;
+  else if constexpr (kSplit == 8) return k == 0 ? prm.unit_base + (cta >> 3) : prm.n_units;
   else return unit_index(k, cta, grid);
 }
 template <int kSplit>
@@ -203,9 +205,9 @@ __device__ __forceinline__ void unit_range(const Unit& w, uint32_t rank, int* jb
   if constexpr (kSplit == 2) {
     *jb = rank == 0 ? 0 : w.ntiles / 2;
     *je = rank == 0 ? w.ntiles / 2 : w.ntiles;
-  } else if constexpr (kSplit == 4) {
-    *jb = (int)rank * w.ntiles / 4;
-    *je = ((int)rank + 1) * w.ntiles / 4;
+  } else if constexpr (kSplit == 4 || kSplit == 8) {
+    *jb = (int)rank * w.ntiles / kSplit;
+    *je = ((int)rank + 1) * w.ntiles / kSplit;
   } else {
     *jb = 0;
     *je = w.ntiles;
@@ -694,13 +696,16 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
       lred[kh * 128 + row] = l;
       if (!pair_sync()) goto softmax_done;
       l += lred[(kh ^ 1) * 128 + row];
-      if constexpr (kSplit == 4) {
-        // A unit split over a cluster of four, as over a pair below: ranks 1-3
-        // stage their shares in their own K rings and, once rank 0's last PV
-        // has completed (its K and V rings are then idle), copy them in bulk
-        // into three consecutive slots there (rank r into slot r - 1); rank 0
-        // merges the four partials, m = the largest maximum of a CTA with
-        // tiles, each weighted by e^(m_s - m).
+      if constexpr (kSplit == 4 || kSplit == 8) {
+        // A unit split over a cluster of four or eight, as over a pair below.
+        // Senders stage their shares in their own K rings; a receiver, once
+        // its last PV has completed (its K and V rings are then idle), takes
+        // up to three shares in consecutive slots there and folds them into
+        // its own partial, m = the largest maximum of a part with tiles, each
+        // part weighted by e^(m_s - m). Four: ranks 1-3 send to rank 0. Eight:
+        // ranks 2-4 send to rank 0 and ranks 5-7 to rank 1; rank 1 then sends
+        // its merged partial to rank 0's slot 0, once rank 0 has folded in
+        // its first three.
         static_assert(kSmemK + 3 * kShareBytes <= kSmemBar, "three shares fit in the K and V rings");
         float o[32];
         if (has) {
@@ -724,7 +729,48 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
         auto share_offset = [&](int i) -> uint32_t {  // this thread's chunk i (4 floats) of its row half
           return (uint32_t)kh * 16384u + (uint32_t)row * 128u + (uint32_t)((i ^ (row & 7)) * 16);
         };
-        if (rank != 0) {
+        auto receive = [&](uint32_t first, int nslots, uint32_t phase) -> bool {
+          for (int r = 0; r < nslots; ++r)
+            mbar_arrive_remote(mapa_shared(smem_u32(bars.slotfree), first + (uint32_t)r));
+          if (row == 0 && kh == 0) mbar_arrive_expect_tx(bars.partner, (uint32_t)nslots * kShareBytes);
+          if (!wait_bar_cluster_warp(bars.partner, phase, prm, abort_flag)) return false;
+          float m = l > 0.f ? m_ref : -INFINITY;
+#pragma unroll 3
+          for (int r = 0; r < nslots; ++r) {
+            const float* ml = reinterpret_cast<const float*>(share + r * kShareBytes + kShareO);
+            if (ml[128 + row] > 0.f) m = fmaxf(m, ml[row]);
+          }
+          const float e0 = l > 0.f ? ex2((m_ref - m) * c) : 0.f;
+          float den = e0 * l;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= e0;
+#pragma unroll 3
+          for (int r = 0; r < nslots; ++r) {
+            const uint8_t* slot = share + r * kShareBytes;
+            const float* ml = reinterpret_cast<const float*>(slot + kShareO);
+            const float lr = ml[128 + row];
+            const float er = lr > 0.f ? ex2((ml[row] - m) * c) : 0.f;
+            den = fmaf(er, lr, den);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 x = *reinterpret_cast<const float4*>(slot + share_offset(i));
+              o[4 * i] = fmaf(er, x.x, o[4 * i]);
+              o[4 * i + 1] = fmaf(er, x.y, o[4 * i + 1]);
+              o[4 * i + 2] = fmaf(er, x.z, o[4 * i + 2]);
+              o[4 * i + 3] = fmaf(er, x.w, o[4 * i + 3]);
+            }
+          }
+          m_ref = m;
+          l = den;
+          return true;
+        };
+        // Stage (o, m_ref, l) in slot 0 of this CTA (each thread its own row
+        // half, so a receiver overwrites only what it has read) and copy it
+        // in bulk into slot `slot` of CTA `to` once that CTA's slots are free.
+        auto send = [&](uint32_t to, uint32_t slot) -> bool {
+          // After a receive, both warps of the row set must have read slot 0's
+          // maxima and sums before the kh = 0 warp overwrites them.
+          if (kSplit == 8 && rank == 1 && !pair_sync()) return false;
           float* ml = reinterpret_cast<float*>(share + kShareO);
 #pragma unroll
           for (int i = 0; i < 8; ++i)
@@ -736,58 +782,39 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
           }
           fence_proxy_async_smem();
           __syncwarp();
-          if (!wait_bar_cluster_warp(bars.slotfree, 0, prm, abort_flag)) goto softmax_done;
+          if (!wait_bar_cluster_warp(bars.slotfree, 0, prm, abort_flag)) return false;
           if ((row & 31) == 0) {
-            const uint32_t bar = mapa_shared(smem_u32(bars.partner), 0);
-            const uint32_t slot = smem_u32(share) + (rank - 1) * kShareBytes;  // the same offset in rank 0
+            const uint32_t bar = mapa_shared(smem_u32(bars.partner), to);
+            const uint32_t dst_slot = smem_u32(share) + slot * kShareBytes;  // the same offset in `to`
             const uint32_t part = (uint32_t)kh * 16384u + (uint32_t)row * 128u;
-            bulk_copy_to_cluster(mapa_shared(slot + part, 0), share + part, 32 * 128, bar);
+            bulk_copy_to_cluster(mapa_shared(dst_slot + part, to), share + part, 32 * 128, bar);
             if (kh == 0) {
-              bulk_copy_to_cluster(mapa_shared(slot + kShareO + row * 4, 0), ml + row, 32 * 4, bar);
-              bulk_copy_to_cluster(mapa_shared(slot + kShareO + (128 + row) * 4, 0), ml + 128 + row, 32 * 4, bar);
+              bulk_copy_to_cluster(mapa_shared(dst_slot + kShareO + row * 4, to), ml + row, 32 * 4, bar);
+              bulk_copy_to_cluster(mapa_shared(dst_slot + kShareO + (128 + row) * 4, to), ml + 128 + row, 32 * 4,
+                                   bar);
             }
           }
-        } else {
-#pragma unroll
-          for (uint32_t r = 1; r < 4; ++r) mbar_arrive_remote(mapa_shared(smem_u32(bars.slotfree), r));
-          if (row == 0 && kh == 0) mbar_arrive_expect_tx(bars.partner, 3 * kShareBytes);
-          if (!wait_bar_cluster_warp(bars.partner, 0, prm, abort_flag)) goto softmax_done;
-          float ms[3], ls[3];
-          float m = l > 0.f ? m_ref : -INFINITY;
-#pragma unroll
-          for (int r = 0; r < 3; ++r) {
-            const float* ml = reinterpret_cast<const float*>(share + r * kShareBytes + kShareO);
-            ms[r] = ml[row];
-            ls[r] = ml[128 + row];
-            if (ls[r] > 0.f) m = fmaxf(m, ms[r]);
-          }
-          const float e0 = l > 0.f ? ex2((m_ref - m) * c) : 0.f;
-          float den = e0 * l;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= e0;
-#pragma unroll
-          for (int r = 0; r < 3; ++r) {
-            const uint8_t* slot = share + r * kShareBytes;
-            const float er = ls[r] > 0.f ? ex2((ms[r] - m) * c) : 0.f;
-            den = fmaf(er, ls[r], den);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float4 x = *reinterpret_cast<const float4*>(slot + share_offset(i));
-              o[4 * i] = fmaf(er, x.x, o[4 * i]);
-              o[4 * i + 1] = fmaf(er, x.y, o[4 * i + 1]);
-              o[4 * i + 2] = fmaf(er, x.z, o[4 * i + 2]);
-              o[4 * i + 3] = fmaf(er, x.w, o[4 * i + 3]);
-            }
-          }
-          const float inv = 1.f / den;  // > 0: the unit sees at least key 0
-          if (pos < p.C) {
+          return true;
+        };
+        bool ok;
+        if (rank == 0) {
+          ok = kSplit == 4 ? receive(1, 3, 0) : (receive(2, 3, 0) && receive(1, 1, 1));
+          if (ok && pos < p.C) {
+            const float inv = 1.f / l;  // > 0: the unit sees at least key 0
             float* dst = p.out + ((size_t)pos * kHQ + w.g * kGroup + (row & 3)) * kD + kh * 32;
 #pragma unroll
             for (int i = 0; i < 8; ++i)
               *reinterpret_cast<float4*>(dst + 4 * i) =
                   make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv, o[4 * i + 3] * inv);
           }
+        } else if (kSplit == 4) {
+          ok = send(0, rank - 1);
+        } else if (rank == 1) {
+          ok = receive(5, 3, 0) && send(0, 0);
+        } else {
+          ok = rank < 5 ? send(0, rank - 2) : send(1, rank - 5);
         }
+        if (!ok) goto softmax_done;
         tc_fence_before();
         continue;
       }
@@ -961,7 +988,8 @@ int encode_kv_tile_map(const void* base, int rows, bool f32, CUtensorMap* map) {
 struct DevState {
   bool ready[2] = {false, false};  // per cache type, its instantiations set up
   int num_sms = 0;
-  int quads[2] = {0, 0};  // per cache type: clusters of four tail CTAs the device holds at once
+  int quads[2] = {0, 0};   // per cache type: clusters of four tail CTAs the device holds at once
+  int octets[2] = {0, 0};  // and of eight
 };
 DevState g_state[64];
 std::mutex g_state_mu;
@@ -970,7 +998,7 @@ template <bool kF32>
 int launch_impl(const Problem& p, cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ECUDA;
-  int num_sms = 0, quads = 0;
+  int num_sms = 0, quads = 0, octets = 0;
   {
     std::lock_guard<std::mutex> lock(g_state_mu);
     DevState& st = g_state[dev];
@@ -982,29 +1010,38 @@ int launch_impl(const Problem& p, cudaStream_t stream) {
           cudaFuncSetAttribute(tc_bf16_kernel<kF32, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)Layout<kF32>::kSmemAlloc) != cudaSuccess ||
           cudaFuncSetAttribute(tc_bf16_kernel<kF32, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)Layout<kF32>::kSmemAlloc) != cudaSuccess ||
+          cudaFuncSetAttribute(tc_bf16_kernel<kF32, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)Layout<kF32>::kSmemAlloc) != cudaSuccess)
         return ATTN_ECUDA;
-      // How many clusters of four fit at once (0 when the query fails: no
-      // four-way split then).
-      cudaLaunchConfig_t qc = {};
-      qc.gridDim = dim3(4 * kHKV);
-      qc.blockDim = dim3(threads_of<kF32>());
-      qc.dynamicSmemBytes = Layout<kF32>::kSmemAlloc;
-      cudaLaunchAttribute qa[1];
-      qa[0].id = cudaLaunchAttributeClusterDimension;
-      qa[0].val.clusterDim.x = 4;
-      qa[0].val.clusterDim.y = 1;
-      qa[0].val.clusterDim.z = 1;
-      qc.attrs = qa;
-      qc.numAttrs = 1;
-      if (cudaOccupancyMaxActiveClusters(&st.quads[kF32], tc_bf16_kernel<kF32, 4>, &qc) != cudaSuccess) {
-        st.quads[kF32] = 0;
-        (void)cudaGetLastError();
-      }
+      // How many clusters of four and of eight fit at once (0 when a query
+      // fails: no such split then).
+      auto clusters_of = [&](int size, void (*kernel)(CUtensorMap, CUtensorMap, Params)) {
+        cudaLaunchConfig_t qc = {};
+        qc.gridDim = dim3(size * kHKV);
+        qc.blockDim = dim3(threads_of<kF32>());
+        qc.dynamicSmemBytes = Layout<kF32>::kSmemAlloc;
+        cudaLaunchAttribute qa[1];
+        qa[0].id = cudaLaunchAttributeClusterDimension;
+        qa[0].val.clusterDim.x = size;
+        qa[0].val.clusterDim.y = 1;
+        qa[0].val.clusterDim.z = 1;
+        qc.attrs = qa;
+        qc.numAttrs = 1;
+        int nc = 0;
+        if (cudaOccupancyMaxActiveClusters(&nc, kernel, &qc) != cudaSuccess) {
+          (void)cudaGetLastError();
+          nc = 0;
+        }
+        return nc;
+      };
+      st.quads[kF32] = clusters_of(4, tc_bf16_kernel<kF32, 4>);
+      st.octets[kF32] = clusters_of(8, tc_bf16_kernel<kF32, 8>);
       st.ready[kF32] = true;
     }
     num_sms = st.num_sms;
     quads = st.quads[kF32];
+    octets = st.octets[kF32];
   }
   alignas(64) CUtensorMap mk, mv;
   int rc = encode_kv_tile_map(p.k, p.P + p.C, kF32, &mk);
@@ -1029,7 +1066,9 @@ int launch_impl(const Problem& p, cudaStream_t stream) {
   // 8192 keys or more). Every unit is split over a cluster of four instead
   // when the device holds one for every unit (chunks of 128 rows or less on
   // 152 SMs: measured 1.3-1.8x faster than pairs against 4096-32768 keys,
-  // 1.1x against 1200-2500).
+  // 1.1x against 1200-2500), and over eight when it holds a cluster of eight
+  // for every unit and the longest unit sees 2048 keys or more (chunks of 32
+  // rows or less: 1.6-1.7x faster than fours against 32768 keys).
   Params main_prm = prm, tail_prm = prm;
   int main_grid = grid, tail_units = 0, split = 2;
   if (prm.n_units > grid) {
@@ -1046,7 +1085,10 @@ int launch_impl(const Problem& p, cudaStream_t stream) {
     main_prm.n_units = 0;
     tail_prm.unit_base = 0;
     tail_units = prm.n_units;
-    if (prm.n_units <= quads) split = 4;
+    if (prm.n_units <= octets && unit_keys(p.P, p.C, (prm.n_qtiles - 1) * kBq, kBq) >= 2048)
+      split = 8;
+    else if (prm.n_units <= quads)
+      split = 4;
   }
   if (main_prm.n_units > 0) {
     tc_bf16_kernel<kF32, 1><<<main_grid, threads_of<kF32>(), Layout<kF32>::kSmemAlloc, stream>>>(mk, mv,
@@ -1068,9 +1110,8 @@ int launch_impl(const Problem& p, cudaStream_t stream) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = main_prm.n_units > 0 ? 2 : 1;  // a dependent only of a whole-unit grid
-  if (cudaLaunchKernelEx(&cfg, split == 4 ? tc_bf16_kernel<kF32, 4> : tc_bf16_kernel<kF32, 2>, mk, mv, tail_prm) !=
-      cudaSuccess)
-    return ATTN_ELAUNCH;
+  auto* tail = split == 8 ? tc_bf16_kernel<kF32, 8> : split == 4 ? tc_bf16_kernel<kF32, 4> : tc_bf16_kernel<kF32, 2>;
+  if (cudaLaunchKernelEx(&cfg, tail, mk, mv, tail_prm) != cudaSuccess) return ATTN_ELAUNCH;
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ELAUNCH;
 }
 

@@ -1,8 +1,10 @@
 """The split-unit grids against the oracle, every element checked on a poisoned,
 guarded output: chunks small enough that every unit is split (the longest unit
-of 256 keys or more, 1024 for the bf16 kernels) over a cluster of four CTAs
-(at most as many units as the device holds such clusters at once: chunks of
-up to 128 rows on 152 SMs) or over a CTA pair (up to 304 rows), and chunks
+of 256 keys or more, 1024 for the bf16 kernels) over a cluster of eight CTAs
+(chunks of up to 32 rows against 1024 keys or more, 2048 for the bf16
+kernels), of four (at most as many units as the device holds such clusters at
+once: chunks of up to 128 rows on 152 SMs) or over a CTA pair (up to 304
+rows), and chunks
 whose last round of units goes to the pair grid (the tail), including a ragged
 last query tile and a paged cache."""
 import numpy as np
@@ -52,7 +54,7 @@ def run(cp, path, inp):
 
 
 # Every unit split (at most 76 units, i.e. C <= 304 rows, on 152 SMs): over
-# clusters of four up to 128 rows, over pairs beyond.
+# clusters of eight up to 32 rows, of four up to 128 rows, over pairs beyond.
 @pytest.mark.parametrize("path,C,P", [
     ("attn_prefill", 1, 2048), ("attn_prefill", 33, 2048), ("attn_prefill", 100, 3000),
     ("attn_prefill", 288, 2500), ("attn_prefill_paged", 100, 3000), ("attn_prefill_paged", 17, 4100),
@@ -66,16 +68,20 @@ def run(cp, path, inp):
     # 1032 keys (9 tiles of 128), a one-row chunk
     ("attn_prefill", 17, 240), ("attn_prefill", 128, 256), ("attn_prefill_bf16kv", 32, 1000),
     ("attn_prefill_bf16x3", 1, 1100), ("attn_prefill_paged", 3, 5000),
+    # clusters of eight: 1025 keys (17 tiles of 64 over eight CTAs), 2048 keys (16 tiles of 128)
+    ("attn_prefill", 32, 3000), ("attn_prefill", 1, 1024), ("attn_prefill_paged", 9, 2500),
+    ("attn_prefill_bf16kv", 17, 3000), ("attn_prefill_bf16kv", 1, 2047), ("attn_prefill_bf16x3", 32, 2100),
 ])
 def test_every_unit_split(cp, path, C, P):
     run(cp, path, W.edge(C, P, seed=C + P))
 
 
 @pytest.mark.parametrize("variant", ["lastkey", "ramp"])
-def test_every_unit_split_max_in_last_tile(cp, variant):
+@pytest.mark.parametrize("path,C", [("attn_prefill", 64), ("attn_prefill", 32), ("attn_prefill_bf16kv", 32)])
+def test_every_unit_split_max_in_last_tile(cp, variant, path, C):
     """A row's maximum in its final key tile: with the unit split, that tile
     belongs to the last rank of the cluster and the merge must carry it."""
-    run(cp, "attn_prefill", W.edge(64, 3000, variant=variant))
+    run(cp, path, W.edge(C, 3000, variant=variant))
 
 
 # The tail: 512 units of which 56 go to the pair grid; C = 2040 leaves the last
