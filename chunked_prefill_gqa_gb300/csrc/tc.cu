@@ -326,10 +326,10 @@ __device__ __forceinline__ bool split_epilogue(uint8_t* smem, uint32_t lane_tmem
   return true;
 }
 
-// The same for a unit split over a cluster of four or eight CTAs. With four,
-// ranks 1-3 stage their shares in their own Q regions and, once rank 0's last
-// PV has completed (its Q region and K ring are then idle), copy them in bulk
-// into consecutive slots there (rank r into slot r - 1). With eight, ranks 2-4
+// The same for a unit split over a cluster of three, four or eight CTAs. With
+// three or four, ranks 1.. stage their shares in their own Q regions and, once
+// rank 0's last PV has completed (its Q region and K ring are then idle), copy
+// them in bulk into consecutive slots there (rank r into slot r - 1). With eight, ranks 2-4
 // send to rank 0's slots 0-2 and ranks 5-7 to rank 1's; rank 1 merges its
 // three with its own partial and sends that, staged in its idle V ring, to
 // rank 0's slot 3. A receiver merges its partials with the same rule: m = the
@@ -340,7 +340,7 @@ __device__ __forceinline__ bool split_epilogue_many(uint8_t* smem, uint32_t lane
                                                     const Bars& bars, const Params& prm, volatile int* abort_flag,
                                                     uint32_t rank, int row, float m_ref, float l, float c,
                                                     bool store, float* dst) {
-  static_assert(kSplit == 4 || kSplit == 8, "clusters of four or eight");
+  static_assert(kSplit == 3 || kSplit == 4 || kSplit == 8, "clusters of three, four or eight");
   float o[64];
   if (has) {
     const int pb = (n - 1) % kNumS;
@@ -422,7 +422,7 @@ __device__ __forceinline__ bool split_epilogue_many(uint8_t* smem, uint32_t lane
     return true;
   };
   if (rank == 0) {
-    if (!receive(1, kSplit == 4 ? 3 : 4)) return false;
+    if (!receive(1, kSplit == 8 ? 4 : kSplit - 1)) return false;
     const float inv = 1.f / l;  // > 0: the unit sees at least key 0
     if (store) {
 #pragma unroll
@@ -449,12 +449,16 @@ __device__ __forceinline__ bool split_epilogue_many(uint8_t* smem, uint32_t lane
 // kTail: launched after kMain as clusters of two CTAs; pair p splits unit
 // unit_base + p along its key tiles (rank 0 the first half, rank 1 the rest)
 // and merges the two online-softmax partials through distributed shared memory.
-// kTail4, kTail8: the same with clusters of four or eight CTAs, each a
-// quarter or an eighth of the unit's tiles (small chunks, whose units are too
+// kTail3, kTail4, kTail8: the same with clusters of three, four or eight
+// CTAs, each that share of the unit's tiles (small chunks, whose units are too
 // few to fill the SMs as pairs).
-constexpr int kMain = 0, kPaged = 1, kTail = 2, kTail4 = 3, kTail8 = 4;
+constexpr int kMain = 0, kPaged = 1, kTail = 2, kTail4 = 3, kTail8 = 4, kTail3 = 5;
 template <int kMode>
-__host__ __device__ constexpr bool is_tail() { return kMode == kTail || kMode == kTail4 || kMode == kTail8; }
+__host__ __device__ constexpr int split_of() {
+  return kMode == kTail ? 2 : kMode == kTail3 ? 3 : kMode == kTail4 ? 4 : kMode == kTail8 ? 8 : 1;
+}
+template <int kMode>
+__host__ __device__ constexpr bool is_tail() { return split_of<kMode>() > 1; }
 
 // Unit u's tiles for this CTA: all of them, or the tail kernel's half.
 template <int kMode>
@@ -462,8 +466,8 @@ __device__ __forceinline__ void unit_range(const Unit& w, uint32_t rank, int* jb
   if constexpr (kMode == kTail) {
     *jb = rank == 0 ? 0 : w.ntiles / 2;
     *je = rank == 0 ? w.ntiles / 2 : w.ntiles;
-  } else if constexpr (kMode == kTail4 || kMode == kTail8) {
-    constexpr int kS = kMode == kTail4 ? 4 : 8;
+  } else if constexpr (is_tail<kMode>()) {
+    constexpr int kS = split_of<kMode>();
     *jb = (int)rank * w.ntiles / kS;
     *je = ((int)rank + 1) * w.ntiles / kS;
   } else {
@@ -479,6 +483,7 @@ __device__ __forceinline__ int work_unit(int k, int cta, int grid, const Params&
   if constexpr (kMode == kTail) return k == 0 ? prm.unit_base + (cta >> 1) : prm.n_units;
   else if constexpr (kMode == kTail4) return k == 0 ? prm.unit_base + (cta >> 2) : prm.n_units;
   else if constexpr (kMode == kTail8) return k == 0 ? prm.unit_base + (cta >> 3) : prm.n_units;
+  else if constexpr (kMode == kTail3) return k == 0 ? prm.unit_base + cta / 3 : prm.n_units;
   else return unit_index(k, cta, grid);
 }
 
@@ -926,9 +931,9 @@ tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUten
           goto softmax_done;
         tc_fence_before();
         continue;
-      } else if constexpr (kMode == kTail4 || kMode == kTail8) {
+      } else if constexpr (is_tail<kMode>()) {
         float* dst = p.out + ((size_t)pos * kHQ + w.g * kGroup + (row & 3)) * kD;
-        if (!split_epilogue_many<kMode == kTail4 ? 4 : 8>(smem, lane_tmem, n, has, bars, prm, abort_flag, rank, row,
+        if (!split_epilogue_many<split_of<kMode>()>(smem, lane_tmem, n, has, bars, prm, abort_flag, rank, row,
                                                           m_ref, l, c, pos < p.C, dst))
           goto softmax_done;
         tc_fence_before();
@@ -1029,6 +1034,7 @@ struct TcDeviceState {
   int num_sms = 0;
   int quads = 0;   // clusters of four tail CTAs the device holds at once
   int octets = 0;  // clusters of eight
+  int trios = 0;   // clusters of three
 };
 TcDeviceState g_tc_state[64];
 std::mutex g_tc_state_mu;
@@ -1037,7 +1043,7 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
                    const int* table = nullptr, int num_pages = 0) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ECUDA;
-  int num_sms = 0, quads = 0, octets = 0;
+  int num_sms = 0, quads = 0, octets = 0, trios = 0;
   {
     std::lock_guard<std::mutex> lock(g_tc_state_mu);
     TcDeviceState& st = g_tc_state[dev];
@@ -1053,10 +1059,12 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
           cudaFuncSetAttribute(tc_kernel<kTail4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc) !=
               cudaSuccess ||
           cudaFuncSetAttribute(tc_kernel<kTail8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc) !=
+              cudaSuccess ||
+          cudaFuncSetAttribute(tc_kernel<kTail3>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc) !=
               cudaSuccess)
         return ATTN_ECUDA;
-      // How many clusters of four and of eight fit at once (0 when a query
-      // fails: no such split then).
+      // How many clusters of three, four and eight fit at once (0 when a
+      // query fails: no such split then).
       auto clusters_of = [&](int size, void (*kernel)(CUtensorMap, CUtensorMap, Params)) {
         cudaLaunchConfig_t qc = {};
         qc.gridDim = dim3(size * kHKV);
@@ -1078,11 +1086,13 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
       };
       st.quads = clusters_of(4, tc_kernel<kTail4>);
       st.octets = clusters_of(8, tc_kernel<kTail8>);
+      st.trios = clusters_of(3, tc_kernel<kTail3>);
       st.ready = true;
     }
     num_sms = st.num_sms;
     quads = st.quads;
     octets = st.octets;
+    trios = st.trios;
   }
   alignas(64) CUtensorMap mk, mv;
   const int rows = table ? num_pages * kPage : p.P + p.C;
@@ -1111,7 +1121,10 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
   // SMs: measured 1.4-1.9x faster than pairs against 2000-32768 keys, 1.1-1.2x
   // against 600-1500), and over a cluster of eight when it holds one of those
   // for every unit and the longest unit sees 1024 keys or more (15 on a GB300:
-  // chunks of 32 rows or less, 1.7x faster than fours against 32768 keys).
+  // chunks of 32 rows or less, 1.7x faster than fours against 32768 keys),
+  // and over a cluster of three when it holds one of those for every unit
+  // (46: chunks of 129-184 rows, 1.2-1.4x faster than pairs against 3000-32768
+  // keys).
   // (The two grids can also split only the longest s units, the whole-unit
   // grid starting s / 8 q-tiles down.) The pair grid is a programmatic
   // dependent of the whole-unit grid: its pairs take SMs as soon as they are
@@ -1138,6 +1151,8 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
       split = 8;
     else if (prm.n_units <= quads)
       split = 4;
+    else if (prm.n_units <= trios)
+      split = 3;
   }
   if (main_prm.n_units > 0) {
     if (table)
@@ -1161,7 +1176,10 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = main_prm.n_units > 0 ? 2 : 1;  // a dependent only of a whole-unit grid
-  auto* tail = split == 8 ? tc_kernel<kTail8> : split == 4 ? tc_kernel<kTail4> : tc_kernel<kTail>;
+  auto* tail = split == 8   ? tc_kernel<kTail8>
+               : split == 4 ? tc_kernel<kTail4>
+               : split == 3 ? tc_kernel<kTail3>
+                            : tc_kernel<kTail>;
   if (cudaLaunchKernelEx(&cfg, tail, mk, mv, tail_prm) != cudaSuccess) return ATTN_ELAUNCH;
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ELAUNCH;
 }

@@ -190,14 +190,15 @@ __device__ __forceinline__ Unit decode_unit(int u, const Params& prm) {
 // kSplit == 1: whole units in snake order. kSplit == 2: launched after that
 // grid as clusters of two CTAs; pair p splits unit unit_base + p along its key
 // tiles (rank 0 the first half, rank 1 the rest) and merges the two
-// online-softmax partials through distributed shared memory. kSplit == 4, 8:
-// the same with clusters of four or eight CTAs, a quarter or an eighth of the
+// online-softmax partials through distributed shared memory. kSplit == 3, 4,
+// 8: the same with clusters of three, four or eight CTAs, that share of the
 // tiles each (small chunks).
 template <int kSplit>
 __device__ __forceinline__ int work_unit(int k, int cta, int grid, const Params& prm) {
   if constexpr (kSplit == 2) return k == 0 ? prm.unit_base + (cta >> 1) : prm.n_units;
   else if constexpr (kSplit == 4) return k == 0 ? prm.unit_base + (cta >> 2) : prm.n_units;
   else if constexpr (kSplit == 8) return k == 0 ? prm.unit_base + (cta >> 3) : prm.n_units;
+  else if constexpr (kSplit == 3) return k == 0 ? prm.unit_base + cta / 3 : prm.n_units;
   else return unit_index(k, cta, grid);
 }
 template <int kSplit>
@@ -205,7 +206,7 @@ __device__ __forceinline__ void unit_range(const Unit& w, uint32_t rank, int* jb
   if constexpr (kSplit == 2) {
     *jb = rank == 0 ? 0 : w.ntiles / 2;
     *je = rank == 0 ? w.ntiles / 2 : w.ntiles;
-  } else if constexpr (kSplit == 4 || kSplit == 8) {
+  } else if constexpr (kSplit == 3 || kSplit == 4 || kSplit == 8) {
     *jb = (int)rank * w.ntiles / kSplit;
     *je = ((int)rank + 1) * w.ntiles / kSplit;
   } else {
@@ -696,8 +697,9 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
       lred[kh * 128 + row] = l;
       if (!pair_sync()) goto softmax_done;
       l += lred[(kh ^ 1) * 128 + row];
-      if constexpr (kSplit == 4 || kSplit == 8) {
-        // A unit split over a cluster of four or eight, as over a pair below.
+      if constexpr (kSplit == 3 || kSplit == 4 || kSplit == 8) {
+        // A unit split over a cluster of three, four or eight, as over a pair
+        // below.
         // Senders stage their shares in their own K rings; a receiver, once
         // its last PV has completed (its K and V rings are then idle), takes
         // up to three shares in consecutive slots there and folds them into
@@ -705,7 +707,7 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
         // part weighted by e^(m_s - m). Four: ranks 1-3 send to rank 0. Eight:
         // ranks 2-4 send to rank 0 and ranks 5-7 to rank 1; rank 1 then sends
         // its merged partial to rank 0's slot 0, once rank 0 has folded in
-        // its first three.
+        // its first three. Three: ranks 1-2 send to rank 0.
         static_assert(kSmemK + 3 * kShareBytes <= kSmemBar, "three shares fit in the K and V rings");
         float o[32];
         if (has) {
@@ -798,7 +800,7 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
         };
         bool ok;
         if (rank == 0) {
-          ok = kSplit == 4 ? receive(1, 3, 0) : (receive(2, 3, 0) && receive(1, 1, 1));
+          ok = kSplit == 8 ? (receive(2, 3, 0) && receive(1, 1, 1)) : receive(1, kSplit - 1, 0);
           if (ok && pos < p.C) {
             const float inv = 1.f / l;  // > 0: the unit sees at least key 0
             float* dst = p.out + ((size_t)pos * kHQ + w.g * kGroup + (row & 3)) * kD + kh * 32;
@@ -807,7 +809,7 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
               *reinterpret_cast<float4*>(dst + 4 * i) =
                   make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv, o[4 * i + 3] * inv);
           }
-        } else if (kSplit == 4) {
+        } else if (kSplit != 8) {
           ok = send(0, rank - 1);
         } else if (rank == 1) {
           ok = receive(5, 3, 0) && send(0, 0);
@@ -990,6 +992,7 @@ struct DevState {
   int num_sms = 0;
   int quads[2] = {0, 0};   // per cache type: clusters of four tail CTAs the device holds at once
   int octets[2] = {0, 0};  // and of eight
+  int trios[2] = {0, 0};   // and of three
 };
 DevState g_state[64];
 std::mutex g_state_mu;
@@ -998,7 +1001,7 @@ template <bool kF32>
 int launch_impl(const Problem& p, cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ECUDA;
-  int num_sms = 0, quads = 0, octets = 0;
+  int num_sms = 0, quads = 0, octets = 0, trios = 0;
   {
     std::lock_guard<std::mutex> lock(g_state_mu);
     DevState& st = g_state[dev];
@@ -1012,10 +1015,12 @@ int launch_impl(const Problem& p, cudaStream_t stream) {
           cudaFuncSetAttribute(tc_bf16_kernel<kF32, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)Layout<kF32>::kSmemAlloc) != cudaSuccess ||
           cudaFuncSetAttribute(tc_bf16_kernel<kF32, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)Layout<kF32>::kSmemAlloc) != cudaSuccess ||
+          cudaFuncSetAttribute(tc_bf16_kernel<kF32, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)Layout<kF32>::kSmemAlloc) != cudaSuccess)
         return ATTN_ECUDA;
-      // How many clusters of four and of eight fit at once (0 when a query
-      // fails: no such split then).
+      // How many clusters of three, four and eight fit at once (0 when a
+      // query fails: no such split then).
       auto clusters_of = [&](int size, void (*kernel)(CUtensorMap, CUtensorMap, Params)) {
         cudaLaunchConfig_t qc = {};
         qc.gridDim = dim3(size * kHKV);
@@ -1037,11 +1042,13 @@ int launch_impl(const Problem& p, cudaStream_t stream) {
       };
       st.quads[kF32] = clusters_of(4, tc_bf16_kernel<kF32, 4>);
       st.octets[kF32] = clusters_of(8, tc_bf16_kernel<kF32, 8>);
+      st.trios[kF32] = clusters_of(3, tc_bf16_kernel<kF32, 3>);
       st.ready[kF32] = true;
     }
     num_sms = st.num_sms;
     quads = st.quads[kF32];
     octets = st.octets[kF32];
+    trios = st.trios[kF32];
   }
   alignas(64) CUtensorMap mk, mv;
   int rc = encode_kv_tile_map(p.k, p.P + p.C, kF32, &mk);
@@ -1068,7 +1075,9 @@ int launch_impl(const Problem& p, cudaStream_t stream) {
   // 152 SMs: measured 1.3-1.8x faster than pairs against 4096-32768 keys,
   // 1.1x against 1200-2500), and over eight when it holds a cluster of eight
   // for every unit and the longest unit sees 2048 keys or more (chunks of 32
-  // rows or less: 1.6-1.7x faster than fours against 32768 keys).
+  // rows or less: 1.6-1.7x faster than fours against 32768 keys), and over
+  // three when it holds a cluster of three for every unit (chunks of 129-184
+  // rows: 1.4x faster than pairs against 32768 keys).
   Params main_prm = prm, tail_prm = prm;
   int main_grid = grid, tail_units = 0, split = 2;
   if (prm.n_units > grid) {
@@ -1089,6 +1098,8 @@ int launch_impl(const Problem& p, cudaStream_t stream) {
       split = 8;
     else if (prm.n_units <= quads)
       split = 4;
+    else if (prm.n_units <= trios)
+      split = 3;
   }
   if (main_prm.n_units > 0) {
     tc_bf16_kernel<kF32, 1><<<main_grid, threads_of<kF32>(), Layout<kF32>::kSmemAlloc, stream>>>(mk, mv,
@@ -1110,7 +1121,10 @@ int launch_impl(const Problem& p, cudaStream_t stream) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = main_prm.n_units > 0 ? 2 : 1;  // a dependent only of a whole-unit grid
-  auto* tail = split == 8 ? tc_bf16_kernel<kF32, 8> : split == 4 ? tc_bf16_kernel<kF32, 4> : tc_bf16_kernel<kF32, 2>;
+  auto* tail = split == 8   ? tc_bf16_kernel<kF32, 8>
+               : split == 4 ? tc_bf16_kernel<kF32, 4>
+               : split == 3 ? tc_bf16_kernel<kF32, 3>
+                            : tc_bf16_kernel<kF32, 2>;
   if (cudaLaunchKernelEx(&cfg, tail, mk, mv, tail_prm) != cudaSuccess) return ATTN_ELAUNCH;
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ELAUNCH;
 }

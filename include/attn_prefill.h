@@ -104,8 +104,9 @@ extern "C" {
  * grid alone, over clusters of four CTAs (each a quarter of a unit's keys)
  * when the device holds a cluster of four for every unit (chunks of up to 128
  * rows on 152 SMs), or of eight when it holds a cluster of eight for every
- * unit and the longest sees 1024 keys or more (chunks of up to 32 rows). None
- * of it needs device memory.
+ * unit and the longest sees 1024 keys or more (chunks of up to 32 rows), or
+ * of three when it holds a cluster of three for every unit (chunks of up to
+ * 184 rows). None of it needs device memory.
  */
 int attn_prefill(const float *q, const float *kCache, const float *vCache, float *out,
                  int C, int P, cudaStream_t stream);

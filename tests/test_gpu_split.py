@@ -2,9 +2,9 @@
 guarded output: chunks small enough that every unit is split (the longest unit
 of 256 keys or more, 1024 for the bf16 kernels) over a cluster of eight CTAs
 (chunks of up to 32 rows against 1024 keys or more, 2048 for the bf16
-kernels), of four (at most as many units as the device holds such clusters at
-once: chunks of up to 128 rows on 152 SMs) or over a CTA pair (up to 304
-rows), and chunks
+kernels), of four or of three (at most as many units as the device holds such
+clusters at once: chunks of up to 128 and 184 rows on 152 SMs) or over a CTA
+pair (up to 304 rows), and chunks
 whose last round of units goes to the pair grid (the tail), including a ragged
 last query tile and a paged cache."""
 import numpy as np
@@ -54,7 +54,8 @@ def run(cp, path, inp):
 
 
 # Every unit split (at most 76 units, i.e. C <= 304 rows, on 152 SMs): over
-# clusters of eight up to 32 rows, of four up to 128 rows, over pairs beyond.
+# clusters of eight up to 32 rows, of four up to 128 rows, of three up to 184
+# rows (on a GB300), over pairs beyond.
 @pytest.mark.parametrize("path,C,P", [
     ("attn_prefill", 1, 2048), ("attn_prefill", 33, 2048), ("attn_prefill", 100, 3000),
     ("attn_prefill", 288, 2500), ("attn_prefill_paged", 100, 3000), ("attn_prefill_paged", 17, 4100),
@@ -71,6 +72,9 @@ def run(cp, path, inp):
     # clusters of eight: 1025 keys (17 tiles of 64 over eight CTAs), 2048 keys (16 tiles of 128)
     ("attn_prefill", 32, 3000), ("attn_prefill", 1, 1024), ("attn_prefill_paged", 9, 2500),
     ("attn_prefill_bf16kv", 17, 3000), ("attn_prefill_bf16kv", 1, 2047), ("attn_prefill_bf16x3", 32, 2100),
+    # clusters of three (33-46 units)
+    ("attn_prefill", 160, 2000), ("attn_prefill", 129, 300), ("attn_prefill_paged", 136, 1500),
+    ("attn_prefill_bf16kv", 150, 2500), ("attn_prefill_bf16x3", 129, 1100),
 ])
 def test_every_unit_split(cp, path, C, P):
     run(cp, path, W.edge(C, P, seed=C + P))
