@@ -96,3 +96,14 @@ def test_every_unit_split_max_in_last_tile(cp, variant, path, C):
 ])
 def test_tail_grid_ragged(cp, path, C, P):
     run(cp, path, W.edge(C, P, seed=7))
+
+
+# A last round of 8, 16, 24 or 40 units goes to clusters of eight, four or
+# three (on a GB300) instead of pairs.
+@pytest.mark.parametrize("path,C,P", [
+    ("attn_prefill", 640, 1500), ("attn_prefill", 660, 2000), ("attn_prefill", 768, 1100),
+    ("attn_prefill_paged", 1280, 1500), ("attn_prefill_bf16kv", 1300, 3000), ("attn_prefill_bf16x3", 640, 2500),
+    ("attn_prefill_bf16kv", 760, 1024),
+])
+def test_tail_grid_clusters(cp, path, C, P):
+    run(cp, path, W.edge(C, P, seed=11))
