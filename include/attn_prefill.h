@@ -96,10 +96,11 @@ extern "C" {
  * representable in tf32, and each product accumulates hi*hi + hi*lo + lo*hi in
  * fp32, so the result matches exact fp32 products to about 2^-20 relative.
  * When the last round of units would leave at least half of the SMs idle and
- * every unit sees 1024 keys or more, a
- * second grid of two-CTA clusters takes those units, each pair splitting one
- * along its keys and merging the two partials with the split-K rule (same
- * page, Flash-Decoding and the split-K merge); a chunk with at most half as
+ * every unit sees 1024 keys or more, a second grid of CTA clusters takes those
+ * units, each cluster splitting one along its keys and merging the partials
+ * with the split-K rule (same page, Flash-Decoding and the split-K merge):
+ * clusters of two, or of three, four or eight when the device holds one such
+ * cluster for every unit of that round; a chunk with at most half as
  * many units as SMs and a longest unit of 256 keys or more runs as that split
  * grid alone, over clusters of four CTAs (each a quarter of a unit's keys)
  * when the device holds a cluster of four for every unit (chunks of up to 128
@@ -158,7 +159,7 @@ int attn_prefill_bf16kv(const float *q, const uint16_t *kCache, const uint16_t *
  * finish (serving chunk end to end: 0.351 -> 0.325 ms). Each sub-chunk's rows are exactly
  * those of the device-pointer entry point called on that sub-chunk; against one
  * call on the whole chunk they agree to rounding (that call may split its last
- * round's units over CTA pairs, another summation order).
+ * round's units over CTA clusters, another summation order).
  *
  *   q_host, kCache_host, vCache_host   read; the layouts of attn_prefill
  *                                      (uint16_t bf16 patterns for the
