@@ -1162,6 +1162,16 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
       split = 4;
     else if (prm.n_units <= trios)
       split = 3;
+  } else if (prm.n_units <= 2 * trios && unit_keys(p.P, p.C, (prm.n_qtiles - 1) * kBq, kBq) >= 4096) {
+    // A partial round of more than half as many units as SMs: every unit over
+    // a cluster of three, the clusters running in two waves as the device
+    // frees SMs (measured 1.1-1.4x for chunks of 300-352 rows against
+    // 4096-32768 keys, paged 1.1-1.2x; below that many keys, or with more
+    // units, whole units stay faster).
+    main_prm.n_units = 0;
+    tail_prm.unit_base = 0;
+    tail_units = prm.n_units;
+    split = 3;
   }
   if (main_prm.n_units > 0) {
     if (table)

@@ -1109,6 +1109,16 @@ int launch_impl(const Problem& p, cudaStream_t stream) {
       split = 4;
     else if (prm.n_units <= trios)
       split = 3;
+  } else if (prm.n_units <= 2 * trios && unit_keys(p.P, p.C, (prm.n_qtiles - 1) * kBq, kBq) >= 8192) {
+    // A partial round of more than half as many units as SMs: every unit over
+    // a cluster of three, the clusters running in two waves as the device
+    // frees SMs (measured 1.15-1.38x for chunks of 320-352 rows against
+    // 8192-32768 keys; below that many keys, or with more units, whole units
+    // stay faster).
+    main_prm.n_units = 0;
+    tail_prm.unit_base = 0;
+    tail_units = prm.n_units;
+    split = 3;
   }
   if (main_prm.n_units > 0) {
     tc_bf16_kernel<kF32, 1><<<main_grid, threads_of<kF32>(), Layout<kF32>::kSmemAlloc, stream>>>(mk, mv,

@@ -55,7 +55,8 @@ def run(cp, path, inp):
 
 # Every unit split (at most 76 units, i.e. C <= 304 rows, on 152 SMs): over
 # clusters of eight up to 32 rows, of four up to 128 rows, of three up to 184
-# rows (on a GB300), over pairs beyond.
+# rows (on a GB300), over pairs beyond; and 77-92 units over threes in two
+# waves when the units are long.
 @pytest.mark.parametrize("path,C,P", [
     ("attn_prefill", 1, 2048), ("attn_prefill", 33, 2048), ("attn_prefill", 100, 3000),
     ("attn_prefill", 288, 2500), ("attn_prefill_paged", 100, 3000), ("attn_prefill_paged", 17, 4100),
@@ -75,6 +76,9 @@ def run(cp, path, inp):
     # clusters of three (33-46 units)
     ("attn_prefill", 160, 2000), ("attn_prefill", 129, 300), ("attn_prefill_paged", 136, 1500),
     ("attn_prefill_bf16kv", 150, 2500), ("attn_prefill_bf16x3", 129, 1100),
+    # a partial round of 77-92 units over clusters of three in two waves
+    ("attn_prefill", 320, 4000), ("attn_prefill_paged", 352, 4000), ("attn_prefill_bf16x3", 300, 8000),
+    ("attn_prefill_bf16kv", 340, 8000),
 ])
 def test_every_unit_split(cp, path, C, P):
     run(cp, path, W.edge(C, P, seed=C + P))
