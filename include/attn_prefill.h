@@ -107,7 +107,10 @@ extern "C" {
  * rows on 152 SMs), or of eight when it holds a cluster of eight for every
  * unit and the longest sees 1024 keys or more (chunks of up to 32 rows), or
  * of three when it holds a cluster of three for every unit (chunks of up to
- * 184 rows). None of it needs device memory.
+ * 184 rows); a chunk of up to twice as many units as that, whose longest unit
+ * sees 4096 keys or more (8192 for the bf16 paths), splits every unit over
+ * three CTAs too, the clusters running in two waves. None of it needs device
+ * memory.
  */
 int attn_prefill(const float *q, const float *kCache, const float *vCache, float *out,
                  int C, int P, cudaStream_t stream);
