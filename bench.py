@@ -44,6 +44,7 @@ METRIC_LONG = "attention TFLOP/s at C=2048,P=30720 (32q/8kv heads, d=64) and % o
 UNIT = "TFLOP/s"
 L2_FLUSH_BYTES = 256 << 20
 NUM_SMS = 152
+TRIOS = 46  # clusters of three of the prefill kernels a GB300 holds at once
 
 # Nominal dense tensor rates (PFLOP/s per GPU) used only as ratios to carry the
 # measured bf16 peak over to tf32: bf16 2.25, tf32 1.1.
@@ -263,19 +264,25 @@ def kernel_source_hash(path_name: str) -> str:
 def launches_per_call(path: str, C: int, P: int) -> int:
     """Kernel launches in one call of `path` on a chunk of C rows at offset P:
     the library's own rule for its split-unit grid, on 32-row query tiles x 8
-    KV heads and the device's SMs. A second grid of CTA pairs takes the last
-    round's units when that round would leave more than half of the SMs idle
-    and every unit sees 1024 keys or more. With at most
-    half as many units as SMs, long units are all split in a single grid of
-    pairs instead of the whole-unit grid: still one launch."""
+    KV heads and the device's SMs. A second grid of CTA clusters takes the
+    last round's units when that round would leave at least half of the SMs
+    idle and every unit sees 1024 keys or more, or when it holds more than
+    half as many units as SMs but at most twice the clusters of three the
+    device holds at once (46 on a GB300) and every unit sees 8192 keys or
+    more. A chunk of a single round whose units are all split runs as one
+    grid of clusters instead of the whole-unit grid: still one launch."""
     if path not in ("attn_prefill", "attn_prefill_bf16x3", "attn_prefill_bf16kv"):
         return 1
     units = -(-C // 32) * 8
     if units > NUM_SMS:
         rem = units % NUM_SMS
-        ok = P + min(32, C) >= 1024  # the shortest unit's keys
-        return 2 if rem > 0 and 2 * rem <= (NUM_SMS & ~1) and ok else 1
-    return 1  # one grid: whole units, or (at most half as many units as SMs) all split
+        shortest = P + min(32, C)  # the shortest unit's keys
+        if rem > 0 and 2 * rem <= (NUM_SMS & ~1) and shortest >= 1024:
+            return 2
+        if NUM_SMS // 2 < rem <= 2 * TRIOS and shortest >= 8192:
+            return 2
+        return 1
+    return 1  # one grid: whole units, or all split
 
 
 def profiled_traffic(path_name: str, workload: str):

@@ -1149,6 +1149,15 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
         split = 4;
       else if (rem <= trios)
         split = 3;
+    } else if (rem > num_sms / 2 && rem <= 2 * trios && unit_keys(p.P, p.C, 0, kBq) >= 8192) {
+      // A last round of more than half as many units as SMs: over clusters of
+      // three in two waves, when its units are long (measured 1.06-1.16x for
+      // chunks of 928-1568 rows against 8192-30000 keys; 0.91-1.03x against
+      // 2048-4096).
+      main_prm.n_units = full;
+      tail_prm.unit_base = full;
+      tail_units = rem;
+      split = 3;
     }
   } else if (2 * prm.n_units <= num_sms && unit_keys(p.P, p.C, (prm.n_qtiles - 1) * kBq, kBq) >= 256) {
     // Measured: splitting only some of the units (more than half as many

@@ -100,7 +100,9 @@ extern "C" {
  * units, each cluster splitting one along its keys and merging the partials
  * with the split-K rule (same page, Flash-Decoding and the split-K merge):
  * clusters of two, or of three, four or eight when the device holds one such
- * cluster for every unit of that round; a chunk with at most half as
+ * cluster for every unit of that round (a last round of up to twice as many
+ * units as clusters of three it holds, each seeing 8192 keys or more, goes
+ * to clusters of three in two waves); a chunk with at most half as
  * many units as SMs and a longest unit of 256 keys or more runs as that split
  * grid alone, over clusters of four CTAs (each a quarter of a unit's keys)
  * when the device holds a cluster of four for every unit (chunks of up to 128

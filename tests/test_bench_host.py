@@ -55,6 +55,8 @@ def test_ffma_roofline_is_the_fp32_pipe():
     ("attn_prefill_bf16kv", 2048, 2048, 2),  # the bf16 paths take the same last-round rule
     ("attn_prefill_bf16kv", 2048, 30720, 2),
     ("attn_decode_paged", 16, 16384, 1),
+    ("attn_prefill", 928, 8192, 2),       # a last round of 80 units over threes in two waves
+    ("attn_prefill", 928, 4096, 1),       # the same units too short for it: whole units
 ])
 def test_launches_per_call(path, C, P, launches):
     assert bench.launches_per_call(path, C, P) == launches

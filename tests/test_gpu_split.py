@@ -103,11 +103,14 @@ def test_tail_grid_ragged(cp, path, C, P):
 
 
 # A last round of 8, 16, 24 or 40 units goes to clusters of eight, four or
-# three (on a GB300) instead of pairs.
+# three (on a GB300) instead of pairs, and one of 77-92 long units to threes
+# in two waves.
 @pytest.mark.parametrize("path,C,P", [
     ("attn_prefill", 640, 1500), ("attn_prefill", 660, 2000), ("attn_prefill", 768, 1100),
     ("attn_prefill_paged", 1280, 1500), ("attn_prefill_bf16kv", 1300, 3000), ("attn_prefill_bf16x3", 640, 2500),
     ("attn_prefill_bf16kv", 760, 1024),
+    # a last round of 80 or 88 long units over threes in two waves
+    ("attn_prefill", 928, 8500), ("attn_prefill_bf16kv", 960, 8200),
 ])
 def test_tail_grid_clusters(cp, path, C, P):
     run(cp, path, W.edge(C, P, seed=11))
