@@ -67,9 +67,12 @@ def parse_args():
                     choices=["attn_prefill", "attn_prefill_bf16x3", "attn_prefill_ffma", "attn_reference_prefill"])
     ap.add_argument("--kv", choices=["fp32", "bf16"], default="fp32",
                     help="bf16: the K/V cache in bf16 (attn_prefill_bf16kv)")
-    ap.add_argument("--workload", choices=["serve", "long", "decode", "matrix"], default="serve",
-                    help="decode: one decode step of 16 sequences x 16384 cached tokens (paged); "
+    ap.add_argument("--workload", choices=["serve", "long", "chunk", "decode", "matrix"], default="serve",
+                    help="chunk: a chunk of --chunk rows against --prefix cached keys (uniform inputs); "
+                         "decode: one decode step of 16 sequences x 16384 cached tokens (paged); "
                          "matrix: the three-kernel score-matrix pipeline at T = 512, 1024, 2048")
+    ap.add_argument("--chunk", type=int, default=64, help="C of --workload chunk")
+    ap.add_argument("--prefix", type=int, default=32768, help="P of --workload chunk")
     ap.add_argument("--paged", action="store_true",
                     help="time attn_prefill_paged on the same workload scattered into shuffled 16-token pages")
     ap.add_argument("--seed", type=int, default=1)
@@ -88,20 +91,31 @@ def parse_args():
     return args
 
 
-def make_workload(name: str, seed: int):
+def make_workload(name: str, seed: int, C: int = 0, P: int = 0):
     if name == "serve":
         inp = W.serve(seed)
         desc = "serving chunk C=2048 P=2048, 32q/8kv, d=64, fp32 uniform[-1,1), 64 planted 4.0 positions"
+    elif name == "chunk":
+        inp = W.make_inputs(C, P, seed, "uniform", name=f"chunk C={C} P={P}")
+        desc = f"chunk C={C} P={P}, 32q/8kv, d=64, fp32 uniform[-1,1)"
     else:
         inp = W.long_prefix(seed)
         desc = "long cached prefix C=2048 P=30720, 32q/8kv, d=64, fp32 normal(0,0.5) clipped to [-2,2]"
     return inp, desc
 
 
+def metric_for(args) -> str:
+    if args.workload == "serve":
+        return METRIC
+    if args.workload == "long":
+        return METRIC_LONG
+    return f"attention TFLOP/s at C={args.chunk},P={args.prefix} (32q/8kv heads, d=64) and % of roofline"
+
+
 def sample_rows_for_cpu(C: int, every: int):
     """Every ``every``-th chunk row, always including the last (the longest)."""
     rows = list(range(every - 1, C, every))
-    if rows[-1] != C - 1:
+    if not rows or rows[-1] != C - 1:
         rows.append(C - 1)
     return rows
 
@@ -375,7 +389,7 @@ def run_reference(args):
         return 0
     import oracle
     oracle.build()
-    inp, desc = make_workload(args.workload, args.seed)
+    inp, desc = make_workload(args.workload, args.seed, args.chunk, args.prefix)
     threads = os.cpu_count() or 1
     # 128 rows per step (every 16th), fewer when the steps asked for would
     # take more than about a minute and a half of host time; the first
@@ -396,7 +410,7 @@ def run_reference(args):
         total_s += dt
     value = total_flops / total_s / 1e12
     sample = f"{len(rows)} of {inp.C} chunk rows (every {every}th + last), all 32 heads, per step"
-    line = {"impl": "reference", "metric": METRIC if args.workload == "serve" else METRIC_LONG,
+    line = {"impl": "reference", "metric": metric_for(args),
             "value": value, "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
@@ -605,7 +619,7 @@ def main():
         if world > 1:
             dist.barrier()
 
-    inp, desc = make_workload(args.workload, args.seed)
+    inp, desc = make_workload(args.workload, args.seed, args.chunk, args.prefix)
     C, P = inp.C, inp.P
     flops = flops_for(C, P)
     dev = torch.device("cuda", torch.cuda.current_device())
@@ -841,7 +855,7 @@ def main():
             peaks["tf32_n128_tflops"] = tensor_peaks["tf32_n128"]["tflops"]
             peaks["bf16_n128_tflops"] = tensor_peaks["bf16_n128"]["tflops"]
         line = {
-            "metric": METRIC if args.workload == "serve" else METRIC_LONG,
+            "metric": metric_for(args),
             "value": round(value, 4), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

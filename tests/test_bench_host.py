@@ -75,3 +75,12 @@ def test_traffic_record_goes_stale_with_its_source(tmp_path, monkeypatch):
     assert bench.profiled_traffic("attn_prefill", "long") is None  # no record for that workload
     (csrc / "tc.cu").write_text("// kernel source changed since the capture\n")
     assert bench.profiled_traffic("attn_prefill", "serve") is None
+
+
+def test_chunk_workload_metric_and_row_sample():
+    import argparse
+    a = argparse.Namespace(workload="chunk", chunk=32, prefix=32768)
+    assert bench.metric_for(a).startswith("attention TFLOP/s at C=32,P=32768 ")
+    assert bench.metric_for(argparse.Namespace(workload="serve", chunk=0, prefix=0)) == bench.METRIC
+    assert bench.sample_rows_for_cpu(32, 64) == [31]  # fewer rows than the stride: the last row
+    assert bench.sample_rows_for_cpu(130, 64) == [63, 127, 129]
