@@ -326,21 +326,24 @@ __device__ __forceinline__ bool split_epilogue(uint8_t* smem, uint32_t lane_tmem
   return true;
 }
 
-// The same for a unit split over a cluster of three, four or eight CTAs. With
-// three or four, ranks 1.. stage their shares in their own Q regions and, once
-// rank 0's last PV has completed (its Q region and K ring are then idle), copy
-// them in bulk into consecutive slots there (rank r into slot r - 1). With eight, ranks 2-4
-// send to rank 0's slots 0-2 and ranks 5-7 to rank 1's; rank 1 merges its
-// three with its own partial and sends that, staged in its idle V ring, to
-// rank 0's slot 3. A receiver merges its partials with the same rule: m = the
-// largest maximum of a part with tiles, each part weighted by e^(m_s - m).
-static_assert(kSmemQ + 4 * kShareBytes <= kSmemBar, "four shares fit in the Q region and the K and V rings");
+// The same for a unit split over a cluster of three, four, eight or twelve
+// CTAs. With three or four, ranks 1.. stage their shares in their own Q
+// regions and, once rank 0's last PV has completed (its Q region and K and V
+// rings are then idle), copy them in bulk into consecutive slots there (rank
+// r into slot r - 1). With eight, ranks 2-4 send to rank 0's slots 0-2 and
+// ranks 5-7 to rank 1's; rank 1 merges its three with its own partial and
+// sends that, staged in its idle V ring, to rank 0's slot 3. With twelve,
+// ranks 4-11 send to ranks 0-3 two each ((r - 4) / 2, slot (r - 4) mod 2);
+// ranks 1-3 merge theirs and send to rank 0's slots 2-4. A receiver merges
+// its partials with the same rule: m = the largest maximum of a part with
+// tiles, each part weighted by e^(m_s - m).
+static_assert(kSmemQ + 5 * kShareBytes <= kSmemBar, "five shares fit in the Q region and the K and V rings");
 template <int kSplit>
 __device__ __forceinline__ bool split_epilogue_many(uint8_t* smem, uint32_t lane_tmem, int n, bool has,
                                                     const Bars& bars, const Params& prm, volatile int* abort_flag,
                                                     uint32_t rank, int row, float m_ref, float l, float c,
                                                     bool store, float* dst) {
-  static_assert(kSplit == 3 || kSplit == 4 || kSplit == 8, "clusters of three, four or eight");
+  static_assert(kSplit == 3 || kSplit == 4 || kSplit == 8 || kSplit == 12, "clusters of three, four, eight or twelve");
   float o[64];
   if (has) {
     const int pb = (n - 1) % kNumS;
@@ -422,7 +425,7 @@ __device__ __forceinline__ bool split_epilogue_many(uint8_t* smem, uint32_t lane
     return true;
   };
   if (rank == 0) {
-    if (!receive(1, kSplit == 8 ? 4 : kSplit - 1)) return false;
+    if (!receive(1, kSplit == 12 ? 5 : kSplit == 8 ? 4 : kSplit - 1)) return false;
     const float inv = 1.f / l;  // > 0: the unit sees at least key 0
     if (store) {
 #pragma unroll
@@ -432,7 +435,13 @@ __device__ __forceinline__ bool split_epilogue_many(uint8_t* smem, uint32_t lane
     }
     return true;
   }
-  if constexpr (kSplit == 8) {
+  if constexpr (kSplit == 12) {
+    if (rank <= 3) {
+      if (!receive(2 * rank + 4, 2)) return false;
+      return send(smem + kSmemV, 0, rank + 1);
+    }
+    return send(share, (rank - 4) >> 1, (rank - 4) & 1);
+  } else if constexpr (kSplit == 8) {
     if (rank == 1) {
       if (!receive(5, 3)) return false;
       return send(smem + kSmemV, 0, 3);
@@ -449,13 +458,18 @@ __device__ __forceinline__ bool split_epilogue_many(uint8_t* smem, uint32_t lane
 // kTail: launched after kMain as clusters of two CTAs; pair p splits unit
 // unit_base + p along its key tiles (rank 0 the first half, rank 1 the rest)
 // and merges the two online-softmax partials through distributed shared memory.
-// kTail3, kTail4, kTail8: the same with clusters of three, four or eight
-// CTAs, each that share of the unit's tiles (small chunks, whose units are too
-// few to fill the SMs as pairs).
-constexpr int kMain = 0, kPaged = 1, kTail = 2, kTail4 = 3, kTail8 = 4, kTail3 = 5;
+// kTail3, kTail4, kTail8, kTail12: the same with clusters of three, four,
+// eight or twelve CTAs, each that share of the unit's tiles (small chunks,
+// whose units are too few to fill the SMs as pairs).
+constexpr int kMain = 0, kPaged = 1, kTail = 2, kTail4 = 3, kTail8 = 4, kTail3 = 5, kTail12 = 6;
 template <int kMode>
 __host__ __device__ constexpr int split_of() {
-  return kMode == kTail ? 2 : kMode == kTail3 ? 3 : kMode == kTail4 ? 4 : kMode == kTail8 ? 8 : 1;
+  return kMode == kTail     ? 2
+         : kMode == kTail3  ? 3
+         : kMode == kTail4  ? 4
+         : kMode == kTail8  ? 8
+         : kMode == kTail12 ? 12
+                            : 1;
 }
 template <int kMode>
 __host__ __device__ constexpr bool is_tail() { return split_of<kMode>() > 1; }
@@ -484,6 +498,7 @@ __device__ __forceinline__ int work_unit(int k, int cta, int grid, const Params&
   else if constexpr (kMode == kTail4) return k == 0 ? prm.unit_base + (cta >> 2) : prm.n_units;
   else if constexpr (kMode == kTail8) return k == 0 ? prm.unit_base + (cta >> 3) : prm.n_units;
   else if constexpr (kMode == kTail3) return k == 0 ? prm.unit_base + cta / 3 : prm.n_units;
+  else if constexpr (kMode == kTail12) return k == 0 ? prm.unit_base + cta / 12 : prm.n_units;
   else return unit_index(k, cta, grid);
 }
 
@@ -1035,6 +1050,7 @@ struct TcDeviceState {
   int quads = 0;   // clusters of four tail CTAs the device holds at once
   int octets = 0;  // clusters of eight
   int trios = 0;   // clusters of three
+  int twelves = 0;  // clusters of twelve
 };
 TcDeviceState g_tc_state[64];
 std::mutex g_tc_state_mu;
@@ -1043,7 +1059,7 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
                    const int* table = nullptr, int num_pages = 0) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ECUDA;
-  int num_sms = 0, quads = 0, octets = 0, trios = 0;
+  int num_sms = 0, quads = 0, octets = 0, trios = 0, twelves = 0;
   {
     std::lock_guard<std::mutex> lock(g_tc_state_mu);
     TcDeviceState& st = g_tc_state[dev];
@@ -1061,8 +1077,15 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
           cudaFuncSetAttribute(tc_kernel<kTail8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc) !=
               cudaSuccess ||
           cudaFuncSetAttribute(tc_kernel<kTail3>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc) !=
+              cudaSuccess ||
+          cudaFuncSetAttribute(tc_kernel<kTail12>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc) !=
               cudaSuccess)
         return ATTN_ECUDA;
+      // Clusters of twelve are a non-portable size: allowed per kernel (on
+      // a device that refuses, no twelve-way split).
+      const bool twelve_ok =
+          cudaFuncSetAttribute(tc_kernel<kTail12>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+      if (!twelve_ok) (void)cudaGetLastError();
       // How many clusters of three, four and eight fit at once (0 when a
       // query fails: no such split then).
       auto clusters_of = [&](int size, void (*kernel)(CUtensorMap, CUtensorMap, Params)) {
@@ -1087,12 +1110,14 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
       st.quads = clusters_of(4, tc_kernel<kTail4>);
       st.octets = clusters_of(8, tc_kernel<kTail8>);
       st.trios = clusters_of(3, tc_kernel<kTail3>);
+      st.twelves = twelve_ok ? clusters_of(12, tc_kernel<kTail12>) : 0;
       st.ready = true;
     }
     num_sms = st.num_sms;
     quads = st.quads;
     octets = st.octets;
     trios = st.trios;
+    twelves = st.twelves;
   }
   alignas(64) CUtensorMap mk, mv;
   const int rows = table ? num_pages * kPage : p.P + p.C;
@@ -1121,7 +1146,10 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
   // SMs: measured 1.4-1.9x faster than pairs against 2000-32768 keys, 1.1-1.2x
   // against 600-1500), and over a cluster of eight when it holds one of those
   // for every unit and the longest unit sees 1024 keys or more (15 on a GB300:
-  // chunks of 32 rows or less, 1.7x faster than fours against 32768 keys),
+  // chunks of 32 rows or less, 1.7x faster than fours against 32768 keys), or
+  // of twelve (a non-portable size, 8 on a GB300) when the longest unit sees
+  // 8192 keys or more (1.1-1.3x faster than eights against 8192-32768 keys,
+  // slower against 1600-2048),
   // and over a cluster of three when it holds one of those for every unit
   // (46: chunks of 129-184 rows, 1.2-1.4x faster than pairs against 3000-32768
   // keys).
@@ -1143,7 +1171,9 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
       // These units too go to the largest clusters the device holds one of for
       // every such unit (measured against pairs, 16 or 24 units over fours:
       // 1.03-1.19x for chunks of 660-1900 rows against 2048-30000 keys).
-      if (rem <= octets && unit_keys(p.P, p.C, 0, kBq) >= 1024)
+      if (rem <= twelves && unit_keys(p.P, p.C, 0, kBq) >= 8192)
+        split = 12;
+      else if (rem <= octets && unit_keys(p.P, p.C, 0, kBq) >= 1024)
         split = 8;
       else if (rem <= quads)
         split = 4;
@@ -1165,7 +1195,9 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
     main_prm.n_units = 0;
     tail_prm.unit_base = 0;
     tail_units = prm.n_units;
-    if (prm.n_units <= octets && unit_keys(p.P, p.C, (prm.n_qtiles - 1) * kBq, kBq) >= 1024)
+    if (prm.n_units <= twelves && unit_keys(p.P, p.C, (prm.n_qtiles - 1) * kBq, kBq) >= 8192)
+      split = 12;
+    else if (prm.n_units <= octets && unit_keys(p.P, p.C, (prm.n_qtiles - 1) * kBq, kBq) >= 1024)
       split = 8;
     else if (prm.n_units <= quads)
       split = 4;
@@ -1207,6 +1239,7 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
   auto* tail = split == 8   ? tc_kernel<kTail8>
                : split == 4 ? tc_kernel<kTail4>
                : split == 3 ? tc_kernel<kTail3>
+               : split == 12 ? tc_kernel<kTail12>
                             : tc_kernel<kTail>;
   if (cudaLaunchKernelEx(&cfg, tail, mk, mv, tail_prm) != cudaSuccess) return ATTN_ELAUNCH;
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ELAUNCH;

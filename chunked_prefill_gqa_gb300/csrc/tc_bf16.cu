@@ -199,6 +199,7 @@ __device__ __forceinline__ int work_unit(int k, int cta, int grid, const Params&
   else if constexpr (kSplit == 4) return k == 0 ? prm.unit_base + (cta >> 2) : prm.n_units;
   else if constexpr (kSplit == 8) return k == 0 ? prm.unit_base + (cta >> 3) : prm.n_units;
   else if constexpr (kSplit == 3) return k == 0 ? prm.unit_base + cta / 3 : prm.n_units;
+  else if constexpr (kSplit == 12) return k == 0 ? prm.unit_base + cta / 12 : prm.n_units;
   else return unit_index(k, cta, grid);
 }
 template <int kSplit>
@@ -206,7 +207,7 @@ __device__ __forceinline__ void unit_range(const Unit& w, uint32_t rank, int* jb
   if constexpr (kSplit == 2) {
     *jb = rank == 0 ? 0 : w.ntiles / 2;
     *je = rank == 0 ? w.ntiles / 2 : w.ntiles;
-  } else if constexpr (kSplit == 3 || kSplit == 4 || kSplit == 8) {
+  } else if constexpr (kSplit == 3 || kSplit == 4 || kSplit == 8 || kSplit == 12) {
     *jb = (int)rank * w.ntiles / kSplit;
     *je = ((int)rank + 1) * w.ntiles / kSplit;
   } else {
@@ -697,9 +698,9 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
       lred[kh * 128 + row] = l;
       if (!pair_sync()) goto softmax_done;
       l += lred[(kh ^ 1) * 128 + row];
-      if constexpr (kSplit == 3 || kSplit == 4 || kSplit == 8) {
-        // A unit split over a cluster of three, four or eight, as over a pair
-        // below.
+      if constexpr (kSplit == 3 || kSplit == 4 || kSplit == 8 || kSplit == 12) {
+        // A unit split over a cluster of three, four, eight or twelve, as over
+        // a pair below.
         // Senders stage their shares in their own K rings; a receiver, once
         // its last PV has completed (its K and V rings are then idle), takes
         // up to three shares in consecutive slots there and folds them into
@@ -707,7 +708,9 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
         // part weighted by e^(m_s - m). Four: ranks 1-3 send to rank 0. Eight:
         // ranks 2-4 send to rank 0 and ranks 5-7 to rank 1; rank 1 then sends
         // its merged partial to rank 0's slot 0, once rank 0 has folded in
-        // its first three. Three: ranks 1-2 send to rank 0.
+        // its first three. Three: ranks 1-2 send to rank 0. Twelve: ranks 4-11
+        // send to ranks 0-3, two each; rank 0 folds in its two, then takes
+        // ranks 1-3's merged partials.
         static_assert(kSmemK + 3 * kShareBytes <= kSmemBar, "three shares fit in the K and V rings");
         float o[32];
         if (has) {
@@ -772,7 +775,7 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
         auto send = [&](uint32_t to, uint32_t slot) -> bool {
           // After a receive, both warps of the row set must have read slot 0's
           // maxima and sums before the kh = 0 warp overwrites them.
-          if (kSplit == 8 && rank == 1 && !pair_sync()) return false;
+          if (((kSplit == 8 && rank == 1) || (kSplit == 12 && rank >= 1 && rank <= 3)) && !pair_sync()) return false;
           float* ml = reinterpret_cast<float*>(share + kShareO);
 #pragma unroll
           for (int i = 0; i < 8; ++i)
@@ -800,7 +803,9 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
         };
         bool ok;
         if (rank == 0) {
-          ok = kSplit == 8 ? (receive(2, 3, 0) && receive(1, 1, 1)) : receive(1, kSplit - 1, 0);
+          ok = kSplit == 12  ? (receive(4, 2, 0) && receive(1, 3, 1))
+               : kSplit == 8 ? (receive(2, 3, 0) && receive(1, 1, 1))
+                             : receive(1, kSplit - 1, 0);
           if (ok && pos < p.C) {
             const float inv = 1.f / l;  // > 0: the unit sees at least key 0
             float* dst = p.out + ((size_t)pos * kHQ + w.g * kGroup + (row & 3)) * kD + kh * 32;
@@ -809,6 +814,9 @@ tc_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
               *reinterpret_cast<float4*>(dst + 4 * i) =
                   make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv, o[4 * i + 3] * inv);
           }
+        } else if (kSplit == 12) {
+          ok = rank <= 3 ? (receive(2 * rank + 4, 2, 0) && send(0, rank - 1))
+                         : send((rank - 4) >> 1, (rank - 4) & 1);
         } else if (kSplit != 8) {
           ok = send(0, rank - 1);
         } else if (rank == 1) {
@@ -993,6 +1001,7 @@ struct DevState {
   int quads[2] = {0, 0};   // per cache type: clusters of four tail CTAs the device holds at once
   int octets[2] = {0, 0};  // and of eight
   int trios[2] = {0, 0};   // and of three
+  int twelves[2] = {0, 0};  // and of twelve
 };
 DevState g_state[64];
 std::mutex g_state_mu;
@@ -1001,7 +1010,7 @@ template <bool kF32>
 int launch_impl(const Problem& p, cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ATTN_ECUDA;
-  int num_sms = 0, quads = 0, octets = 0, trios = 0;
+  int num_sms = 0, quads = 0, octets = 0, trios = 0, twelves = 0;
   {
     std::lock_guard<std::mutex> lock(g_state_mu);
     DevState& st = g_state[dev];
@@ -1017,8 +1026,15 @@ int launch_impl(const Problem& p, cudaStream_t stream) {
           cudaFuncSetAttribute(tc_bf16_kernel<kF32, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)Layout<kF32>::kSmemAlloc) != cudaSuccess ||
           cudaFuncSetAttribute(tc_bf16_kernel<kF32, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)Layout<kF32>::kSmemAlloc) != cudaSuccess ||
+          cudaFuncSetAttribute(tc_bf16_kernel<kF32, 12>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)Layout<kF32>::kSmemAlloc) != cudaSuccess)
         return ATTN_ECUDA;
+      // Clusters of twelve are a non-portable size: allowed per kernel (on
+      // a device that refuses, no twelve-way split).
+      const bool twelve_ok = cudaFuncSetAttribute(tc_bf16_kernel<kF32, 12>,
+                                                  cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+      if (!twelve_ok) (void)cudaGetLastError();
       // How many clusters of three, four and eight fit at once (0 when a
       // query fails: no such split then).
       auto clusters_of = [&](int size, void (*kernel)(CUtensorMap, CUtensorMap, Params)) {
@@ -1043,12 +1059,14 @@ int launch_impl(const Problem& p, cudaStream_t stream) {
       st.quads[kF32] = clusters_of(4, tc_bf16_kernel<kF32, 4>);
       st.octets[kF32] = clusters_of(8, tc_bf16_kernel<kF32, 8>);
       st.trios[kF32] = clusters_of(3, tc_bf16_kernel<kF32, 3>);
+      st.twelves[kF32] = twelve_ok ? clusters_of(12, tc_bf16_kernel<kF32, 12>) : 0;
       st.ready[kF32] = true;
     }
     num_sms = st.num_sms;
     quads = st.quads[kF32];
     octets = st.octets[kF32];
     trios = st.trios[kF32];
+    twelves = st.twelves[kF32];
   }
   alignas(64) CUtensorMap mk, mv;
   int rc = encode_kv_tile_map(p.k, p.P + p.C, kF32, &mk);
@@ -1075,7 +1093,8 @@ int launch_impl(const Problem& p, cudaStream_t stream) {
   // 152 SMs: measured 1.3-1.8x faster than pairs against 4096-32768 keys,
   // 1.1x against 1200-2500), and over eight when it holds a cluster of eight
   // for every unit and the longest unit sees 2048 keys or more (chunks of 32
-  // rows or less: 1.6-1.7x faster than fours against 32768 keys), and over
+  // rows or less: 1.6-1.7x faster than fours against 32768 keys; over twelve,
+  // a non-portable size, from 8192 keys), and over
   // three when it holds a cluster of three for every unit (chunks of 129-184
   // rows: 1.4x faster than pairs against 32768 keys).
   Params main_prm = prm, tail_prm = prm;
@@ -1090,7 +1109,9 @@ int launch_impl(const Problem& p, cudaStream_t stream) {
       // These units too go to the largest clusters the device holds one of for
       // every such unit (measured against pairs, 16 or 24 units over fours:
       // 1.03-1.19x for chunks of 660-1900 rows against 2048-30000 keys).
-      if (rem <= octets && unit_keys(p.P, p.C, 0, kBq) >= 2048)
+      if (rem <= twelves && unit_keys(p.P, p.C, 0, kBq) >= 8192)
+        split = 12;
+      else if (rem <= octets && unit_keys(p.P, p.C, 0, kBq) >= 2048)
         split = 8;
       else if (rem <= quads)
         split = 4;
@@ -1112,7 +1133,9 @@ int launch_impl(const Problem& p, cudaStream_t stream) {
     main_prm.n_units = 0;
     tail_prm.unit_base = 0;
     tail_units = prm.n_units;
-    if (prm.n_units <= octets && unit_keys(p.P, p.C, (prm.n_qtiles - 1) * kBq, kBq) >= 2048)
+    if (prm.n_units <= twelves && unit_keys(p.P, p.C, (prm.n_qtiles - 1) * kBq, kBq) >= 8192)
+      split = 12;
+    else if (prm.n_units <= octets && unit_keys(p.P, p.C, (prm.n_qtiles - 1) * kBq, kBq) >= 2048)
       split = 8;
     else if (prm.n_units <= quads)
       split = 4;
@@ -1152,6 +1175,7 @@ int launch_impl(const Problem& p, cudaStream_t stream) {
   auto* tail = split == 8   ? tc_bf16_kernel<kF32, 8>
                : split == 4 ? tc_bf16_kernel<kF32, 4>
                : split == 3 ? tc_bf16_kernel<kF32, 3>
+               : split == 12 ? tc_bf16_kernel<kF32, 12>
                             : tc_bf16_kernel<kF32, 2>;
   if (cudaLaunchKernelEx(&cfg, tail, mk, mv, tail_prm) != cudaSuccess) return ATTN_ELAUNCH;
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ELAUNCH;

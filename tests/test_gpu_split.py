@@ -1,8 +1,8 @@
 """The split-unit grids against the oracle, every element checked on a poisoned,
 guarded output: chunks small enough that every unit is split (the longest unit
-of 256 keys or more, 1024 for the bf16 kernels) over a cluster of eight CTAs
-(chunks of up to 32 rows against 1024 keys or more, 2048 for the bf16
-kernels), of four or of three (at most as many units as the device holds such
+of 256 keys or more, 1024 for the bf16 kernels) over a cluster of twelve CTAs
+(chunks of up to 32 rows against 8192 keys or more) or eight (against 1024
+keys or more, 2048 for the bf16 kernels), of four or of three (at most as many units as the device holds such
 clusters at once: chunks of up to 128 and 184 rows on 152 SMs) or over a CTA
 pair (up to 304 rows), and chunks
 whose last round of units goes to the pair grid (the tail), including a ragged
@@ -79,6 +79,9 @@ def run(cp, path, inp):
     # a partial round of 77-92 units over clusters of three in two waves
     ("attn_prefill", 320, 4000), ("attn_prefill_paged", 352, 4000), ("attn_prefill_bf16x3", 300, 8000),
     ("attn_prefill_bf16kv", 340, 8000),
+    # clusters of twelve (a non-portable size: up to 32 rows against 8192 keys or more)
+    ("attn_prefill", 32, 8200), ("attn_prefill", 1, 8191), ("attn_prefill_paged", 16, 9000),
+    ("attn_prefill_bf16kv", 32, 8500), ("attn_prefill_bf16x3", 1, 8191),
 ])
 def test_every_unit_split(cp, path, C, P):
     run(cp, path, W.edge(C, P, seed=C + P))
@@ -111,6 +114,8 @@ def test_tail_grid_ragged(cp, path, C, P):
     ("attn_prefill_bf16kv", 760, 1024),
     # a last round of 80 or 88 long units over threes in two waves
     ("attn_prefill", 928, 8500), ("attn_prefill_bf16kv", 960, 8200),
+    # a last round of 8 long units over twelves
+    ("attn_prefill", 640, 8200), ("attn_prefill_bf16kv", 640, 8200),
 ])
 def test_tail_grid_clusters(cp, path, C, P):
     run(cp, path, W.edge(C, P, seed=11))
