@@ -1149,7 +1149,9 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
   // chunks of 32 rows or less, 1.7x faster than fours against 32768 keys), or
   // of twelve (a non-portable size, 8 on a GB300) when the longest unit sees
   // 8192 keys or more (1.1-1.3x faster than eights against 8192-32768 keys,
-  // slower against 1600-2048),
+  // slower against 1600-2048; 16 units, more than the clusters of eight it
+  // holds, go to twelves in two waves from 16384 keys: 1.07-1.18x faster than
+  // fours, slower against 8192),
   // and over a cluster of three when it holds one of those for every unit
   // (46: chunks of 129-184 rows, 1.2-1.4x faster than pairs against 3000-32768
   // keys).
@@ -1199,6 +1201,8 @@ int tc_launch_impl(const Problem& p, cudaStream_t stream, unsigned long long tim
       split = 12;
     else if (prm.n_units <= octets && unit_keys(p.P, p.C, (prm.n_qtiles - 1) * kBq, kBq) >= 1024)
       split = 8;
+    else if (prm.n_units <= 2 * twelves && unit_keys(p.P, p.C, (prm.n_qtiles - 1) * kBq, kBq) >= 16384)
+      split = 12;  // more units than clusters of eight: twelves in two waves (long units only)
     else if (prm.n_units <= quads)
       split = 4;
     else if (prm.n_units <= trios)

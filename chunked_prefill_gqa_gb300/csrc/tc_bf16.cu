@@ -1137,6 +1137,8 @@ int launch_impl(const Problem& p, cudaStream_t stream) {
       split = 12;
     else if (prm.n_units <= octets && unit_keys(p.P, p.C, (prm.n_qtiles - 1) * kBq, kBq) >= 2048)
       split = 8;
+    else if (prm.n_units <= 2 * twelves && unit_keys(p.P, p.C, (prm.n_qtiles - 1) * kBq, kBq) >= 16384)
+      split = 12;  // more units than clusters of eight: twelves in two waves (long units only)
     else if (prm.n_units <= quads)
       split = 4;
     else if (prm.n_units <= trios)

@@ -108,7 +108,7 @@ extern "C" {
  * when the device holds a cluster of four for every unit (chunks of up to 128
  * rows on 152 SMs), or of eight (twelve from 8192 keys) when it holds such a
  * cluster for every unit and the longest sees 1024 keys or more (chunks of up
- * to 32 rows), or
+ * to 32 rows; up to 64 rows over twelves in two waves from 16384 keys), or
  * of three when it holds a cluster of three for every unit (chunks of up to
  * 184 rows); a chunk of up to twice as many units as that, whose longest unit
  * sees 4096 keys or more (8192 for the bf16 paths), splits every unit over

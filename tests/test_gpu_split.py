@@ -82,6 +82,8 @@ def run(cp, path, inp):
     # clusters of twelve (a non-portable size: up to 32 rows against 8192 keys or more)
     ("attn_prefill", 32, 8200), ("attn_prefill", 1, 8191), ("attn_prefill_paged", 16, 9000),
     ("attn_prefill_bf16kv", 32, 8500), ("attn_prefill_bf16x3", 1, 8191),
+    # 16 units against 16384 keys or more: twelves in two waves
+    ("attn_prefill", 64, 16400), ("attn_prefill_bf16kv", 40, 17000),
 ])
 def test_every_unit_split(cp, path, C, P):
     run(cp, path, W.edge(C, P, seed=C + P))
